@@ -1,0 +1,179 @@
+"""Seeded synthetic workloads for split-KV attention (shapes, seeds and input tensors).
+
+This module only *draws* inputs: it holds none of the attention or merge
+arithmetic.  It is the one module that both the CUDA path's callers (tests,
+``bench.py``) and the oracle's callers use, so both sides see the same bytes.
+
+Input recipe (per workload, seed = 1000 + index):
+  * Q, K, V ~ N(0, 1) drawn in float32 with ``torch.Generator(device).manual_seed``
+    and rounded to bfloat16.
+  * fp8 workloads quantise K and V per (batch, KV head, block of ``scale_block``
+    tokens): scale = amax(|x|) / 448, code = e4m3(clamp(x / scale, +-448)) with
+    torch's round-to-nearest-even cast; the fp32 scales are stored [B, Hkv, n_blocks].
+  * Ragged workloads draw seq_len_b uniformly from {S/2, ..., S}; every other
+    workload uses seq_len_b = S.
+  * Every K/V row at a position >= seq_len_b is poisoned with NaN (bf16 0x7FC0,
+    e4m3 0x7F) so that any read past the end of a sequence shows up in the output.
+  * MLA workloads hold one latent buffer [B, 1, S, dk]; V is the view of its first
+    ``dv`` columns (same storage, row stride dk).
+
+Shapes follow the pages' workloads: Llama-405B-like GQA heads (Hq=128, Hkv=8,
+d=128) from the Helix and context-parallel pages, a DeepSeek-style absorbed MLA
+latent (512 + 64 RoPE dims), and the 8-step ring pass-KV prefill chunk.
+"""
+
+from dataclasses import dataclass, replace
+import math
+
+import torch
+
+NO_CAUSAL = 1 << 62  # causal_offset that masks nothing (decode)
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Tq: int
+    Hq: int
+    Hkv: int
+    dk: int
+    dv: int
+    S: int  # KV positions allocated per (batch, KV head)
+    kv_dtype: str = "bf16"  # "bf16" | "fp8_e4m3"
+    scale_block: int = 64
+    n_split: int = 1
+    ragged: bool = False
+    causal_offset: int = NO_CAUSAL
+    softmax_scale: float = 0.0  # 0 -> 1/sqrt(dk)
+    mla: bool = False
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.dk)
+
+    @property
+    def group(self) -> int:
+        return self.Hq // self.Hkv
+
+    def split_bounds(self):
+        """[B][n_split+1] contiguous, equal sequence shards of the allocated S."""
+        row = [(j * self.S) // self.n_split for j in range(self.n_split + 1)]
+        return [list(row) for _ in range(self.B)]
+
+
+# The five workloads, in the order they are numbered (0..4).
+TINY_GQA = Workload("tiny_gqa_decode", B=1, Tq=1, Hq=8, Hkv=2, dk=64, dv=64, S=1024,
+                    n_split=4, seed=1000)
+HELIX_DENSE_128K = Workload("helix_dense_decode_s128k", B=8, Tq=1, Hq=128, Hkv=8, dk=128,
+                            dv=128, S=131072, n_split=1, seed=1001)
+HELIX_KVP8_FP8_1M = Workload("helix_kvp8_fp8_decode_s1m", B=8, Tq=1, Hq=128, Hkv=8, dk=128,
+                             dv=128, S=1 << 20, kv_dtype="fp8_e4m3", scale_block=64,
+                             n_split=8, ragged=True, seed=1002)
+MLA_ABSORBED = Workload("mla_absorbed_decode_s32k", B=16, Tq=1, Hq=128, Hkv=1, dk=576, dv=512,
+                        S=32768, n_split=4, softmax_scale=1.0 / math.sqrt(192.0), mla=True,
+                        seed=1003)
+RING_PREFILL = Workload("ring_prefill_chunk_8x4096", B=1, Tq=4096, Hq=128, Hkv=8, dk=128,
+                        dv=128, S=8 * 4096, n_split=8, causal_offset=7 * 4096, seed=1004)
+
+WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL]
+
+
+def scaled(w: Workload, **kw) -> Workload:
+    """A smaller workload of the same structure (for parity at oracle-friendly sizes)."""
+    if "S" in kw and "causal_offset" not in kw and w.causal_offset != NO_CAUSAL:
+        # keep the Q chunk at the end of the KV so the last split is the diagonal
+        kw["causal_offset"] = kw["S"] - kw.get("Tq", w.Tq)
+    return replace(w, **kw)
+
+
+def _randn(shape, gen, device):
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+
+def _quantize_e4m3_blocks(x, block):
+    """x [n_tok, d] float32 -> (codes uint8 [n_tok, d], scales float32 [ceil(n_tok/block)])."""
+    n_tok, d = x.shape
+    nb = (n_tok + block - 1) // block
+    pad = nb * block - n_tok
+    xp = torch.nn.functional.pad(x, (0, 0, 0, pad)) if pad else x
+    xb = xp.view(nb, block, d)
+    amax = xb.abs().amax(dim=(1, 2))
+    scales = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    y = (xb / scales[:, None, None]).clamp(-E4M3_MAX, E4M3_MAX)
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(nb * block, d)[:n_tok]
+    return codes.contiguous(), scales.float()
+
+
+def make_inputs(w: Workload, device="cpu", poison=True):
+    """Draw every input of a workload on ``device``.
+
+    Returns a dict with
+      q        bf16  [B, Tq, Hq, dk]
+      k, v     bf16  [B, Hkv, S, dk|dv]  or uint8 e4m3 codes of that shape
+               (MLA: k is the latent [B, 1, S, dk] and v a view of its first dv columns)
+      k_scale, v_scale  float32 [B, Hkv, ceil(S/scale_block)] or None
+      seq_lens int32 [B] (on ``device``)
+      seq_lens_host  list[int]
+      split_bounds   list[list[int]]  ([B][n_split+1])
+    """
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    B, Hkv, S = w.B, w.Hkv, w.S
+    q = _randn((B, w.Tq, w.Hq, w.dk), gen, dev).to(torch.bfloat16)
+    if w.ragged:
+        seq = torch.randint(S // 2, S + 1, (B,), generator=gen, device=dev)
+    else:
+        seq = torch.full((B,), S, dtype=torch.int64, device=dev)
+    seq_host = [int(x) for x in seq.cpu().tolist()]
+
+    k_scale = v_scale = None
+    if w.mla:
+        if w.kv_dtype != "bf16":
+            raise ValueError("MLA workloads are bf16")
+        lat = torch.empty((B, 1, S, w.dk), dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            lat[b, 0] = _randn((S, w.dk), gen, dev).to(torch.bfloat16)
+            if poison and seq_host[b] < S:
+                lat[b, 0, seq_host[b]:] = float("nan")
+        k = lat
+        v = lat[..., : w.dv]
+    elif w.kv_dtype == "bf16":
+        k = torch.empty((B, Hkv, S, w.dk), dtype=torch.bfloat16, device=dev)
+        v = torch.empty((B, Hkv, S, w.dv), dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            for g in range(Hkv):
+                k[b, g] = _randn((S, w.dk), gen, dev).to(torch.bfloat16)
+                v[b, g] = _randn((S, w.dv), gen, dev).to(torch.bfloat16)
+            if poison and seq_host[b] < S:
+                k[b, :, seq_host[b]:] = float("nan")
+                v[b, :, seq_host[b]:] = float("nan")
+    elif w.kv_dtype == "fp8_e4m3":
+        nb = (S + w.scale_block - 1) // w.scale_block
+        k = torch.empty((B, Hkv, S, w.dk), dtype=torch.uint8, device=dev)
+        v = torch.empty((B, Hkv, S, w.dv), dtype=torch.uint8, device=dev)
+        k_scale = torch.empty((B, Hkv, nb), dtype=torch.float32, device=dev)
+        v_scale = torch.empty((B, Hkv, nb), dtype=torch.float32, device=dev)
+        for b in range(B):
+            for g in range(Hkv):
+                k[b, g], k_scale[b, g] = _quantize_e4m3_blocks(_randn((S, w.dk), gen, dev), w.scale_block)
+                v[b, g], v_scale[b, g] = _quantize_e4m3_blocks(_randn((S, w.dv), gen, dev), w.scale_block)
+            if poison and seq_host[b] < S:
+                k[b, :, seq_host[b]:] = 0x7F
+                v[b, :, seq_host[b]:] = 0x7F
+    else:
+        raise ValueError(f"unknown kv dtype {w.kv_dtype}")
+
+    return {
+        "q": q,
+        "k": k,
+        "v": v,
+        "k_scale": k_scale,
+        "v_scale": v_scale,
+        "seq_lens": seq.to(torch.int32),
+        "seq_lens_host": seq_host,
+        "split_bounds": w.split_bounds(),
+    }

@@ -1,0 +1,111 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check the pins catch each one.
+
+Each mutant replaces one oracle function for the duration of one pin; the pin must
+then fail.  This shows the pins in ``test_oracle_pins.py`` are strong enough to
+reject the usual slips, not only that the oracle passes them.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as A
+from oracle import formats as F
+import tests.test_oracle_pins as P
+
+_orig_attend = A.attend
+_orig_merge = A.merge_lse
+
+
+def _attend_no_scale(q, k, v, scale, q_pos=None, kv_pos=None):
+    return _orig_attend(q, k, v, 1.0, q_pos, kv_pos)
+
+
+def _attend_causal_off_by_one(q, k, v, scale, q_pos=None, kv_pos=None):
+    if q_pos is not None:
+        q_pos = np.asarray(q_pos) - 1  # t < p instead of t <= p
+    return _orig_attend(q, k, v, scale, q_pos, kv_pos)
+
+
+def _attend_sign_flip(q, k, v, scale, q_pos=None, kv_pos=None):
+    return _orig_attend(-np.asarray(q), k, v, scale, q_pos, kv_pos)
+
+
+def _kv_head_interleaved(h, Hq, Hkv):
+    return h % Hkv
+
+
+def _merge_linear_weights(o_parts, lse_parts):
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    w = lse_parts - lse_parts.min(axis=0) + 1.0  # weights not exponentiated
+    o = (w[..., None] * np.asarray(o_parts)).sum(0) / w.sum(0)[..., None]
+    return o, np.log(np.exp(lse_parts).sum(0))
+
+
+def _merge_lse_without_max(o_parts, lse_parts):
+    o, lse = _orig_merge(o_parts, lse_parts)
+    m = np.asarray(lse_parts, dtype=np.float64).max(axis=0)
+    return o, lse - np.where(np.isfinite(m), m, 0.0)  # dropped the "+ m" term
+
+
+def _e4m3_bias8(codes):
+    c = np.asarray(codes).astype(np.uint8)
+    v = F.__dict__["_orig_e4m3"](c)
+    return v / 2.0
+
+
+def _split_ignores_seq_len(lo, hi, seq_len):
+    return max(lo, 0), hi
+
+
+MUTANTS = [
+    ("attend without softmax scale", [(A, "attend", _attend_no_scale), (oracle, "attend", _attend_no_scale)],
+     [P.test_golden_closed_forms]),
+    ("causal mask off by one", [(A, "attend", _attend_causal_off_by_one)],
+     [P.test_causal_offset_zero_is_dense_lower_triangle]),
+    ("score sign flipped", [(A, "attend", _attend_sign_flip), (oracle, "attend", _attend_sign_flip)],
+     [P.test_golden_closed_forms, P.test_two_tokens_is_a_logistic_blend]),
+    ("interleaved GQA head map", [(A, "kv_head_of", _kv_head_interleaved)],
+     [P.test_gqa_contiguous_groups]),
+    ("merge weights not exponentiated", [(A, "merge_lse", _merge_linear_weights),
+                                         (oracle, "merge_lse", _merge_linear_weights)],
+     [P.test_merge_two_fragments_closed_form_and_empty_split]),
+    ("merged lse drops the max", [(A, "merge_lse", _merge_lse_without_max),
+                                  (oracle, "merge_lse", _merge_lse_without_max)],
+     [P.test_merge_two_fragments_closed_form_and_empty_split]),
+    ("e4m3 exponent bias 8", [(oracle, "e4m3_bits_to_f64", _e4m3_bias8)],
+     [P.test_e4m3_all_codes_match_torch]),
+    ("split not clipped to seq_len", [(A, "_visible_range", _split_ignores_seq_len)],
+     [P.test_split_past_seq_len_is_empty_and_poison_is_never_read]),
+]
+
+
+def _run_pin(fn):
+    import inspect
+    import json
+    import os
+
+    if fn is P.test_golden_closed_forms:
+        cases = json.load(open(os.path.join(P.GOLDEN, "closed_form_attention.json")))["cases"]
+        for c in cases:
+            fn(c)
+    elif "seed" in inspect.signature(fn).parameters:
+        fn(0)
+    else:
+        fn()
+
+
+@pytest.mark.parametrize("name,patches,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, patches, pins, monkeypatch):
+    F.__dict__.setdefault("_orig_e4m3", F.e4m3_bits_to_f64)
+    for mod, attr, repl in patches:
+        monkeypatch.setattr(mod, attr, repl)
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            _run_pin(pin)
+
+
+def test_unmutated_pins_pass():
+    for _, _, pins in MUTANTS:
+        for pin in pins:
+            _run_pin(pin)
