@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark: split-KV decode attention on GB300 (one JSON line on stdout, rank 0).
+
+Default workload: the Helix dense-model decode layer -- B=8, Hq=128, Hkv=8 (group 16),
+d=128, S=131072 bf16 KV per sequence, one new token per sequence, no split (KVP=1),
+bf16 output + fp32 LSE.  One step = one gqa_decode_attn call (split-KV partial kernel
++ LSE merge) over the resident KV cache.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload (the
+attention of a layer shards into independent problems; no data-path collective), the
+timed region is bracketed by barriers, the max time over ranks is taken, and value is
+the KV bytes of all ranks over that time ("scaling": "weak").
+
+The reference arm (--impl reference) times the fp64 CPU oracle on a bounded sample of
+the same workload on this host's cores; it is a deliberately slow correctness
+baseline, not a competitor.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the oracle's BLAS uses every core this process may run on; state it explicitly
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_decode_attention_gqa_gb300 import workloads as W  # noqa: E402
+from mla_decode_attention_gqa_gb300 import roofline as RL  # noqa: E402
+
+METRIC = "decode attn µs/layer & KV-read HBM GB/s (fraction of GB300 peak) at S=128K/1M"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["mla_decode_attention_gqa_gb300/csrc/gqa_partial.cu", "mla_decode_attention_gqa_gb300/csrc/skv_common.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def workload_by_name(name):
+    for w in W.WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in W.WORKLOADS]}")
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if the
+    kernel sources still match the ones that were profiled (else None)."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+        e = rec[workload_name]
+        if e.get("kernel_source_sha") != kernel_source_sha():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(w, budget_s=12.0, max_groups=None):
+    """Time the fp64 oracle on whole (batch, KV head) groups of the workload until the
+    budget is spent; returns (KV bytes processed, seconds, groups, tokens)."""
+    import numpy as np
+    import oracle
+
+    gen = torch.Generator().manual_seed(w.seed)
+    G = w.Hq // w.Hkv
+    bounds = w.split_bounds()[0]
+    done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
+    while elapsed < budget_s and (max_groups is None or groups < max_groups):
+        S = w.S
+        q = torch.randn((1, w.Tq, G, w.dk), generator=gen).to(torch.bfloat16)
+        k = torch.randn((S, w.dk), generator=gen).to(torch.bfloat16)
+        v = torch.randn((S, w.dv), generator=gen).to(torch.bfloat16)
+        if w.kv_dtype == "fp8_e4m3":
+            kc, ks = W._quantize_e4m3_blocks(k.float(), w.scale_block)
+            vc, vs = W._quantize_e4m3_blocks(v.float(), w.scale_block)
+        t0 = time.perf_counter()
+        qf = oracle.bf16_bits_to_f64(q.view(torch.int16).numpy())
+        if w.kv_dtype == "fp8_e4m3":
+            kf = oracle.dequant_e4m3_blocks(kc.numpy(), ks.numpy(), w.scale_block)
+            vf = oracle.dequant_e4m3_blocks(vc.numpy(), vs.numpy(), w.scale_block)
+        else:
+            kf = oracle.bf16_bits_to_f64(k.view(torch.int16).numpy())
+            vf = oracle.bf16_bits_to_f64(v.view(torch.int16).numpy())
+        o, lse = oracle.split_attention(qf, kf[None, None], vf[None, None], [S], [bounds], w.causal_offset, w.scale)
+        oracle.merge_lse(o, lse)
+        elapsed += time.perf_counter() - t0
+        done_bytes += RL.kv_bytes(1, w.dk, w.dv, w.kv_dtype, [S], [bounds], mla=w.mla, scale_block=w.scale_block)
+        groups += 1
+        tokens += S
+    return done_bytes, elapsed, groups, tokens
+
+
+def reference_arm(args, w, ws, rank):
+    if rank != 0:
+        return
+    steps = []
+    bytes_total, secs_total = 0, 0.0
+    sample = None
+    for i in range(args.warmup + args.steps):
+        b, s, g, t = oracle_sample(w, budget_s=0.0, max_groups=1)
+        if i >= args.warmup:
+            steps.append(s)
+            bytes_total += b
+            secs_total += s
+            sample = f"1 (batch, KV head) group of {t} tokens x {w.Tq} rows x {w.Hq // w.Hkv} heads per step"
+    gbs = bytes_total / secs_total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs_total / len(steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def ours_arm(args, w, ws, rank, local):
+    import mla_decode_attention_gqa_gb300 as skv
+
+    dev = torch.device("cuda", local)
+    t0 = time.time()
+    inp = W.make_inputs(w, dev)
+    torch.cuda.synchronize()
+    log(f"[rank {rank}] inputs ready in {time.time() - t0:.1f}s")
+    kw = dict(k_scale=inp["k_scale"], v_scale=inp["v_scale"], softmax_scale=w.scale, scale_block=w.scale_block)
+    bounds = inp["split_bounds"]
+    kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, inp["seq_lens_host"], bounds, mla=w.mla,
+                           scale_block=w.scale_block)
+    flops = RL.attn_flops(w.Tq, w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, w.causal_offset)
+    out = torch.empty((w.B, w.Tq, w.Hq, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Tq, w.Hq), dtype=torch.float32, device=dev)
+
+    def step():
+        skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, out=out,
+                            lse=lse, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if skv.device_error() != 0:
+        raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    start_all = torch.cuda.Event(enable_timing=True)
+    end_all = torch.cuda.Event(enable_timing=True)
+    start_all.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end_all.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    total_ms = start_all.elapsed_time(end_all)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if skv.device_error() != 0:
+        raise RuntimeError("a kernel reported a timed-out wait in the timed region")
+
+    max_total_ms = max_over_ranks(total_ms, ws)
+    all_bytes = sum_over_ranks(float(kv_bytes) * args.steps, ws)
+    value_gbs = all_bytes / (max_total_ms * 1e-3) / 1e9
+    ms_per_step = max_total_ms / args.steps
+
+    # e2e: the public call with host (pinned) inputs; copies in and the result back every step
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for key in ("q", "k", "v", "k_scale", "v_scale", "seq_lens"):
+            t = inp[key]
+            host[key] = None if t is None else t.cpu().pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        dev_bufs = {k2: (None if t is None else torch.empty_like(t, device=dev)) for k2, t in host.items()}
+        del inp
+        torch.cuda.empty_cache()
+
+        def e2e_step():
+            for k2, t in host.items():
+                if t is not None:
+                    dev_bufs[k2].copy_(t, non_blocking=True)
+            skv.gqa_decode_attn(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
+                                w.causal_offset, k_scale=dev_bufs["k_scale"], v_scale=dev_bufs["v_scale"],
+                                softmax_scale=w.scale, scale_block=w.scale_block, out=out, lse=lse)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        e2e_steps = max(1, min(args.steps, 5))
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), ws)
+        e2e_bytes = sum_over_ranks(float(kv_bytes) * e2e_steps, ws)
+        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / e2e_steps, 3)}
+
+    if rank != 0:
+        return
+    peak, peak_kind = hbm_peak()
+    # dominant kernel: the split-KV partial kernel (the merge kernel is ~1% of the step);
+    # its per-launch time is taken as the measured step time, which also holds the merge
+    achieved = kv_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and ws >= 1:
+        b, s, g, t = oracle_sample(w, budget_s=args.cpu_budget)
+        cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle",
+               "sample": f"{g} (batch, KV head) groups x {t // max(g, 1)} tokens, {w.Tq} row(s) x {w.Hq // w.Hkv} heads each, "
+                         f"{s:.1f} s"}
+    line = {
+        "metric": METRIC,
+        "value": round(value_gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "us_per_layer": round(ms_per_step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 KV, bf16 q",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V)",
+        "config": {"workload": w.name, "B": w.B, "Tq": w.Tq, "Hq": w.Hq, "Hkv": w.Hkv, "dk": w.dk, "dv": w.dv,
+                   "S": w.S, "kv_dtype": w.kv_dtype, "n_split": w.n_split,
+                   "l2": "no flush: every step streams %.2f GB of KV, far above the 129 MB L2" % (kv_bytes / 1e9),
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(w.name), "algorithmic_bytes_per_launch": kv_bytes,
+                     "flops_per_launch": flops, "tflops": round(flops / (statistics.mean(step_ms) * 1e-3) / 1e12, 2),
+                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),
+                                   round(max(step_ms), 4)],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=W.HELIX_DENSE_128K.name)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = workload_by_name(args.config)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, w, ws, rank)
+    else:
+        ours_arm(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * splitkv_attn.h -- exact attention over a KV cache split along the sequence, with an
+ * exact log-sum-exp (LSE) merge of the per-split partials.  C ABI of
+ * libsplitkv_attn.so (NVIDIA GB300, sm_103a).
+ *
+ * The operation (cited by web page title and section):
+ *   - "Helix Parallelism: Why Tensor Parallelism Hits a Wall at Million-Token
+ *     Context", section "Sharding the sequence instead": the KV cache is sharded
+ *     along the sequence; attention over each shard yields a partial output plus a
+ *     log-sum-exp per token and query head; the fragments are merged exactly with
+ *     m = max lse, den = sum exp(lse - m), o = sum o * exp(lse - m) / den.
+ *   - "Context Parallelism for Scalable Million-Token Inference" (knowledge note),
+ *     section "Pass-KV keeps queries local and circulates keys and values": the
+ *     same merge over the N ring steps of a prefill chunk; section "A runtime
+ *     heuristic chooses the ring direction": shape(Q) = [T, N_H, D_H] and
+ *     shape(K) = shape(V) = [T+P, N_KV, D_H].
+ *   - "现代大模型推理并行策略总览", section "Transformer 的工程实践": query heads
+ *     map to KV heads in contiguous groups; section "序列布局": the causal mask is
+ *     decided by original token positions.
+ *
+ * On one GPU the KVP shards / ring steps are the splits of one call; the merge is
+ * the reduction the pages' All-to-All feeds.
+ *
+ * Conventions for every entry point
+ *   - Device pointers are owned by the caller and must stay valid until the work
+ *     queued on `stream` (a cudaStream_t, NULL = legacy default stream) completes.
+ *     The library allocates no memory.  Calls are asynchronous on `stream`.
+ *   - Errors are returned, never raised: argument errors are detected on the host
+ *     before anything is launched; a CUDA error maps to SKV_ECUDA.  The text of
+ *     the last error of the calling thread is splitkv_last_error().
+ *   - Query head h reads KV head h / (Hq / Hkv).
+ *   - Visibility: query row i of sequence b sees KV position t iff
+ *       bounds[b][j] <= t < bounds[b][j+1]   (its split j),
+ *       t < seq_lens[b]  (and t < S_max), and
+ *       t <= causal_offset + i.
+ *     Decode passes a causal_offset >= S_max (SKV_NO_CAUSAL) so nothing is masked;
+ *     a prefill chunk whose first row sits at global position P passes P.
+ *   - Partials: o is normalised by its own softmax denominator and lse is the
+ *     natural log of that denominator over scaled scores (softmax_scale * q.k).
+ *     A split with no visible token has o = 0 and lse = -inf.
+ *   - fp8-e4m3 KV: value = e4m3(code) * scale[b][kv_head][t / scale_block].
+ *   - MLA (latent KV): Hkv = 1, dk = 576 (512 latent + 64 rope), dv = 512 and
+ *     v_cache = k_cache with the same strides (V is the first 512 latent columns).
+ */
+#ifndef SPLITKV_ATTN_H
+#define SPLITKV_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SKV_OK = 0,
+  SKV_EINVAL = -1,       /* invalid argument: null pointer, shape, stride, alignment, bounds */
+  SKV_EUNSUPPORTED = -2, /* valid but not implemented (head dims, dtype combination) */
+  SKV_ECUDA = -3,        /* CUDA error while launching; see splitkv_last_error() */
+  SKV_EWORKSPACE = -4    /* workspace missing or smaller than the matching *_workspace_size */
+} skv_status;
+
+typedef enum { SKV_KV_BF16 = 0, SKV_KV_FP8_E4M3 = 1 } skv_kv_dtype;
+
+/* causal_offset that masks nothing */
+#define SKV_NO_CAUSAL ((int64_t)1 << 62)
+
+/* Problem description shared by attn_partial and gqa_decode_attn. */
+typedef struct {
+  int32_t B;            /* sequences in the batch */
+  int32_t Tq;           /* query rows per sequence (1 for decode) */
+  int32_t Hq;           /* query heads */
+  int32_t Hkv;          /* KV heads, Hq % Hkv == 0 */
+  int32_t dk;           /* query/key head dim */
+  int32_t dv;           /* value head dim */
+  int64_t S_max;        /* KV positions allocated per (sequence, KV head), < 2^31 */
+  float softmax_scale;  /* multiplies q.k (e.g. 1/sqrt(dk)) */
+  int32_t kv_dtype;     /* skv_kv_dtype */
+  int32_t scale_block;  /* fp8 only: tokens per scale block, a positive multiple of 64 */
+  int64_t q_strides[3]; /* q: bf16, element strides of (b, query row, head); dim stride 1 */
+  int64_t k_strides[3]; /* k_cache: element strides of (b, KV head, token); dim stride 1 */
+  int64_t v_strides[3]; /* v_cache: same for V */
+} skv_desc;
+
+/* Library version: (major << 16) | minor. */
+int32_t splitkv_version(void);
+
+/* Text of the calling thread's last error ("" if none).  Valid until the thread's next call. */
+const char* splitkv_last_error(void);
+
+/*
+ * Read and clear the device error word of the current device (blocking: waits for all
+ * work on the device).  *code = 0 if no kernel gave up a bounded wait, else a bitmask
+ * (1: a consumer waited too long for a tile, 2: the loader waited too long for a free
+ * stage, 4: a final drain waited too long).  Every wait in the kernels has a time limit.
+ */
+skv_status splitkv_device_error(uint32_t* code);
+
+/*
+ * attn_partial -- one partial attention output per split.
+ *
+ *   q            bf16, logical [B][Tq][Hq][dk] with desc->q_strides
+ *   k_cache      bf16 or e4m3 codes, logical [B][Hkv][S_max][dk] with desc->k_strides
+ *   v_cache      same for V ([..][dv], desc->v_strides)
+ *   k_scale      fp8: fp32 [B][Hkv][ceil(S_max / scale_block)] contiguous; NULL for bf16
+ *   v_scale      fp8: same layout; NULL for bf16
+ *   seq_lens     DEVICE int32 [B]; 0 <= seq_lens[b] <= S_max
+ *   split_bounds HOST int32 [B][n_split + 1], non-decreasing per row, bounds[b][0] >= 0;
+ *                B * (n_split + 1) <= 2048.  Copied at the call (by value into the launch).
+ *   n_split      >= 1
+ *   causal_offset  see Visibility above
+ *   out_partial  fp32 [n_split][B][Tq][Hq][dv] contiguous, 16-byte aligned
+ *   lse_partial  fp32 [n_split][B][Tq][Hq] contiguous
+ *   workspace    device scratch of at least attn_partial_workspace_size() bytes (256-byte
+ *                aligned); may be NULL when that size is 0.  Used when long splits are cut
+ *                into chunks to fill the GPU; the chunks are merged back per split.
+ * Alignment: q, k_cache, v_cache 16-byte aligned; q strides multiples of 8 elements; K/V
+ * token/head/batch strides multiples of 16 bytes.
+ */
+skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
+                                       size_t* bytes);
+skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                        const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
+                        float* lse_partial, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_merge_lse -- exact LSE merge of n_split partials (the merge of the pages above).
+ *
+ *   out_partials fp32 [n_split][B][Tq][Hq][dv], lse_partials fp32 [n_split][B][Tq][Hq] (device)
+ *   out          bf16 [B][Tq][Hq][dv];  lse  fp32 [B][Tq][Hq]  (device)
+ * Rows whose partials are all empty (lse = -inf) get out = 0, lse = -inf.  dv must be a
+ * multiple of 4; pointers 16-byte aligned (out 8-byte).
+ */
+skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, int32_t dv,
+                          const float* out_partials, const float* lse_partials, void* out, float* lse,
+                          void* stream);
+
+/*
+ * gqa_decode_attn -- split-KV attention and the merge in one call: the exact attention of
+ * every query row over the union of its splits, written as bf16 out [B][Tq][Hq][dv] and
+ * fp32 lse [B][Tq][Hq] (contiguous).  Arguments as attn_partial; the per-split / per-chunk
+ * partials live in the caller's workspace of at least gqa_decode_attn_workspace_size() bytes.
+ */
+skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
+                                          size_t* bytes);
+skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                           const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_ATTN_H */

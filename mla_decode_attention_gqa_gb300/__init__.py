@@ -1,0 +1,301 @@
+"""Python binding of libsplitkv_attn.so: exact split-KV attention with an LSE merge on GB300.
+
+Thin ctypes marshalling over the C ABI declared in ``include/splitkv_attn.h``:
+every step of the computation runs in the library's CUDA kernels; PyTorch only
+provides device memory (outputs, workspace) and the current CUDA stream.  There is
+no CPU fallback: the first call loads the library and raises if it is missing, and
+every call fails if its tensors are not on a CUDA device.
+
+Entry points (same names as the C ABI):
+  attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out_partial, lse_partial)
+  attn_merge_lse(out_partials, lse_partials) -> (out, lse)
+  gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out, lse)
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .workloads import NO_CAUSAL
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsplitkv_attn.so")
+
+SKV_OK, SKV_EINVAL, SKV_EUNSUPPORTED, SKV_ECUDA, SKV_EWORKSPACE = 0, -1, -2, -3, -4
+SKV_KV_BF16, SKV_KV_FP8_E4M3 = 0, 1
+_STATUS = {0: "SKV_OK", -1: "SKV_EINVAL", -2: "SKV_EUNSUPPORTED", -3: "SKV_ECUDA", -4: "SKV_EWORKSPACE"}
+
+# Every symbol declared in include/splitkv_attn.h.
+EXPORTED_SYMBOLS = (
+    "splitkv_version",
+    "splitkv_last_error",
+    "splitkv_device_error",
+    "attn_partial_workspace_size",
+    "attn_partial",
+    "attn_merge_lse",
+    "gqa_decode_attn_workspace_size",
+    "gqa_decode_attn",
+)
+
+
+class SkvDesc(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32),
+        ("Tq", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("dk", ctypes.c_int32),
+        ("dv", ctypes.c_int32),
+        ("S_max", ctypes.c_int64),
+        ("softmax_scale", ctypes.c_float),
+        ("kv_dtype", ctypes.c_int32),
+        ("scale_block", ctypes.c_int32),
+        ("q_strides", ctypes.c_int64 * 3),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3),
+    ]
+
+
+class SplitKVError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m mla_decode_attention_gqa_gb300.build` "
+            "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(SkvDesc)
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    lib.splitkv_version.restype = I32
+    lib.splitkv_last_error.restype = ctypes.c_char_p
+    lib.splitkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.splitkv_device_error.restype = I32
+    for name in ("attn_partial_workspace_size", "gqa_decode_attn_workspace_size"):
+        f = getattr(lib, name)
+        f.argtypes = [D, I32P, I32, ctypes.POINTER(SZ)]
+        f.restype = I32
+    common = [D, P, P, P, P, P, P, I32P, I32, I64]
+    lib.attn_partial.argtypes = common + [P, P, P, SZ, P]
+    lib.attn_partial.restype = I32
+    lib.gqa_decode_attn.argtypes = common + [P, P, P, SZ, P]
+    lib.gqa_decode_attn.restype = I32
+    lib.attn_merge_lse.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P]
+    lib.attn_merge_lse.restype = I32
+    return lib
+
+
+class _LazyLib:
+    """Loads the shared library at first use (so that the pure-host modules of this
+    package - workloads, roofline - import without it); a missing library raises."""
+
+    _handle = None
+
+    def __getattr__(self, name):
+        if _LazyLib._handle is None:
+            _LazyLib._handle = _load()
+        return getattr(_LazyLib._handle, name)
+
+
+_lib = _LazyLib()
+
+
+def load_library():
+    """Load (once) and return the ctypes handle of libsplitkv_attn.so."""
+    _lib.splitkv_version  # noqa: B018 - forces the load
+    return _LazyLib._handle
+
+
+def version():
+    v = _lib.splitkv_version()
+    return (v >> 16, v & 0xFFFF)
+
+
+def last_error():
+    return _lib.splitkv_last_error().decode()
+
+
+def device_error():
+    """Read and clear the device error word (blocking); 0 means no kernel gave up a wait."""
+    code = ctypes.c_uint32(0)
+    _check(_lib.splitkv_device_error(ctypes.byref(code)))
+    return int(code.value)
+
+
+def _check(status):
+    if status != SKV_OK:
+        raise SplitKVError(status, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("split-KV attention runs on CUDA tensors only (no CPU path)")
+
+
+def _kv_dtype(k):
+    if k.dtype == torch.bfloat16:
+        return SKV_KV_BF16
+    if k.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return SKV_KV_FP8_E4M3
+    raise ValueError(f"unsupported KV dtype {k.dtype}: bf16 or e4m3 codes (uint8 / float8_e4m3fn)")
+
+
+def make_desc(q, k_cache, v_cache, softmax_scale=None, scale_block=64):
+    """Describe q [B,Tq,Hq,dk] and k/v caches [B,Hkv,S,d] (any strides, unit last dim)."""
+    if q.dim() != 4 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B,Tq,Hq,dk] and caches [B,Hkv,S,d]")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("q must be bf16")
+    for t in (q, k_cache, v_cache):
+        if t.stride(-1) != 1:
+            raise ValueError("the head dim must be unit-stride")
+    B, Tq, Hq, dk = q.shape
+    Bk, Hkv, S, dk2 = k_cache.shape
+    if Bk != B or dk2 != dk or v_cache.shape[:3] != k_cache.shape[:3]:
+        raise ValueError("q / k_cache / v_cache shapes disagree")
+    d = SkvDesc()
+    d.B, d.Tq, d.Hq, d.Hkv, d.dk, d.dv = B, Tq, Hq, Hkv, dk, v_cache.shape[3]
+    d.S_max = S
+    d.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(dk)
+    d.kv_dtype = _kv_dtype(k_cache)
+    d.scale_block = scale_block
+    for i in range(3):
+        d.q_strides[i] = q.stride(i)
+        d.k_strides[i] = k_cache.stride(i)
+        d.v_strides[i] = v_cache.stride(i)
+    return d
+
+
+def _bounds_array(split_bounds, B):
+    rows = [list(map(int, r)) for r in split_bounds]
+    if len(rows) == 1 and B > 1:
+        rows = rows * B
+    if len(rows) != B or len({len(r) for r in rows}) != 1:
+        raise ValueError("split_bounds must be [B][n_split+1] (or one row shared by every sequence)")
+    n_split = len(rows[0]) - 1
+    flat = (ctypes.c_int32 * (B * (n_split + 1)))(*[x for r in rows for x in r])
+    return flat, n_split
+
+
+_ws_cache = {}
+
+
+def _workspace(nbytes, device):
+    """A reusable device scratch buffer of at least nbytes (torch allocation)."""
+    if nbytes == 0:
+        return None
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale, scale_block):
+    _require_cuda(q, k_cache, v_cache, seq_lens, k_scale, v_scale)
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    d = make_desc(q, k_cache, v_cache, softmax_scale, scale_block)
+    bounds, n_split = _bounds_array(split_bounds, d.B)
+    for s in (k_scale, v_scale):
+        if s is not None and (s.dtype != torch.float32 or not s.is_contiguous()):
+            raise ValueError("scales must be contiguous float32 [B,Hkv,n_blocks]")
+    return d, bounds, n_split
+
+
+def attn_partial_workspace_size(desc, bounds, n_split):
+    n = ctypes.c_size_t(0)
+    _check(_lib.attn_partial_workspace_size(ctypes.byref(desc), bounds, n_split, ctypes.byref(n)))
+    return int(n.value)
+
+
+def gqa_decode_attn_workspace_size(desc, bounds, n_split):
+    n = ctypes.c_size_t(0)
+    _check(_lib.gqa_decode_attn_workspace_size(ctypes.byref(desc), bounds, n_split, ctypes.byref(n)))
+    return int(n.value)
+
+
+def attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_CAUSAL, k_scale=None,
+                 v_scale=None, softmax_scale=None, scale_block=64, out_partial=None, lse_partial=None):
+    """Per-split partial attention: returns (out_partial fp32 [n_split,B,Tq,Hq,dv], lse fp32 [n_split,B,Tq,Hq])."""
+    d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
+                               scale_block)
+    dev = q.device
+    if out_partial is None:
+        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    ws = _workspace(nbytes, dev)
+    _check(_lib.attn_partial(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                             _ptr(seq_lens), bounds, n_split, int(causal_offset), _ptr(out_partial),
+                             _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
+    return out_partial, lse_partial
+
+
+def attn_merge_lse(out_partials, lse_partials, out=None, lse=None):
+    """Exact LSE merge over the first axis: returns (out bf16 [B,Tq,Hq,dv], lse fp32 [B,Tq,Hq])."""
+    _require_cuda(out_partials, lse_partials)
+    if out_partials.dtype != torch.float32 or lse_partials.dtype != torch.float32:
+        raise ValueError("partials must be float32")
+    if not (out_partials.is_contiguous() and lse_partials.is_contiguous()):
+        raise ValueError("partials must be contiguous")
+    n_split, B, Tq, Hq, dv = out_partials.shape
+    if out is None:
+        out = torch.empty((B, Tq, Hq, dv), dtype=torch.bfloat16, device=out_partials.device)
+    if lse is None:
+        lse = torch.empty((B, Tq, Hq), dtype=torch.float32, device=out_partials.device)
+    _check(_lib.attn_merge_lse(n_split, B, Tq, Hq, dv, _ptr(out_partials), _ptr(lse_partials), _ptr(out), _ptr(lse),
+                               _stream()))
+    return out, lse
+
+
+def gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_CAUSAL, k_scale=None,
+                    v_scale=None, softmax_scale=None, scale_block=64, out=None, lse=None, workspace=None):
+    """Split-KV attention plus merge in one call: returns (out bf16 [B,Tq,Hq,dv], lse fp32 [B,Tq,Hq])."""
+    d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
+                               scale_block)
+    dev = q.device
+    if out is None:
+        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
+    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    _check(_lib.gqa_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                _ptr(seq_lens), bounds, n_split, int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
+                                nbytes if workspace is None else workspace.numel(), _stream()))
+    return out, lse
+
+
+__all__ = [
+    "attn_partial",
+    "attn_merge_lse",
+    "gqa_decode_attn",
+    "make_desc",
+    "device_error",
+    "last_error",
+    "version",
+    "SplitKVError",
+    "SkvDesc",
+    "LIB_PATH",
+    "load_library",
+    "EXPORTED_SYMBOLS",
+    "NO_CAUSAL",
+]

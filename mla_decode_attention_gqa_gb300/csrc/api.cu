@@ -1,0 +1,409 @@
+// C-ABI entry points of libsplitkv_attn.so: argument validation, work decomposition,
+// TMA descriptor set-up and dispatch to the kernels.  See include/splitkv_attn.h for
+// the contract of every call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/splitkv_attn.h"
+#include "skv_internal.h"
+
+// Device error word written by kernels whose bounded waits gave up.
+__device__ unsigned int g_skv_device_error = 0;
+
+namespace {
+
+using namespace skv;
+
+thread_local std::string t_last_error;
+
+skv_status fail(skv_status code, const std::string& msg) {
+  t_last_error = msg;
+  return code;
+}
+
+skv_status cuda_fail(cudaError_t e, const char* where) {
+  t_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return SKV_ECUDA;
+}
+
+constexpr int kMaxDevices = 64;
+
+unsigned int* device_error_word(cudaError_t* err) {
+  static unsigned int* cache[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_skv_device_error);
+    if (*err != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(ptr);
+  }
+  return cache[dev];
+}
+
+// SM count and resident CTAs per SM of a kernel variant (fallback when no device is
+// visible, e.g. for size queries on a build host: a GB300's 152 SMs, 2 CTAs per SM).
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn(cudaError_t* err) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  static cudaError_t once_err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    once_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (once_err == cudaSuccess && q != cudaDriverEntryPointSuccess) once_err = cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  *err = once_err;
+  return fn;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ plan of a call
+
+struct Plan {
+  GqaVariant variant;
+  int rows_per_cta = 0;
+  int m_tiles = 1;
+  int n_chunk = 1;
+  int chunk_tiles = 1;
+  int64_t n_items = 0;
+  int n_part = 0;  // n_split * n_chunk
+};
+
+bool is_gqa_shape(const skv_desc* d) {
+  if (d->dk != d->dv) return false;
+  if (d->kv_dtype == SKV_KV_BF16) return d->dk == 64 || d->dk == 128;
+  return d->dk == 128;
+}
+
+skv_status validate(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
+  if (!d) return fail(SKV_EINVAL, "desc is NULL");
+  if (d->B <= 0 || d->Tq <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->dk <= 0 || d->dv <= 0)
+    return fail(SKV_EINVAL, "B, Tq, Hq, Hkv, dk, dv must be positive");
+  if (d->Hq % d->Hkv) return fail(SKV_EINVAL, "Hq must be a multiple of Hkv");
+  if (d->S_max <= 0 || d->S_max >= (int64_t(1) << 31)) return fail(SKV_EINVAL, "S_max must be in [1, 2^31)");
+  if (!std::isfinite(d->softmax_scale) || d->softmax_scale == 0.f)
+    return fail(SKV_EINVAL, "softmax_scale must be finite and non-zero");
+  if (d->kv_dtype != SKV_KV_BF16 && d->kv_dtype != SKV_KV_FP8_E4M3) return fail(SKV_EINVAL, "unknown kv_dtype");
+  if (d->kv_dtype == SKV_KV_FP8_E4M3 && (d->scale_block <= 0 || d->scale_block % kTileN))
+    return fail(SKV_EINVAL, "scale_block must be a positive multiple of 64 for fp8 KV");
+  if (n_split < 1) return fail(SKV_EINVAL, "n_split must be >= 1");
+  if (static_cast<int64_t>(d->B) * (n_split + 1) > kMaxBounds)
+    return fail(SKV_EINVAL, "B * (n_split + 1) must be <= 2048");
+  if (!bounds) return fail(SKV_EINVAL, "split_bounds is NULL");
+  for (int b = 0; b < d->B; ++b) {
+    const int32_t* r = bounds + static_cast<int64_t>(b) * (n_split + 1);
+    if (r[0] < 0) return fail(SKV_EINVAL, "split_bounds must be >= 0");
+    for (int j = 0; j < n_split; ++j)
+      if (r[j + 1] < r[j]) return fail(SKV_EINVAL, "split_bounds must be non-decreasing per sequence");
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (d->q_strides[i] < 0 || d->k_strides[i] < 0 || d->v_strides[i] < 0)
+      return fail(SKV_EINVAL, "strides must be non-negative");
+    if (d->q_strides[i] % 8) return fail(SKV_EINVAL, "q strides must be multiples of 8 elements (16 bytes)");
+  }
+  const int esz = d->kv_dtype == SKV_KV_FP8_E4M3 ? 1 : 2;
+  for (int i = 0; i < 3; ++i) {
+    if ((d->k_strides[i] * esz) % 16 || (d->v_strides[i] * esz) % 16)
+      return fail(SKV_EINVAL, "K/V strides must be multiples of 16 bytes");
+  }
+  if (d->k_strides[2] < d->dk || d->v_strides[2] < d->dv)
+    return fail(SKV_EINVAL, "K/V token stride must cover a whole head row");
+  if (!is_gqa_shape(d)) {
+    return fail(SKV_EUNSUPPORTED, "unsupported head dims / dtype: supported are bf16 dk=dv in {64,128} and "
+                                  "fp8-e4m3 dk=dv=128");
+  }
+  return SKV_OK;
+}
+
+skv_status validate_ptrs(const skv_desc* d, const void* q, const void* k, const void* v, const float* ks,
+                         const float* vs, const int32_t* seq_lens) {
+  if (!q || !k || !v || !seq_lens) return fail(SKV_EINVAL, "q, k_cache, v_cache and seq_lens must be non-NULL");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
+    return fail(SKV_EINVAL, "q, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(seq_lens, 4)) return fail(SKV_EINVAL, "seq_lens must be 4-byte aligned");
+  if (d->kv_dtype == SKV_KV_FP8_E4M3) {
+    if (!ks || !vs) return fail(SKV_EINVAL, "fp8 KV needs k_scale and v_scale");
+    if (!aligned(ks, 4) || !aligned(vs, 4)) return fail(SKV_EINVAL, "scales must be 4-byte aligned");
+  }
+  return SKV_OK;
+}
+
+Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
+  Plan pl;
+  const int G = d->Hq / d->Hkv;
+  const bool fp8 = d->kv_dtype == SKV_KV_FP8_E4M3;
+  const bool decode = static_cast<int64_t>(d->Tq) * G <= 16;
+  if (fp8)
+    pl.variant = decode ? GqaVariant::kFp8D128Decode : GqaVariant::kFp8D128Prefill;
+  else if (d->dk == 64)
+    pl.variant = decode ? GqaVariant::kBf16D64Decode : GqaVariant::kBf16D64Prefill;
+  else
+    pl.variant = decode ? GqaVariant::kBf16D128Decode : GqaVariant::kBf16D128Prefill;
+  const GqaLaunchInfo li = gqa_launch_info(pl.variant);
+  pl.rows_per_cta = li.rows_per_cta;
+  const int64_t rows = static_cast<int64_t>(d->Tq) * G;
+  pl.m_tiles = static_cast<int>((rows + li.rows_per_cta - 1) / li.rows_per_cta);
+
+  // longest split, in tiles of its tile-aligned window
+  int64_t max_tiles = 0;
+  for (int b = 0; b < d->B; ++b) {
+    const int32_t* r = bounds + static_cast<int64_t>(b) * (n_split + 1);
+    for (int j = 0; j < n_split; ++j) {
+      const int64_t lo = (r[j] / kTileN) * kTileN;
+      const int64_t hi = std::min<int64_t>(r[j + 1], d->S_max);
+      if (hi > lo) max_tiles = std::max<int64_t>(max_tiles, (hi - lo + kTileN - 1) / kTileN);
+    }
+  }
+  const int64_t base = static_cast<int64_t>(d->B) * d->Hkv * n_split * pl.m_tiles;
+  const int64_t slots = static_cast<int64_t>(device_sm_count()) * 2;  // 2 resident CTAs per SM
+  pl.n_chunk = 1;
+  pl.chunk_tiles = static_cast<int>(std::max<int64_t>(max_tiles, 1));
+  if (max_tiles > 1 && base < 4 * slots) {
+    // Cut every split into n chunks so that the grid fills the GPU in whole waves;
+    // cost model: waves * (tiles per chunk + per-CTA overhead of ~3 tiles).
+    double best = 1e300;
+    const int64_t n_hi = std::min<int64_t>(max_tiles, 512);
+    for (int64_t n = 1; n <= n_hi; ++n) {
+      const int64_t ct = (max_tiles + n - 1) / n;
+      const int64_t nn = (max_tiles + ct - 1) / ct;
+      const int64_t waves = (base * nn + slots - 1) / slots;
+      const double cost = static_cast<double>(waves) * static_cast<double>(ct + 3);
+      if (cost < best * 0.999) {
+        best = cost;
+        pl.n_chunk = static_cast<int>(nn);
+        pl.chunk_tiles = static_cast<int>(ct);
+      }
+    }
+  }
+  pl.n_part = n_split * pl.n_chunk;
+  pl.n_items = base * pl.n_chunk;
+  return pl;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t ws_bytes_for(const skv_desc* d, int n_part) {
+  const size_t rows = static_cast<size_t>(d->B) * d->Tq * d->Hq;
+  return align_up(static_cast<size_t>(n_part) * rows * d->dv * 4, 256) + align_up(static_cast<size_t>(n_part) * rows * 4, 256);
+}
+
+skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, const int64_t* strides, int dim) {
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
+  const bool fp8 = d->kv_dtype == SKV_KV_FP8_E4M3;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(d->S_max),
+                        static_cast<cuuint64_t>(d->Hkv), static_cast<cuuint64_t>(d->B)};
+  const int64_t tok_b = strides[2] * esz;
+  int64_t head_b = strides[1] * esz, batch_b = strides[0] * esz;
+  // a stride of a size-1 dimension is never stepped; give it any legal value
+  if (d->Hkv == 1 || head_b == 0) head_b = std::max<int64_t>(head_b, tok_b * d->S_max);
+  if (d->B == 1 || batch_b == 0) batch_b = std::max<int64_t>(batch_b, head_b * d->Hkv);
+  cuuint64_t gstride[3] = {static_cast<cuuint64_t>(tok_b), static_cast<cuuint64_t>(head_b),
+                           static_cast<cuuint64_t>(batch_b)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kTileN), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                      const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return fail(SKV_ECUDA, buf);
+  }
+  return SKV_OK;
+}
+
+// Fill the launch parameters common to every GQA partial launch.
+skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, const void* q, const float* ks,
+                       const float* vs, const int32_t* seq_lens, const int32_t* bounds, int32_t n_split,
+                       int64_t causal_offset, float* out_o, float* out_lse, bool zero_empty) {
+  std::memset(p, 0, sizeof(*p));
+  cudaError_t e;
+  p->err = device_error_word(&e);
+  if (!p->err) return cuda_fail(e, "device error word");
+  p->q = q;
+  p->q_sb = d->q_strides[0];
+  p->q_st = d->q_strides[1];
+  p->q_sh = d->q_strides[2];
+  p->k_scale = ks;
+  p->v_scale = vs;
+  p->scale_block = d->kv_dtype == SKV_KV_FP8_E4M3 ? d->scale_block : kTileN;
+  p->n_scale_blk = static_cast<int32_t>((d->S_max + p->scale_block - 1) / p->scale_block);
+  p->seq_lens = seq_lens;
+  p->out_o = out_o;
+  p->out_lse = out_lse;
+  p->causal_offset = causal_offset;
+  p->scale_log2 = d->softmax_scale * 1.4426950408889634f;
+  p->B = d->B;
+  p->Tq = d->Tq;
+  p->Hq = d->Hq;
+  p->Hkv = d->Hkv;
+  p->G = d->Hq / d->Hkv;
+  p->S_max = static_cast<int32_t>(d->S_max);
+  p->n_split = n_split;
+  p->n_chunk = pl.n_chunk;
+  p->chunk_tiles = pl.chunk_tiles;
+  p->m_tiles = pl.m_tiles;
+  p->zero_empty = zero_empty ? 1 : 0;
+  for (int i = 0; i < d->B * (n_split + 1); ++i) p->bounds[i] = bounds[i];
+  return SKV_OK;
+}
+
+skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const void* k, const void* v,
+                       const float* ks, const float* vs, const int32_t* seq_lens, const int32_t* bounds,
+                       int32_t n_split, int64_t causal_offset, float* out_o, float* out_lse, bool zero_empty,
+                       cudaStream_t stream) {
+  static thread_local PartialParams p;  // ~8 KB: keep it off the stack
+  skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, out_o, out_lse,
+                              zero_empty);
+  if (st != SKV_OK) return st;
+  CUtensorMap tmk, tmv;
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv)) != SKV_OK) return st;
+  cudaError_t e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
+  return SKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t splitkv_version(void) { return (1 << 16) | 0; }
+
+const char* splitkv_last_error(void) { return t_last_error.c_str(); }
+
+skv_status splitkv_device_error(uint32_t* code) {
+  if (!code) return fail(SKV_EINVAL, "code is NULL");
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_skv_device_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  e = cudaMemcpyToSymbol(g_skv_device_error, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  *code = v;
+  return SKV_OK;
+}
+
+skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
+                                       size_t* bytes) {
+  if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  *bytes = pl.n_chunk > 1 ? ws_bytes_for(desc, pl.n_part) : 0;
+  return SKV_OK;
+}
+
+skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                        const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
+                        float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
+  if (!out_partial || !lse_partial) return fail(SKV_EINVAL, "out_partial and lse_partial must be non-NULL");
+  if (!aligned(out_partial, 16) || !aligned(lse_partial, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pl.n_chunk == 1) {
+    return run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                       causal_offset, out_partial, lse_partial, true, s);
+  }
+  const size_t need = ws_bytes_for(desc, pl.n_part);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than attn_partial_workspace_size()");
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
+  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
+                   ws_o, ws_l, false, s);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_chunk, n_split, static_cast<int64_t>(rows), desc->dv, out_partial,
+                               false, lse_partial, s);
+  if (e != cudaSuccess) return cuda_fail(e, "chunk merge launch");
+  return SKV_OK;
+}
+
+skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, int32_t dv, const float* out_partials,
+                          const float* lse_partials, void* out, float* lse, void* stream) {
+  if (n_split < 1 || B <= 0 || Tq <= 0 || Hq <= 0 || dv <= 0) return fail(SKV_EINVAL, "sizes must be positive");
+  if (dv % 4) return fail(SKV_EINVAL, "dv must be a multiple of 4");
+  if (!out_partials || !lse_partials || !out || !lse) return fail(SKV_EINVAL, "pointers must be non-NULL");
+  if (!aligned(out_partials, 16) || !aligned(out, 8) || !aligned(lse_partials, 4) || !aligned(lse, 4))
+    return fail(SKV_EINVAL, "pointers misaligned");
+  const int64_t rows = static_cast<int64_t>(B) * Tq * Hq;
+  cudaError_t e = launch_merge(out_partials, lse_partials, n_split, 1, rows, dv, out, true, lse,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SKV_OK;
+}
+
+skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
+                                          size_t* bytes) {
+  if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  *bytes = ws_bytes_for(desc, pl.n_part);
+  return SKV_OK;
+}
+
+skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                           const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
+  if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
+  if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const size_t need = ws_bytes_for(desc, pl.n_part);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_workspace_size()");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
+  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
+                   ws_o, ws_l, false, s);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SKV_OK;
+}
+
+}  // extern "C"

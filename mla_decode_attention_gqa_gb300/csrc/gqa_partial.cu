@@ -1,0 +1,530 @@
+// Split-KV partial attention for grouped-query attention (GQA), bf16 or fp8-e4m3 KV.
+//
+// What it computes (per work item = sequence b, KV head g, split j, chunk c, row tile):
+// for every query row t and query head h of KV head g's group, the softmax attention
+// of q[b,t,h] over the visible tokens of the item's token range, returned as the
+// normalised partial output o and its natural-log log-sum-exp -- the "partial
+// attention output plus a log-sum-exp" each KVP rank emits in "Helix Parallelism:
+// Why Tensor Parallelism Hits a Wall at Million-Token Context" (section "Sharding
+// the sequence instead"), and each ring step emits in "Context Parallelism for
+// Scalable Million-Token Inference" (section "Pass-KV keeps queries local and
+// circulates keys and values").  Query heads map to KV heads in contiguous groups
+// (head h reads KV head h / G).  A token t is visible to query row i when it lies in
+// the range, t < seq_len[b] and t <= causal_offset + i.
+//
+// GB300 design:
+//   * one producer warp streams K and V tiles (64 tokens) with TMA tiled bulk-tensor
+//     copies into a multi-stage shared-memory ring (128-byte swizzle, conflict-free
+//     ldmatrix), completion tracked by mbarriers; tiles are read-once, so the loads
+//     carry an L2 evict-first policy;
+//   * every consumer warp owns 16 rows of the item (for decode: the 16 query heads
+//     of one KV head), so each K/V byte crosses HBM once per KV head and serves the
+//     whole group;
+//   * QK^T and PV run on mma.sync m16n8k16 tensor-core tiles with fp32 accumulation;
+//     the online softmax (running max / sum, rescale) is kept in registers with
+//     quad shuffles; exponentials are base-2 with log2(e) folded into the scale;
+//   * decode variants spread the item's tiles over 4 consumer warps and combine
+//     their (m, l, O) in shared memory at the end; prefill variants give each of
+//     4 warps its own 16 rows and share every tile.
+//   * fp8: K/V codes are widened to fp16 in registers (exact), q is used in fp16,
+//     the K block scale multiplies the score and the V block scale multiplies p.
+#include <cuda_runtime.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+
+namespace skv {
+
+namespace {
+
+template <bool FP8_, int D_, int WM_, int WN_, int NSTAGE_, int MINB_>
+struct GqaCfg {
+  static constexpr bool FP8 = FP8_;
+  static constexpr int D = D_;  // dk = dv
+  static constexpr int WM = WM_;
+  static constexpr int WN = WN_;
+  static constexpr int NSTAGE = NSTAGE_;
+  static constexpr int MINB = MINB_;
+  static constexpr int TN = kTileN;
+  static constexpr int ESZ = FP8 ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ESZ;
+  static constexpr int NBOX = ROW_BYTES / 128;  // 128-byte TMA boxes per token row
+  static constexpr int BOX_ELEMS = 128 / ESZ;
+  static constexpr int BOX_BYTES = TN * 128;
+  static constexpr int TILE_BYTES = TN * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int NCW = WM * WN;
+  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int ROWS = 16 * WM;
+  static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
+  static constexpr int BAR_BYTES = 2 * NSTAGE * 8;
+  static constexpr int ML_BYTES = WN * ROWS * 2 * 4;
+  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + ML_BYTES;
+  static_assert(ROW_BYTES % 128 == 0, "token rows must be whole 128-byte boxes");
+  static_assert(WN == 1 || WN * ROWS * D * 4 <= RING_BYTES, "combine buffer must fit in the ring");
+  static_assert(D % 16 == 0, "head dim must be a multiple of 16");
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Byte offset of (token row, byte in the row) in a K or V tile of the ring.
+template <class C>
+__device__ __forceinline__ uint32_t tile_off(uint32_t tok, uint32_t byte) {
+  return (byte >> 7) * C::BOX_BYTES + swz128(tok, byte & 127u);
+}
+
+__device__ __forceinline__ uint32_t half_mask(bool lo, bool hi) {
+  return (lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+    gqa_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
+  constexpr int D = C::D, TN = C::TN, NSTAGE = C::NSTAGE, WN = C::WN, WM = C::WM;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
+  uint64_t* empty = full + NSTAGE;
+  float* ml = reinterpret_cast<float*>(empty + NSTAGE);  // [WN][ROWS][2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item
+  int64_t item = blockIdx.x;
+  const int mt = static_cast<int>(item % p.m_tiles);
+  item /= p.m_tiles;
+  const int c = static_cast<int>(item % p.n_chunk);
+  item /= p.n_chunk;
+  const int j = static_cast<int>(item % p.n_split);
+  item /= p.n_split;
+  const int g = static_cast<int>(item % p.Hkv);
+  const int b = static_cast<int>(item / p.Hkv);
+
+  const int seq_len = p.seq_lens[b];
+  const int* bnd = p.bounds + b * (p.n_split + 1);
+  int lo = max(bnd[j], 0);
+  int hi = min(min(bnd[j + 1], seq_len), p.S_max);
+  const int win_lo = (lo / TN) * TN + c * p.chunk_tiles * TN;
+  const int win_hi = win_lo + p.chunk_tiles * TN;
+  int r_lo = max(lo, win_lo);
+  int r_hi = min(hi, win_hi);
+  const int rows_total = p.Tq * p.G;
+  const int m0 = mt * C::ROWS;
+  const int m_last = min(m0 + C::ROWS, rows_total) - 1;
+  {
+    // no row of this tile sees a token past causal_offset + (its query row)
+    const int64_t horizon = p.causal_offset + m_last / p.G;
+    if (horizon < static_cast<int64_t>(r_hi) - 1) r_hi = static_cast<int>(max(horizon + 1, (int64_t)r_lo));
+  }
+  const int tile_begin = r_lo / TN;
+  const int n_tiles = (r_hi > r_lo) ? ((r_hi + TN - 1) / TN - tile_begin) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], WM);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer warp
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % NSTAGE;
+        if (i >= NSTAGE && !mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1, p.err, kDevErrEmptyWait)) break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        uint8_t* ks = smem + s * C::STAGE_BYTES;
+        uint8_t* vs = ks + C::TILE_BYTES;
+        const int tok = (tile_begin + i) * TN;
+#pragma unroll
+        for (int bx = 0; bx < C::NBOX; ++bx) {
+          tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, &full[s], bx * C::BOX_ELEMS, tok, g, b, pol);
+          tma_load_4d(vs + bx * C::BOX_BYTES, &tmv, &full[s], bx * C::BOX_ELEMS, tok, g, b, pol);
+        }
+        issued = i + 1;
+      }
+      // drain: every issued copy must have landed before this CTA may exit
+      for (int i = max(0, issued - NSTAGE); i < issued; ++i) {
+        if (!mbar_wait(&full[i % NSTAGE], (i / NSTAGE) & 1, p.err, kDevErrDrainWait)) break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumer warps
+  const int wm = warp % WM, wn = warp / WM;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int mrow0 = m0 + wm * 16 + gq, mrow1 = mrow0 + 8;
+  const bool v0 = mrow0 < rows_total, v1 = mrow1 < rows_total;
+  const int tq0 = v0 ? mrow0 / p.G : 0, tq1 = v1 ? mrow1 / p.G : 0;
+  const int h0 = g * p.G + (v0 ? mrow0 % p.G : 0), h1 = g * p.G + (v1 ? mrow1 % p.G : 0);
+  const int64_t hz0 = p.causal_offset + tq0, hz1 = p.causal_offset + tq1;
+  const int64_t hz_min = p.causal_offset + (m0 + wm * 16) / p.G;
+
+  // ---- Q fragments (A operand, 16 rows x D)
+  uint32_t qa[D / 16][4];
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* q0 = q + b * p.q_sb + tq0 * p.q_st + h0 * p.q_sh;
+    const __nv_bfloat16* q1 = q + b * p.q_sb + tq1 * p.q_st + h1 * p.q_sh;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      if constexpr (!C::FP8) {
+        const int d0 = 16 * ks + 2 * tq;
+        qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
+        qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
+        qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
+        qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
+      } else {
+        // k-slots (2tq, 2tq+1 | 2tq+8, 2tq+9) hold d = 16ks + 4tq + (0,1 | 2,3), the
+        // order in which ldmatrix delivers the e4m3 key bytes
+        const int d0 = 16 * ks + 4 * tq;
+        float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (v0) {
+          const uint2 u = *reinterpret_cast<const uint2*>(q0 + d0);
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+          f0[0] = __low2float(a); f0[1] = __high2float(a); f0[2] = __low2float(bb); f0[3] = __high2float(bb);
+        }
+        if (v1) {
+          const uint2 u = *reinterpret_cast<const uint2*>(q1 + d0);
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+          f1[0] = __low2float(a); f1[1] = __high2float(a); f1[2] = __low2float(bb); f1[3] = __high2float(bb);
+        }
+        qa[ks][0] = pack_f16(f0[0], f0[1]);
+        qa[ks][1] = pack_f16(f1[0], f1[1]);
+        qa[ks][2] = pack_f16(f0[2], f0[3]);
+        qa[ks][3] = pack_f16(f1[2], f1[3]);
+      }
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrun[2] = {-INFINITY, -INFINITY};
+  float lrun[2] = {0.f, 0.f};
+  const float* kscale_row = nullptr;
+  const float* vscale_row = nullptr;
+  if constexpr (C::FP8) {
+    kscale_row = p.k_scale + (static_cast<int64_t>(b) * p.Hkv + g) * p.n_scale_blk;
+    vscale_row = p.v_scale + (static_cast<int64_t>(b) * p.Hkv + g) * p.n_scale_blk;
+  }
+
+  for (int i = wn; i < n_tiles; i += WN) {
+    const int s = i % NSTAGE;
+    const int t0 = (tile_begin + i) * TN;
+    float ksc = 1.f, vsc = 1.f;
+    if constexpr (C::FP8) {
+      ksc = __ldg(kscale_row + t0 / p.scale_block);
+      vsc = __ldg(vscale_row + t0 / p.scale_block);
+    }
+    if (!mbar_wait(&full[s], (i / NSTAGE) & 1, p.err, kDevErrFullWait)) break;
+    const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+
+    // ---- S = Q K^T  (16 x 64)
+    float sc[TN / 8][4];
+#pragma unroll
+    for (int i2 = 0; i2 < TN / 8; ++i2) sc[i2][0] = sc[i2][1] = sc[i2][2] = sc[i2][3] = 0.f;
+    const int mi = lane >> 3;
+    if constexpr (!C::FP8) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int np = 0; np < TN / 16; ++np) {
+          const uint32_t tok = 16 * np + (mi >> 1) * 8 + (lane & 7);
+          const uint32_t byte = (2 * ks + (mi & 1)) * 16;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
+          mma_bf16(sc[2 * np], qa[ks], r0, r1);
+          mma_bf16(sc[2 * np + 1], qa[ks], r2, r3);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks += 2) {
+#pragma unroll
+        for (int np = 0; np < TN / 16; ++np) {
+          const uint32_t tok = 16 * np + (mi >> 1) * 8 + (lane & 7);
+          const uint32_t byte = (ks + (mi & 1)) * 16;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
+          mma_f16(sc[2 * np], qa[ks], e4m3x2_to_f16x2(r0 & 0xFFFF), e4m3x2_to_f16x2(r0 >> 16));
+          mma_f16(sc[2 * np], qa[ks + 1], e4m3x2_to_f16x2(r1 & 0xFFFF), e4m3x2_to_f16x2(r1 >> 16));
+          mma_f16(sc[2 * np + 1], qa[ks], e4m3x2_to_f16x2(r2 & 0xFFFF), e4m3x2_to_f16x2(r2 >> 16));
+          mma_f16(sc[2 * np + 1], qa[ks + 1], e4m3x2_to_f16x2(r3 & 0xFFFF), e4m3x2_to_f16x2(r3 >> 16));
+        }
+      }
+    }
+
+    // ---- scale, mask, online softmax
+    const float sl = p.scale_log2 * ksc;
+    const bool in_range = (t0 >= r_lo) && (t0 + TN <= r_hi);
+    const bool need_mask = !in_range || (static_cast<int64_t>(t0) + TN - 1 > hz_min);
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < TN / 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = sc[nt][e] * sl;
+        if (need_mask) {
+          const int tok = t0 + 8 * nt + 2 * tq + (e & 1);
+          const int64_t hz = (e < 2) ? hz0 : hz1;
+          const bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
+          x = ok ? x : -INFINITY;
+        }
+        sc[nt][e] = x;
+        tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
+      }
+    }
+    float base[2], alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 1));
+      tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 2));
+      const float mnew = fmaxf(mrun[r], tmax[r]);
+      base[r] = (mnew == -INFINITY) ? 0.f : mnew;
+      alpha[r] = fast_exp2(mrun[r] - base[r]);  // 0 when mrun = -inf
+      mrun[r] = mnew;
+      lrun[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int i2 = 0; i2 < D / 8; ++i2) {
+      o[i2][0] *= alpha[0];
+      o[i2][1] *= alpha[0];
+      o[i2][2] *= alpha[1];
+      o[i2][3] *= alpha[1];
+    }
+    uint32_t pa[TN / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < TN / 8; ++nt) {
+      const float p0 = fast_exp2(sc[nt][0] - base[0]);
+      const float p1 = fast_exp2(sc[nt][1] - base[0]);
+      const float p2 = fast_exp2(sc[nt][2] - base[1]);
+      const float p3 = fast_exp2(sc[nt][3] - base[1]);
+      lrun[0] += p0 + p1;
+      lrun[1] += p2 + p3;
+      const int kk = nt >> 1, hf = (nt & 1) * 2;
+      if constexpr (!C::FP8) {
+        pa[kk][hf + 0] = pack_bf16(p0, p1);
+        pa[kk][hf + 1] = pack_bf16(p2, p3);
+      } else {
+        pa[kk][hf + 0] = pack_f16(p0 * vsc, p1 * vsc);
+        pa[kk][hf + 1] = pack_f16(p2 * vsc, p3 * vsc);
+      }
+    }
+
+    // ---- O += P V
+    const bool vmask = !in_range;
+#pragma unroll
+    for (int kk = 0; kk < TN / 16; ++kk) {
+      if constexpr (!C::FP8) {
+        uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+        if (vmask) {
+          const int ta = t0 + 16 * kk + 2 * tq, tb = ta + 8;
+          mlo = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
+          mhi = half_mask(tb >= r_lo && tb < r_hi, tb + 1 >= r_lo && tb + 1 < r_hi);
+        }
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const uint32_t tok = 16 * kk + (mi & 1) * 8 + (lane & 7);
+          const uint32_t byte = (2 * dp + (mi >> 1)) * 16;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
+          mma_bf16(o[2 * dp], pa[kk], r0 & mlo, r1 & mhi);
+          mma_bf16(o[2 * dp + 1], pa[kk], r2 & mlo, r3 & mhi);
+        }
+      } else {
+        bool ok0 = true, ok1 = true;
+        if (vmask) {
+          const int ta = t0 + 16 * kk + gq, tb = ta + 8;
+          ok0 = ta >= r_lo && ta < r_hi;
+          ok1 = tb >= r_lo && tb < r_hi;
+        }
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const uint32_t tok = 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
+          uint32_t r0, r1;
+          ldsm_x2(vbase + tile_off<C>(tok, cc * 16), r0, r1);
+          r0 = ok0 ? r0 : 0u;
+          r1 = ok1 ? r1 : 0u;
+          const uint32_t h0v = e4m3x2_to_f16x2(r0 & 0xFFFF), h1v = e4m3x2_to_f16x2(r0 >> 16);
+          const uint32_t h2v = e4m3x2_to_f16x2(r1 & 0xFFFF), h3v = e4m3x2_to_f16x2(r1 >> 16);
+          mma_f16(o[2 * cc], pa[kk], movmatrix_t(h0v), movmatrix_t(h2v));
+          mma_f16(o[2 * cc + 1], pa[kk], movmatrix_t(h1v), movmatrix_t(h3v));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---- finish: normalise, combine the WN warps of a row set, store
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 1);
+    lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 2);
+  }
+  constexpr float kLn2 = 0.6931471805599453f;
+  const int part = j * p.n_chunk + c;
+  auto row_out = [&](int t_q, int h) -> int64_t {
+    return ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
+  };
+
+  if constexpr (WN == 1) {
+    const float inv0 = lrun[0] > 0.f ? 1.f / lrun[0] : 0.f;
+    const float inv1 = lrun[1] > 0.f ? 1.f / lrun[1] : 0.f;
+    const bool w0 = v0 && (lrun[0] > 0.f || p.zero_empty);
+    const bool w1 = v1 && (lrun[1] > 0.f || p.zero_empty);
+    float* o0 = p.out_o + row_out(tq0, h0) * D;
+    float* o1 = p.out_o + row_out(tq1, h1) * D;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      int d;
+      if constexpr (!C::FP8) {
+        d = 8 * nt + 2 * tq;
+      } else {
+        d = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1);
+      }
+      if (w0) *reinterpret_cast<float2*>(o0 + d) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
+      if (w1) *reinterpret_cast<float2*>(o1 + d) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+    }
+    if (tq == 0) {
+      if (v0) p.out_lse[row_out(tq0, h0)] = lrun[0] > 0.f ? (mrun[0] + __log2f(lrun[0])) * kLn2 : -INFINITY;
+      if (v1) p.out_lse[row_out(tq1, h1)] = lrun[1] > 0.f ? (mrun[1] + __log2f(lrun[1])) * kLn2 : -INFINITY;
+    }
+  } else {
+    constexpr int NCT = C::NCW * 32;
+    named_bar_sync(1, NCT);  // every consumer is done with the ring
+    const int lr0 = wm * 16 + gq, lr1 = lr0 + 8;  // local rows
+    if (tq == 0) {
+      ml[(wn * C::ROWS + lr0) * 2 + 0] = mrun[0];
+      ml[(wn * C::ROWS + lr0) * 2 + 1] = lrun[0];
+      ml[(wn * C::ROWS + lr1) * 2 + 0] = mrun[1];
+      ml[(wn * C::ROWS + lr1) * 2 + 1] = lrun[1];
+    }
+    named_bar_sync(1, NCT);
+    float f[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int lr = r ? lr1 : lr0;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < WN; ++w) M = fmaxf(M, ml[(w * C::ROWS + lr) * 2]);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < WN; ++w) L += ml[(w * C::ROWS + lr) * 2 + 1] * fast_exp2(ml[(w * C::ROWS + lr) * 2] - M);
+      }
+      f[r] = (L > 0.f) ? fast_exp2(mrun[r] - M) / L : 0.f;
+    }
+    float* obuf = reinterpret_cast<float*>(smem);  // [WN][ROWS][D]
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      int d;
+      if constexpr (!C::FP8) {
+        d = 8 * nt + 2 * tq;
+      } else {
+        d = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1);
+      }
+      *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr0) * D + d) = make_float2(o[nt][0] * f[0], o[nt][1] * f[0]);
+      *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr1) * D + d) = make_float2(o[nt][2] * f[1], o[nt][3] * f[1]);
+    }
+    named_bar_sync(1, NCT);
+    const int tid = threadIdx.x;  // < NCT
+    for (int e = tid * 4; e < C::ROWS * D; e += NCT * 4) {
+      const int lr = e / D, d = e % D;
+      const int m = m0 + lr;
+      if (m >= rows_total) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < WN; ++w) M = fmaxf(M, ml[(w * C::ROWS + lr) * 2]);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < WN; ++w) L += ml[(w * C::ROWS + lr) * 2 + 1] * fast_exp2(ml[(w * C::ROWS + lr) * 2] - M);
+      }
+      const int t_q = m / p.G, h = g * p.G + m % p.G;
+      const int64_t ro = row_out(t_q, h);
+      if (L > 0.f || p.zero_empty) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < WN; ++w) {
+          const float4 x = *reinterpret_cast<const float4*>(obuf + (w * C::ROWS + lr) * D + d);
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
+        }
+        *reinterpret_cast<float4*>(p.out_o + ro * D + d) = acc;
+      }
+      if (d == 0) p.out_lse[ro] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+using CfgBf16D64Dec = GqaCfg<false, 64, 1, 4, 6, 2>;
+using CfgBf16D128Dec = GqaCfg<false, 128, 1, 4, 3, 2>;
+using CfgFp8D128Dec = GqaCfg<true, 128, 1, 4, 6, 2>;
+using CfgBf16D64Pre = GqaCfg<false, 64, 4, 1, 6, 2>;
+using CfgBf16D128Pre = GqaCfg<false, 128, 4, 1, 3, 2>;
+using CfgFp8D128Pre = GqaCfg<true, 128, 4, 1, 6, 2>;
+
+template <class C>
+GqaLaunchInfo info_of() {
+  return GqaLaunchInfo{C::ROWS, C::THREADS, C::SMEM};
+}
+
+template <class C>
+cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items,
+                       cudaStream_t stream) {
+  static bool attr_done = false;  // per variant; set once per process
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gqa_partial_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (n_items <= 0) return cudaSuccess;
+  gqa_partial_kernel<C><<<static_cast<unsigned int>(n_items), C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+GqaLaunchInfo gqa_launch_info(GqaVariant v) {
+  switch (v) {
+    case GqaVariant::kBf16D64Decode: return info_of<CfgBf16D64Dec>();
+    case GqaVariant::kBf16D128Decode: return info_of<CfgBf16D128Dec>();
+    case GqaVariant::kFp8D128Decode: return info_of<CfgFp8D128Dec>();
+    case GqaVariant::kBf16D64Prefill: return info_of<CfgBf16D64Pre>();
+    case GqaVariant::kBf16D128Prefill: return info_of<CfgBf16D128Pre>();
+    case GqaVariant::kFp8D128Prefill: return info_of<CfgFp8D128Pre>();
+  }
+  return GqaLaunchInfo{0, 0, 0};
+}
+
+cudaError_t launch_gqa_partial(GqaVariant v, const PartialParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               int64_t n_items, cudaStream_t stream) {
+  switch (v) {
+    case GqaVariant::kBf16D64Decode: return launch_cfg<CfgBf16D64Dec>(p, tmk, tmv, n_items, stream);
+    case GqaVariant::kBf16D128Decode: return launch_cfg<CfgBf16D128Dec>(p, tmk, tmv, n_items, stream);
+    case GqaVariant::kFp8D128Decode: return launch_cfg<CfgFp8D128Dec>(p, tmk, tmv, n_items, stream);
+    case GqaVariant::kBf16D64Prefill: return launch_cfg<CfgBf16D64Pre>(p, tmk, tmv, n_items, stream);
+    case GqaVariant::kBf16D128Prefill: return launch_cfg<CfgBf16D128Pre>(p, tmk, tmv, n_items, stream);
+    case GqaVariant::kFp8D128Prefill: return launch_cfg<CfgFp8D128Pre>(p, tmk, tmv, n_items, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace skv

@@ -1,0 +1,99 @@
+// Exact merge of partial attention outputs by their log-sum-exp.
+//
+// For every output row: m = max_s lse_s, w_s = exp(lse_s - m), o = sum_s w_s o_s / sum_s w_s,
+// lse = m + ln sum_s w_s -- the merge of "Helix Parallelism: Why Tensor Parallelism
+// Hits a Wall at Million-Token Context" (section "Sharding the sequence instead",
+// the merge after the All-to-All) and the exact-merge equation of "Context
+// Parallelism for Scalable Million-Token Inference" (section "Pass-KV keeps queries
+// local and circulates keys and values").  The merged lse (m + ln den) is the
+// reading that makes a merged result mergeable again.  Partials with lse = -inf
+// carry weight 0 and their o is never read; a row whose partials are all empty gets
+// o = 0, lse = -inf.
+//
+// One warp per output row; each lane owns 4 consecutive output columns per pass
+// (16-byte loads), so reads of the n_in partial rows are coalesced and read once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "skv_internal.h"
+
+namespace skv {
+
+namespace {
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ in_o, const float* __restrict__ in_lse,
+                                                    int32_t n_in, int32_t g_out, int64_t R, int32_t dv,
+                                                    void* __restrict__ out, float* __restrict__ out_lse) {
+  const int64_t row_id = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row_id >= static_cast<int64_t>(g_out) * R) return;
+  const int64_t grp = row_id / R, r = row_id % R;
+  const float* lse_base = in_lse + grp * n_in * R + r;  // + s*R
+  const float* o_base = in_o + (grp * n_in * R + r) * dv;  // + s*R*dv
+
+  float m = -INFINITY;
+  for (int s = lane; s < n_in; s += 32) m = fmaxf(m, lse_base[static_cast<int64_t>(s) * R]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+
+  float den = 0.f;
+  if (m != -INFINITY) {
+    for (int s = lane; s < n_in; s += 32) den += __expf(lse_base[static_cast<int64_t>(s) * R] - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+
+  const int64_t out_row = grp * R + r;
+  for (int d = lane * 4; d < dv; d += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_in; ++s) {
+        const float ls = lse_base[static_cast<int64_t>(s) * R];
+        if (ls == -INFINITY) continue;
+        const float w = __expf(ls - m);
+        const float4 x = *reinterpret_cast<const float4*>(o_base + static_cast<int64_t>(s) * R * dv + d);
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+      }
+    }
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    if constexpr (OUT_BF16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + out_row * dv + d) = u;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + out_row * dv + d) = acc;
+    }
+  }
+  if (lane == 0) out_lse[out_row] = (den > 0.f) ? m + logf(den) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, int32_t g_out, int64_t R, int32_t dv,
+                         void* out, bool out_bf16, float* out_lse, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(g_out) * R;
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  if (out_bf16) {
+    merge_kernel<true><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(in_o, in_lse, n_in, g_out, R, dv, out,
+                                                                              out_lse);
+  } else {
+    merge_kernel<false><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(in_o, in_lse, n_in, g_out, R, dv, out,
+                                                                               out_lse);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,72 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace skv {
+
+// Largest B * (n_split + 1) whose split bounds travel inside the kernel parameters.
+constexpr int kMaxBounds = 2048;
+
+// Tokens per KV tile of the GQA partial kernel (and the chunk granularity).
+constexpr int kTileN = 64;
+
+// Parameters of one split-KV partial-attention launch.
+//
+// Work item = (b, kv head g, split j, chunk c, row tile mt).  Split j of sequence b
+// covers tokens [bounds[b][j], bounds[b][j+1]) clipped to seq_lens[b]; chunk c of it
+// covers the tile-aligned window [a + c*chunk_tiles*kTileN, a + (c+1)*chunk_tiles*kTileN)
+// with a = floor(bounds[b][j] / kTileN) * kTileN.  Row m of kv head g's row space
+// (m < Tq*G) is query row t = m / G of query head g*G + m % G.
+//
+// The item writes its partial (normalised o, natural-log lse) to part
+// p = j * n_chunk + c of out_o [n_part][B][Tq][Hq][dv] and out_lse [n_part][B][Tq][Hq].
+struct PartialParams {
+  const void* q;  // bf16 [B][Tq][Hq][dk] with strides below (elements)
+  int64_t q_sb, q_st, q_sh;
+  const float* k_scale;  // fp8 only: [B][Hkv][n_scale_blk]
+  const float* v_scale;
+  int32_t n_scale_blk;
+  int32_t scale_block;
+  const int32_t* seq_lens;  // device [B]
+  float* out_o;
+  float* out_lse;
+  unsigned int* err;  // device error word
+  int64_t causal_offset;
+  float scale_log2;  // softmax_scale * log2(e)
+  int32_t B, Tq, Hq, Hkv, G;
+  int32_t S_max;  // tokens at or past S_max do not exist
+  int32_t n_split, n_chunk, chunk_tiles, m_tiles;
+  int32_t zero_empty;  // write o = 0 for items with no visible token
+  int32_t bounds[kMaxBounds];  // [B][n_split + 1]
+};
+
+// Supported GQA kernel variants.
+enum class GqaVariant {
+  kBf16D64Decode,
+  kBf16D128Decode,
+  kFp8D128Decode,
+  kBf16D64Prefill,
+  kBf16D128Prefill,
+  kFp8D128Prefill,
+};
+
+struct GqaLaunchInfo {
+  int rows_per_cta;  // M rows handled by one CTA
+  int threads;
+  int smem_bytes;
+};
+
+GqaLaunchInfo gqa_launch_info(GqaVariant v);
+
+cudaError_t launch_gqa_partial(GqaVariant v, const PartialParams& p, const CUtensorMap& tmk,
+                               const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream);
+
+// Merge n_in partials per output group: in_o [G_out][n_in][R][dv], in_lse [G_out][n_in][R]
+// -> out [G_out][R][dv] (fp32 or bf16) and out_lse [G_out][R].
+cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, int32_t g_out, int64_t R,
+                         int32_t dv, void* out, bool out_bf16, float* out_lse, cudaStream_t stream);
+
+}  // namespace skv

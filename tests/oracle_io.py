@@ -1,0 +1,75 @@
+"""Test helpers: turn a workload's torch tensors into the oracle's float64 inputs and
+compare GPU results with the oracle's.  (Test code: may import the oracle.)"""
+
+import numpy as np
+import torch
+
+import oracle
+
+# Parity bars (written in the tests): max-abs error of the output and of the LSE.
+TOL_BF16 = {"out": 1e-2, "lse": 1e-3}
+TOL_FP8 = {"out": 4e-2, "lse": 4e-2}
+
+
+def tol_for(w):
+    return TOL_FP8 if w.kv_dtype == "fp8_e4m3" else TOL_BF16
+
+
+def q_f64(q):
+    return oracle.bf16_bits_to_f64(q.contiguous().view(torch.int16).cpu().numpy())
+
+
+def kv_f64(inp, w, which, b, g):
+    """Dequantised K or V rows [S, d] of (batch b, KV head g) as float64."""
+    t = inp[which][b, g]
+    if w.kv_dtype == "bf16":
+        return oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).cpu().numpy())
+    scales = inp["k_scale" if which == "k" else "v_scale"][b, g].cpu().numpy()
+    return oracle.dequant_e4m3_blocks(t.contiguous().cpu().numpy(), scales, w.scale_block)
+
+
+def oracle_group(inp, w, b, g, bounds=None, causal_offset=None):
+    """Oracle partials of one (batch, KV head): o [n_split, Tq, G, dv], lse [n_split, Tq, G]."""
+    G = w.Hq // w.Hkv
+    bounds = inp["split_bounds"] if bounds is None else bounds
+    causal = w.causal_offset if causal_offset is None else causal_offset
+    qb = q_f64(inp["q"][b : b + 1, :, g * G : (g + 1) * G])
+    kb = kv_f64(inp, w, "k", b, g)[None, None]
+    vb = kv_f64(inp, w, "v", b, g)[None, None]
+    o, lse = oracle.split_attention(qb, kb, vb, [inp["seq_lens_host"][b]], [bounds[b]], causal, w.scale)
+    return o[:, 0], lse[:, 0]
+
+
+def oracle_all(inp, w, bounds=None, causal_offset=None):
+    """Oracle partials of every (batch, KV head): o [n_split,B,Tq,Hq,dv], lse [n_split,B,Tq,Hq]."""
+    G = w.Hq // w.Hkv
+    bounds = inp["split_bounds"] if bounds is None else bounds
+    n_split = len(bounds[0]) - 1
+    o = np.zeros((n_split, w.B, w.Tq, w.Hq, w.dv))
+    lse = np.zeros((n_split, w.B, w.Tq, w.Hq))
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            og, lg = oracle_group(inp, w, b, g, bounds, causal_offset)
+            o[:, b, :, g * G : (g + 1) * G] = og
+            lse[:, b, :, g * G : (g + 1) * G] = lg
+    return o, lse
+
+
+def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
+    """Element-wise parity: |o - o_ref| <= tol['out'], |lse - lse_ref| <= tol['lse'];
+    rows with lse_ref = -inf must have lse = -inf and o = 0."""
+    go = got_o.detach().float().cpu().numpy().astype(np.float64)
+    gl = got_lse.detach().float().cpu().numpy().astype(np.float64)
+    assert go.shape == ref_o.shape, (what, go.shape, ref_o.shape)
+    assert gl.shape == ref_lse.shape, (what, gl.shape, ref_lse.shape)
+    assert np.all(np.isfinite(go)), f"{what}: non-finite output"
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(gl), empty), f"{what}: empty-row pattern differs"
+    if empty.any():
+        assert np.all(go[empty] == 0.0), f"{what}: empty rows must be 0"
+    full = ~empty
+    err_o = float(np.max(np.abs(go - ref_o))) if go.size else 0.0
+    err_l = float(np.max(np.abs(gl[full] - ref_lse[full]))) if full.any() else 0.0
+    assert err_o <= tol["out"], f"{what}: out max-abs err {err_o:.3e} > {tol['out']}"
+    assert err_l <= tol["lse"], f"{what}: lse max-abs err {err_l:.3e} > {tol['lse']}"
+    return err_o, err_l

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol, and
+rejects bad arguments with a status code before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_decode_attention_gqa_gb300 as skv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splitkv_attn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?[\s\*]+([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared_functions() == sorted(skv.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = skv.load_library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert skv.version() == (1, 0)
+
+
+def _desc(**kw):
+    d = skv.SkvDesc()
+    d.B, d.Tq, d.Hq, d.Hkv, d.dk, d.dv = 2, 1, 16, 4, 128, 128
+    d.S_max = 1024
+    d.softmax_scale = 0.088
+    d.kv_dtype = skv.SKV_KV_BF16 if hasattr(skv, "SKV_KV_BF16") else 0
+    d.scale_block = 64
+    q = [16 * 128, 16 * 128, 128]
+    k = [4 * 1024 * 128, 1024 * 128, 128]
+    for i in range(3):
+        d.q_strides[i], d.k_strides[i], d.v_strides[i] = q[i], k[i], k[i]
+    for key, val in kw.items():
+        if key in ("q_strides", "k_strides", "v_strides"):
+            for i in range(3):
+                getattr(d, key)[i] = val[i]
+        else:
+            setattr(d, key, val)
+    return d
+
+
+def _bounds(rows):
+    flat = [x for r in rows for x in r]
+    return (ctypes.c_int32 * len(flat))(*flat), len(rows[0]) - 1
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+
+def _call_partial(d, rows=((0, 1024), (0, 1024)), q=FAKE, k=FAKE, v=FAKE, seq=FAKE, ks=None, vs=None):
+    lib = skv.load_library()
+    b, n = _bounds(rows)
+    return lib.attn_partial(ctypes.byref(d), q, k, v, ks, vs, seq, b, n, 0, FAKE, FAKE, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=15), skv.SKV_EINVAL),
+    (dict(B=0), skv.SKV_EINVAL),
+    (dict(S_max=0), skv.SKV_EINVAL),
+    (dict(softmax_scale=float("inf")), skv.SKV_EINVAL),
+    (dict(kv_dtype=7), skv.SKV_EINVAL),
+    (dict(q_strides=(16 * 128, 16 * 128, 100)), skv.SKV_EINVAL),
+    (dict(k_strides=(4 * 1024 * 128, 1024 * 128, 100)), skv.SKV_EINVAL),
+    (dict(dk=96, dv=96), skv.SKV_EUNSUPPORTED),
+    (dict(dk=128, dv=64), skv.SKV_EUNSUPPORTED),
+    (dict(kv_dtype=1, scale_block=32), skv.SKV_EINVAL),
+])
+def test_bad_descriptors_are_rejected(kw, status):
+    assert _call_partial(_desc(**kw)) == status
+    assert skv.last_error() != ""
+
+
+def test_bad_pointers_and_bounds_are_rejected():
+    d = _desc()
+    assert _call_partial(d, q=None) == skv.SKV_EINVAL
+    assert _call_partial(d, seq=None) == skv.SKV_EINVAL
+    assert _call_partial(d, k=ctypes.c_void_p(0x10008)) == skv.SKV_EINVAL  # not 16-byte aligned
+    assert _call_partial(d, rows=((0, 10), (5, 4))) == skv.SKV_EINVAL  # decreasing
+    assert _call_partial(d, rows=((-1, 10), (0, 4))) == skv.SKV_EINVAL  # negative
+    d8 = _desc(kv_dtype=1)
+    assert _call_partial(d8) == skv.SKV_EINVAL  # fp8 without scales
+    assert "scale" in skv.last_error()
+
+
+def test_too_many_bounds_rejected():
+    d = _desc(B=300)
+    rows = [tuple(range(0, 1024, 128)) + (1024,)] * 300
+    assert _call_partial(d, rows=rows) == skv.SKV_EINVAL
+
+
+def test_merge_argument_checks():
+    lib = skv.load_library()
+    assert lib.attn_merge_lse(0, 1, 1, 1, 4, FAKE, FAKE, FAKE, FAKE, None) == skv.SKV_EINVAL
+    assert lib.attn_merge_lse(2, 1, 1, 1, 6, FAKE, FAKE, FAKE, FAKE, None) == skv.SKV_EINVAL
+    assert lib.attn_merge_lse(2, 1, 1, 1, 8, None, FAKE, FAKE, FAKE, None) == skv.SKV_EINVAL
+
+
+def test_workspace_sizes_are_host_queries():
+    d = _desc()
+    b, n = _bounds(((0, 1024), (0, 1024)))
+    assert skv.gqa_decode_attn_workspace_size(d, b, n) > 0
+    assert skv.attn_partial_workspace_size(d, b, n) >= 0
+
+
+def test_missing_workspace_is_reported():
+    lib = skv.load_library()
+    d = _desc()
+    b, n = _bounds(((0, 1024), (0, 1024)))
+    st = lib.gqa_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, b, n, 0, FAKE, FAKE, None, 0, None)
+    assert st == skv.SKV_EWORKSPACE
