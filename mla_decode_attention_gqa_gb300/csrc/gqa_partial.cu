@@ -63,6 +63,10 @@ struct GqaCfg {
   static_assert(ROW_BYTES % 128 == 0, "token rows must be whole 128-byte boxes");
   static_assert(WN == 1 || WN * ROWS * D * 4 <= RING_BYTES, "combine buffer must fit in the ring");
   static_assert(D % 16 == 0, "head dim must be a multiple of 16");
+  // A consumer warp takes tiles WN apart; it must never wait on a stage more than one
+  // phase ahead of the last completed one, or the parity wait would alias an older
+  // phase.  With NSTAGE >= WN the tile NSTAGE before its next one has always landed.
+  static_assert(NSTAGE >= WN, "need at least one ring stage per consumer warp column");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 }
 
 using CfgBf16D64Dec = GqaCfg<false, 64, 1, 4, 6, 2>;
-using CfgBf16D128Dec = GqaCfg<false, 128, 1, 4, 3, 2>;
+using CfgBf16D128Dec = GqaCfg<false, 128, 1, 3, 3, 2>;
 using CfgFp8D128Dec = GqaCfg<true, 128, 1, 4, 6, 2>;
 using CfgBf16D64Pre = GqaCfg<false, 64, 4, 1, 6, 2>;
 using CfgBf16D128Pre = GqaCfg<false, 128, 4, 1, 3, 2>;
