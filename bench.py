@@ -234,7 +234,7 @@ def reference_arm(args, w, ws, rank):
     bytes_total, secs_total = 0, 0.0
     sample = None
     for i in range(args.warmup + args.steps):
-        b, s, g, t = oracle_sample(w, budget_s=0.0, max_groups=1)
+        b, s, g, t = oracle_sample(w, budget_s=float("inf"), max_groups=1)
         if i >= args.warmup:
             steps.append(s)
             bytes_total += b
@@ -405,10 +405,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--S", type=int, default=None, help="smaller KV length of the same workload (profiling)")
+    ap.add_argument("--B", type=int, default=None, help="smaller batch of the same workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = workload_by_name(args.config)
+    over = {k: v for k, v in (("S", args.S), ("B", args.B)) if v is not None}
+    if over:
+        w = W.scaled(w, **over)
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         reference_arm(args, w, ws, rank)
