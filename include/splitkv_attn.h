@@ -149,6 +149,32 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
                            float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * gqa_decode_attn_noalloc -- gqa_decode_attn for callers that cannot allocate device memory.
+ *
+ * No counterpart in the pages: this is a deployment convenience of this library.  Some
+ * callers cannot call cudaMalloc or hand over a workspace: a plugin living inside a host
+ * runtime that owns every device allocation and forbids allocating behind its back, a
+ * latency-critical path where an allocation (which may synchronise the whole device) is not
+ * acceptable, or a foreign-language caller that only has the C ABI and no device allocator.
+ * This entry point takes the same arguments as gqa_decode_attn minus the workspace and
+ * allocates nothing: the per-split / per-chunk partials go to a fixed scratch array of
+ * 32 MiB (33554432 bytes) compiled into the library, which every GPU that loads the library
+ * keeps reserved until the process exits.
+ *   - A problem whose partials need more than 32 MiB (B * Tq * Hq * (dv + 1) * 4 bytes per
+ *     part, rounded) is rejected with SKV_EWORKSPACE and a message giving both sizes.
+ *   - The first call on each device looks up the scratch array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - Every call on a device uses the same scratch array, so calls that may overlap on the
+ *     GPU (different streams, or different host threads) race and corrupt each other's
+ *     results; serialise them (one stream, or events).  The scratch keeps the last call's
+ *     contents; nothing in it needs to start at zero.
+ */
+skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                                   const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                                   const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
+                                   float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

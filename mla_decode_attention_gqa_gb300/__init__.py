@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "attn_merge_lse",
     "gqa_decode_attn_workspace_size",
     "gqa_decode_attn",
+    "gqa_decode_attn_noalloc",
 )
 
 

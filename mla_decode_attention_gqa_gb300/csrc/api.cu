@@ -407,3 +407,77 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// gqa_decode_attn_noalloc: the fused decode call for callers that cannot allocate
+// device memory.  Its per-split / per-chunk partials live in a fixed scratch array
+// compiled into this library instead of a caller-provided workspace.
+
+namespace {
+
+// Largest partial buffer the no-allocation entry point can use (32 MiB).  Every GPU
+// that loads this library reserves it for the life of the process.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device
+// (with that device current) and cached.  In host code the array's name only stands in
+// for the symbol; only this looked-up address may be given to a kernel.
+skv_status noalloc_scratch_ptr(void** out) {
+  static void* cache[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SKV_EINVAL, "device index out of range");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    if (!ptr) return fail(SKV_ECUDA, "cudaGetSymbolAddress returned NULL for the no-alloc scratch");
+    cache[dev] = ptr;
+  }
+  *out = cache[dev];
+  return SKV_OK;
+}
+
+}  // namespace
+
+extern "C" skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* q, const void* k_cache,
+                                              const void* v_cache, const float* k_scale, const float* v_scale,
+                                              const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
+                                              int64_t causal_offset, void* out, float* lse, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
+  if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
+  if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const size_t need = ws_bytes_for(desc, pl.n_part);
+  if (need > kNoAllocScratchBytes) {
+    char buf[256];
+    snprintf(buf, sizeof buf,
+             "gqa_decode_attn_noalloc: this problem needs %zu bytes of partials but the built-in scratch holds "
+             "%zu bytes; use gqa_decode_attn with a workspace",
+             need, kNoAllocScratchBytes);
+    return fail(SKV_EWORKSPACE, buf);
+  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch_ptr(&scratch)) != SKV_OK) return st;
+  // Nothing in the scratch has to start at zero: the partial kernel writes the lse of
+  // every (part, row) slot before the merge reads it, and the merge never reads the o
+  // of a slot whose lse is -inf.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  float* ws_o = static_cast<float*>(scratch);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
+  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
+                   ws_o, ws_l, false, s);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SKV_OK;
+}
