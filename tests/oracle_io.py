@@ -73,3 +73,30 @@ def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
     assert err_o <= tol["out"], f"{what}: out max-abs err {err_o:.3e} > {tol['out']}"
     assert err_l <= tol["lse"], f"{what}: lse max-abs err {err_l:.3e} > {tol['lse']}"
     return err_o, err_l
+
+
+def oracle_rows(inp, w, b, g, t_rows, bounds=None, causal_offset=None):
+    """Oracle partials of selected query rows of one (batch, KV head):
+    o [n_split, len(t_rows), G, dv], lse [n_split, len(t_rows), G].  Used at full size,
+    where computing every row would be too slow on the host."""
+    G = w.Hq // w.Hkv
+    bounds = inp["split_bounds"] if bounds is None else bounds
+    causal = w.causal_offset if causal_offset is None else causal_offset
+    n_split = len(bounds[b]) - 1
+    seq = inp["seq_lens_host"][b]
+    t_rows = list(t_rows)
+    qb = q_f64(inp["q"][b, t_rows, g * G : (g + 1) * G])  # [R, G, dk]
+    kf = kv_f64(inp, w, "k", b, g)
+    vf = kv_f64(inp, w, "v", b, g)
+    R = len(t_rows)
+    o = np.zeros((n_split, R, G, w.dv))
+    lse = np.full((n_split, R, G), -np.inf)
+    q_pos = np.repeat(causal + np.asarray(t_rows, dtype=np.int64), G)
+    for j in range(n_split):
+        lo, hi = max(bounds[b][j], 0), min(bounds[b][j + 1], seq, w.S)
+        if hi <= lo:
+            continue
+        oo, ll = oracle.attend(qb.reshape(R * G, w.dk), kf[lo:hi], vf[lo:hi], w.scale, q_pos, np.arange(lo, hi))
+        o[j] = oo.reshape(R, G, w.dv)
+        lse[j] = ll.reshape(R, G)
+    return o, lse

@@ -1,0 +1,69 @@
+"""GPU parity at the workloads' full sizes, on sampled outputs the oracle computes one
+group at a time (every query head of a sampled KV head, at sampled query rows), in the
+launch configuration bench.py times (the fused gqa_decode_attn call) and through
+attn_partial + attn_merge_lse.  Bars as in test_gpu_parity_gqa.py."""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_decode_attention_gqa_gb300 as skv
+from mla_decode_attention_gqa_gb300 import workloads as W
+import oracle
+from tests import oracle_io as io
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+DEV = "cuda:0"
+
+
+def _check_groups(w, inp, out, lse, groups, t_rows, parts=None):
+    tol = io.tol_for(w)
+    G = w.Hq // w.Hkv
+    for b, g in groups:
+        ro_p, rl_p = io.oracle_rows(inp, w, b, g, t_rows)
+        ro, rl = oracle.merge_lse(ro_p, rl_p)
+        got_o = out[b, t_rows, g * G : (g + 1) * G]
+        got_l = lse[b, t_rows, g * G : (g + 1) * G]
+        io.assert_close(got_o, got_l, ro, rl, tol, f"merged b={b} g={g}")
+        if parts is not None:
+            po, pl = parts
+            io.assert_close(po[:, b, t_rows, g * G : (g + 1) * G], pl[:, b, t_rows, g * G : (g + 1) * G], ro_p, rl_p,
+                            tol, f"partials b={b} g={g}")
+
+
+def test_helix_dense_decode_full_size():
+    w = W.HELIX_DENSE_128K  # B=8 Hq=128 Hkv=8 d=128 S=131072 bf16
+    inp = W.make_inputs(w, DEV)
+    out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"],
+                                   softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    _check_groups(w, inp, out, lse, [(0, 0), (3, 5), (7, 7)], [0])
+
+
+def test_helix_kvp8_fp8_full_size():
+    w = W.HELIX_KVP8_FP8_1M  # fp8, S=2^20, 8 shards, ragged
+    inp = W.make_inputs(w, DEV)
+    kw = dict(k_scale=inp["k_scale"], v_scale=inp["v_scale"], softmax_scale=w.scale, scale_block=w.scale_block)
+    out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"], **kw)
+    po, pl = skv.attn_partial(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"], **kw)
+    mo, ml = skv.attn_merge_lse(po, pl)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    assert (mo.float() - out.float()).abs().max().item() <= 1e-2
+    # the sequence with the shortest and the one with the longest length, two KV heads each
+    seq = inp["seq_lens_host"]
+    bs = sorted(range(w.B), key=lambda b: seq[b])
+    _check_groups(w, inp, out, lse, [(bs[0], 0), (bs[-1], 7)], [0], parts=(po, pl))
+
+
+def test_ring_prefill_full_size_sampled_rows():
+    w = W.RING_PREFILL  # Tq=4096 over 8 x 4096 KV, causal on the diagonal
+    inp = W.make_inputs(w, DEV)
+    out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"],
+                                   w.causal_offset, softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    rows = [0, 1, 63, 64, 2047, 4094, 4095]
+    _check_groups(w, inp, out, lse, [(0, 0), (0, 7)], rows)
