@@ -88,6 +88,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ------------------------------------------------------------------ plan of a call
 
 struct Plan {
+  bool mla = false;
   GqaVariant variant;
   int rows_per_cta = 0;
   int m_tiles = 1;
@@ -96,6 +97,10 @@ struct Plan {
   int64_t n_items = 0;
   int n_part = 0;  // n_split * n_chunk
 };
+
+bool is_mla_shape(const skv_desc* d) {
+  return d->dk == 576 && d->dv == 512 && d->Hkv == 1 && d->kv_dtype == SKV_KV_BF16;
+}
 
 bool is_gqa_shape(const skv_desc* d) {
   if (d->dk != d->dv) return false;
@@ -136,9 +141,14 @@ skv_status validate(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
   }
   if (d->k_strides[2] < d->dk || d->v_strides[2] < d->dv)
     return fail(SKV_EINVAL, "K/V token stride must cover a whole head row");
-  if (!is_gqa_shape(d)) {
-    return fail(SKV_EUNSUPPORTED, "unsupported head dims / dtype: supported are bf16 dk=dv in {64,128} and "
-                                  "fp8-e4m3 dk=dv=128");
+  if (!is_gqa_shape(d) && !is_mla_shape(d)) {
+    return fail(SKV_EUNSUPPORTED, "unsupported head dims / dtype: supported are bf16 dk=dv in {64,128}, "
+                                  "fp8-e4m3 dk=dv=128, and the bf16 MLA latent (Hkv=1, dk=576, dv=512)");
+  }
+  if (is_mla_shape(d)) {
+    for (int i = 0; i < 3; ++i)
+      if (d->k_strides[i] != d->v_strides[i])
+        return fail(SKV_EINVAL, "MLA: v_cache must be the latent buffer itself (same strides as k_cache)");
   }
   return SKV_OK;
 }
@@ -149,6 +159,7 @@ skv_status validate_ptrs(const skv_desc* d, const void* q, const void* k, const 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
     return fail(SKV_EINVAL, "q, k_cache and v_cache must be 16-byte aligned");
   if (!aligned(seq_lens, 4)) return fail(SKV_EINVAL, "seq_lens must be 4-byte aligned");
+  if (is_mla_shape(d) && k != v) return fail(SKV_EINVAL, "MLA: v_cache must equal k_cache (V is the latent)");
   if (d->kv_dtype == SKV_KV_FP8_E4M3) {
     if (!ks || !vs) return fail(SKV_EINVAL, "fp8 KV needs k_scale and v_scale");
     if (!aligned(ks, 4) || !aligned(vs, 4)) return fail(SKV_EINVAL, "scales must be 4-byte aligned");
@@ -161,13 +172,14 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
   const int G = d->Hq / d->Hkv;
   const bool fp8 = d->kv_dtype == SKV_KV_FP8_E4M3;
   const bool decode = static_cast<int64_t>(d->Tq) * G <= 16;
+  pl.mla = is_mla_shape(d);
   if (fp8)
     pl.variant = decode ? GqaVariant::kFp8D128Decode : GqaVariant::kFp8D128Prefill;
   else if (d->dk == 64)
     pl.variant = decode ? GqaVariant::kBf16D64Decode : GqaVariant::kBf16D64Prefill;
   else
     pl.variant = decode ? GqaVariant::kBf16D128Decode : GqaVariant::kBf16D128Prefill;
-  const GqaLaunchInfo li = gqa_launch_info(pl.variant);
+  const GqaLaunchInfo li = pl.mla ? mla_launch_info() : gqa_launch_info(pl.variant);
   pl.rows_per_cta = li.rows_per_cta;
   const int64_t rows = static_cast<int64_t>(d->Tq) * G;
   pl.m_tiles = static_cast<int>((rows + li.rows_per_cta - 1) / li.rows_per_cta);
@@ -183,7 +195,7 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
     }
   }
   const int64_t base = static_cast<int64_t>(d->B) * d->Hkv * n_split * pl.m_tiles;
-  const int64_t slots = static_cast<int64_t>(device_sm_count()) * 2;  // 2 resident CTAs per SM
+  const int64_t slots = static_cast<int64_t>(device_sm_count()) * li.ctas_per_sm;  // resident CTAs
   pl.n_chunk = 1;
   pl.chunk_tiles = static_cast<int>(std::max<int64_t>(max_tiles, 1));
   if (max_tiles > 1 && base < 4 * slots) {
@@ -215,7 +227,8 @@ size_t ws_bytes_for(const skv_desc* d, int n_part) {
   return align_up(static_cast<size_t>(n_part) * rows * d->dv * 4, 256) + align_up(static_cast<size_t>(n_part) * rows * 4, 256);
 }
 
-skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, const int64_t* strides, int dim) {
+skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, const int64_t* strides, int dim,
+                         int box_rows) {
   cudaError_t e;
   auto encode = get_encode_fn(&e);
   if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
@@ -230,7 +243,7 @@ skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, 
   if (d->B == 1 || batch_b == 0) batch_b = std::max<int64_t>(batch_b, head_b * d->Hkv);
   cuuint64_t gstride[3] = {static_cast<cuuint64_t>(tok_b), static_cast<cuuint64_t>(head_b),
                            static_cast<cuuint64_t>(batch_b)};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kTileN), 1, 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                       const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -289,9 +302,17 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
                               zero_empty);
   if (st != SKV_OK) return st;
   CUtensorMap tmk, tmv;
-  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk)) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv)) != SKV_OK) return st;
-  cudaError_t e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
+  cudaError_t e;
+  if (pl.mla) {
+    // one latent map serves K (all 576 columns) and V (its first 512 columns)
+    if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kMlaTileN)) != SKV_OK) return st;
+    e = launch_mla_partial(p, tmk, pl.n_items, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "MLA partial attention launch");
+    return SKV_OK;
+  }
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN)) != SKV_OK) return st;
+  e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
   return SKV_OK;
 }

@@ -59,7 +59,9 @@ struct GqaCfg {
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
   static constexpr int BAR_BYTES = 2 * NSTAGE * 8;
   static constexpr int ML_BYTES = WN * ROWS * 2 * 4;
-  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + ML_BYTES;
+  // fp8 variants keep their fp16 q fragments in shared memory ([WM][D/16][32 lanes] x 16 B)
+  static constexpr int QF_BYTES = FP8 ? WM * (D / 16) * 32 * 16 : 0;
+  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + ML_BYTES + QF_BYTES;
   static_assert(ROW_BYTES % 128 == 0, "token rows must be whole 128-byte boxes");
   static_assert(WN == 1 || WN * ROWS * D * 4 <= RING_BYTES, "combine buffer must fit in the ring");
   static_assert(D % 16 == 0, "head dim must be a multiple of 16");
@@ -93,6 +95,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
   uint64_t* empty = full + NSTAGE;
   float* ml = reinterpret_cast<float*>(empty + NSTAGE);  // [WN][ROWS][2]
+  uint4* qfrag = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ml) + C::ML_BYTES);  // fp8 only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -174,8 +177,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int64_t hz0 = p.causal_offset + tq0, hz1 = p.causal_offset + tq1;
   const int64_t hz_min = p.causal_offset + (m0 + wm * 16) / p.G;
 
-  // ---- Q fragments (A operand, 16 rows x D)
-  uint32_t qa[D / 16][4];
+  // ---- Q fragments (A operand, 16 rows x D): registers for bf16, shared memory for fp8
+  uint32_t qa[C::FP8 ? 1 : D / 16][4];
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* q0 = q + b * p.q_sb + tq0 * p.q_st + h0 * p.q_sh;
@@ -205,13 +208,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
           const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
           f1[0] = __low2float(a); f1[1] = __high2float(a); f1[2] = __low2float(bb); f1[3] = __high2float(bb);
         }
-        qa[ks][0] = pack_f16(f0[0], f0[1]);
-        qa[ks][1] = pack_f16(f1[0], f1[1]);
-        qa[ks][2] = pack_f16(f0[2], f0[3]);
-        qa[ks][3] = pack_f16(f1[2], f1[3]);
+        if (wn == 0) {
+          qfrag[(wm * (D / 16) + ks) * 32 + lane] =
+              make_uint4(pack_f16(f0[0], f0[1]), pack_f16(f1[0], f1[1]), pack_f16(f0[2], f0[3]),
+                         pack_f16(f1[2], f1[3]));
+        }
       }
     }
   }
+  if constexpr (C::FP8) named_bar_sync(1, C::NCW * 32);  // q fragments visible to every consumer
 
   float o[D / 8][4];
 #pragma unroll
@@ -258,16 +263,20 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     } else {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ks += 2) {
+        const uint4 qv0 = qfrag[(wm * (D / 16) + ks) * 32 + lane];
+        const uint4 qv1 = qfrag[(wm * (D / 16) + ks + 1) * 32 + lane];
+        const uint32_t qa0[4] = {qv0.x, qv0.y, qv0.z, qv0.w};
+        const uint32_t qa1[4] = {qv1.x, qv1.y, qv1.z, qv1.w};
 #pragma unroll
         for (int np = 0; np < TN / 16; ++np) {
           const uint32_t tok = 16 * np + (mi >> 1) * 8 + (lane & 7);
           const uint32_t byte = (ks + (mi & 1)) * 16;
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
-          mma_f16(sc[2 * np], qa[ks], e4m3x2_to_f16x2(r0 & 0xFFFF), e4m3x2_to_f16x2(r0 >> 16));
-          mma_f16(sc[2 * np], qa[ks + 1], e4m3x2_to_f16x2(r1 & 0xFFFF), e4m3x2_to_f16x2(r1 >> 16));
-          mma_f16(sc[2 * np + 1], qa[ks], e4m3x2_to_f16x2(r2 & 0xFFFF), e4m3x2_to_f16x2(r2 >> 16));
-          mma_f16(sc[2 * np + 1], qa[ks + 1], e4m3x2_to_f16x2(r3 & 0xFFFF), e4m3x2_to_f16x2(r3 >> 16));
+          mma_f16(sc[2 * np], qa0, e4m3x2_to_f16x2(r0 & 0xFFFF), e4m3x2_to_f16x2(r0 >> 16));
+          mma_f16(sc[2 * np], qa1, e4m3x2_to_f16x2(r1 & 0xFFFF), e4m3x2_to_f16x2(r1 >> 16));
+          mma_f16(sc[2 * np + 1], qa0, e4m3x2_to_f16x2(r2 & 0xFFFF), e4m3x2_to_f16x2(r2 >> 16));
+          mma_f16(sc[2 * np + 1], qa1, e4m3x2_to_f16x2(r3 & 0xFFFF), e4m3x2_to_f16x2(r3 >> 16));
         }
       }
     }
@@ -303,12 +312,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       mrun[r] = mnew;
       lrun[r] *= alpha[r];
     }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row max moved
 #pragma unroll
-    for (int i2 = 0; i2 < D / 8; ++i2) {
-      o[i2][0] *= alpha[0];
-      o[i2][1] *= alpha[0];
-      o[i2][2] *= alpha[1];
-      o[i2][3] *= alpha[1];
+      for (int i2 = 0; i2 < D / 8; ++i2) {
+        o[i2][0] *= alpha[0];
+        o[i2][1] *= alpha[0];
+        o[i2][2] *= alpha[1];
+        o[i2][3] *= alpha[1];
+      }
     }
     uint32_t pa[TN / 16][4];
 #pragma unroll
@@ -487,7 +498,7 @@ using CfgFp8D128Pre = GqaCfg<true, 128, 4, 1, 6, 2>;
 
 template <class C>
 GqaLaunchInfo info_of() {
-  return GqaLaunchInfo{C::ROWS, C::THREADS, C::SMEM};
+  return GqaLaunchInfo{C::ROWS, C::THREADS, C::SMEM, C::MINB};
 }
 
 template <class C>
@@ -515,7 +526,7 @@ GqaLaunchInfo gqa_launch_info(GqaVariant v) {
     case GqaVariant::kBf16D128Prefill: return info_of<CfgBf16D128Pre>();
     case GqaVariant::kFp8D128Prefill: return info_of<CfgFp8D128Pre>();
   }
-  return GqaLaunchInfo{0, 0, 0};
+  return GqaLaunchInfo{0, 0, 0, 1};
 }
 
 cudaError_t launch_gqa_partial(GqaVariant v, const PartialParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,

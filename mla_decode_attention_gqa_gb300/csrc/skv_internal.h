@@ -57,12 +57,19 @@ struct GqaLaunchInfo {
   int rows_per_cta;  // M rows handled by one CTA
   int threads;
   int smem_bytes;
+  int ctas_per_sm;  // resident CTAs per SM the variant is built for
 };
 
 GqaLaunchInfo gqa_launch_info(GqaVariant v);
 
 cudaError_t launch_gqa_partial(GqaVariant v, const PartialParams& p, const CUtensorMap& tmk,
                                const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream);
+
+// MLA latent variant (dk = 576 latent+rope, dv = 512, one shared latent "head").
+// Tiles are 32 tokens; the tensor map's box is 64 elements x 32 tokens.
+constexpr int kMlaTileN = 32;
+GqaLaunchInfo mla_launch_info();
+cudaError_t launch_mla_partial(const PartialParams& p, const CUtensorMap& tmk, int64_t n_items, cudaStream_t stream);
 
 // Merge n_in partials per output group: in_o [G_out][n_in][R][dv], in_lse [G_out][n_in][R]
 // -> out [G_out][R][dv] (fp32 or bf16) and out_lse [G_out][R].

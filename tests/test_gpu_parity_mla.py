@@ -1,0 +1,68 @@
+"""GPU parity of the MLA latent-cache variant (Hkv = 1, key = 576-dim latent+rope row,
+value = its first 512 dims, 128 query heads) against the fp64 oracle.
+Bars: bf16 out max-abs <= 1e-2, lse <= 1e-3."""
+
+import pytest
+import torch
+
+import mla_decode_attention_gqa_gb300 as skv
+from mla_decode_attention_gqa_gb300 import workloads as W
+import oracle
+from tests import oracle_io as io
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _all_paths(w, inp, bounds=None):
+    bounds = inp["split_bounds"] if bounds is None else bounds
+    kw = dict(softmax_scale=w.scale)
+    o_p, l_p = skv.attn_partial(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, **kw)
+    o_m, l_m = skv.attn_merge_lse(o_p, l_p)
+    o_f, l_f = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, **kw)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    ro_p, rl_p = io.oracle_all(inp, w, bounds)
+    ro, rl = oracle.merge_lse(ro_p, rl_p)
+    io.assert_close(o_p, l_p, ro_p, rl_p, io.TOL_BF16, "partials")
+    io.assert_close(o_m, l_m, ro, rl, io.TOL_BF16, "merged")
+    io.assert_close(o_f, l_f, ro, rl, io.TOL_BF16, "fused")
+
+
+def test_mla_absorbed_small_s():
+    w = W.scaled(W.MLA_ABSORBED, B=2, S=2048)
+    _all_paths(w, W.make_inputs(w, DEV))
+
+
+def test_mla_ragged_tail_and_odd_splits():
+    w = W.scaled(W.MLA_ABSORBED, B=2, S=1000, n_split=3)
+    inp = W.make_inputs(w, DEV)
+    _all_paths(w, inp, bounds=[[0, 333, 334, 1000], [17, 500, 900, 990]])
+
+
+def test_mla_fewer_heads_partial_row_tile():
+    # 96 heads: the second 64-head tile of each item is half empty
+    w = W.scaled(W.MLA_ABSORBED, B=1, Hq=96, S=640, n_split=2)
+    _all_paths(w, W.make_inputs(w, DEV))
+
+
+def test_mla_ragged_lengths_with_nan_past_the_end():
+    w = W.scaled(W.MLA_ABSORBED, B=3, S=1500, ragged=True)
+    inp = W.make_inputs(w, DEV)
+    assert min(inp["seq_lens_host"]) < w.S
+    _all_paths(w, inp)
+
+
+@pytest.mark.slow
+def test_mla_absorbed_full_size_sampled():
+    w = W.MLA_ABSORBED  # B=16, Hq=128, latent 576 (V 512), S=32768, 4 splits
+    inp = W.make_inputs(w, DEV)
+    out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"],
+                                   softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    for b in (0, 15):
+        ro_p, rl_p = io.oracle_rows(inp, w, b, 0, [0])
+        ro, rl = oracle.merge_lse(ro_p, rl_p)
+        io.assert_close(out[b, [0]], lse[b, [0]], ro, rl, io.TOL_BF16, f"b={b}")
