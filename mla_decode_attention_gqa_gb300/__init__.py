@@ -40,6 +40,9 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attn_noalloc",
 )
 
+# Every symbol declared in include/splitkv_attn_selftest.h (hardware self-tests).
+SELFTEST_SYMBOLS = ("splitkv_selftest_umma_gemm",)
+
 
 class SkvDesc(ctypes.Structure):
     _fields_ = [

@@ -13,6 +13,7 @@
 #include <string>
 
 #include "../../include/splitkv_attn.h"
+#include "../../include/splitkv_attn_selftest.h"
 #include "skv_internal.h"
 
 // Device error word written by kernels whose bounded waits gave up.
@@ -257,6 +258,28 @@ skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, 
   return SKV_OK;
 }
 
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per row,
+// `outer` rows `row_bytes` apart, box of box_inner x box_outer.
+skv_status encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                          uint32_t box_inner, uint32_t box_outer) {
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (2-D) failed (CUresult %d)", static_cast<int>(r));
+    return fail(SKV_ECUDA, buf);
+  }
+  return SKV_OK;
+}
+
 // Fill the launch parameters common to every GQA partial launch.
 skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, const void* q, const float* ks,
                        const float* vs, const int32_t* seq_lens, const int32_t* bounds, int32_t n_split,
@@ -333,6 +356,27 @@ skv_status splitkv_device_error(uint32_t* code) {
   e = cudaMemcpyToSymbol(g_skv_device_error, &zero, sizeof(zero));
   if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
   *code = v;
+  return SKV_OK;
+}
+
+skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, int32_t N, int32_t b_mn_major,
+                                      void* stream) {
+  if (!A || !B || !C) return fail(SKV_EINVAL, "A, B and C must be non-NULL");
+  if (N != 64 && N != 128) return fail(SKV_EINVAL, "N must be 64 or 128");
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return fail(SKV_EINVAL, "pointers must be 16-byte aligned");
+  CUtensorMap ta, tb;
+  skv_status st = encode_2d_bf16(&ta, A, 64, 128, 128, 64, 128);
+  if (st != SKV_OK) return st;
+  if (b_mn_major)
+    st = encode_2d_bf16(&tb, B, static_cast<uint64_t>(N), 64, static_cast<uint64_t>(N) * 2, 64, 64);
+  else
+    st = encode_2d_bf16(&tb, B, 64, static_cast<uint64_t>(N), 128, 64, static_cast<uint32_t>(N));
+  if (st != SKV_OK) return st;
+  cudaError_t e;
+  unsigned int* err = device_error_word(&e);
+  if (!err) return cuda_fail(e, "device error word");
+  e = launch_umma_selftest(ta, tb, C, N, b_mn_major != 0, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 self-test launch");
   return SKV_OK;
 }
 

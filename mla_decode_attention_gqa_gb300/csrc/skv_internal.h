@@ -71,6 +71,10 @@ constexpr int kMlaTileN = 32;
 GqaLaunchInfo mla_launch_info();
 cudaError_t launch_mla_partial(const PartialParams& p, const CUtensorMap& tmk, int64_t n_items, cudaStream_t stream);
 
+// tcgen05 self-test GEMM (see umma_selftest.cu).
+cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, float* C, int N, bool b_mn_major,
+                                 unsigned int* err, cudaStream_t stream);
+
 // Merge n_in partials per output group: in_o [G_out][n_in][R][dv], in_lse [G_out][n_in][R]
 // -> out [G_out][R][dv] (fp32 or bf16) and out_lse [G_out][R].
 cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, int32_t g_out, int64_t R,

@@ -11,10 +11,11 @@ import mla_decode_attention_gqa_gb300 as skv
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "splitkv_attn.h")
+SELFTEST_HEADER = os.path.join(ROOT, "include", "splitkv_attn_selftest.h")
 
 
-def _declared_functions():
-    text = open(HEADER).read()
+def _declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?[\s\*]+([A-Za-z_]\w*)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "defined")))
@@ -24,9 +25,13 @@ def test_header_declares_the_binding_symbols():
     assert _declared_functions() == sorted(skv.EXPORTED_SYMBOLS)
 
 
+def test_selftest_header_declares_the_selftest_symbols():
+    assert _declared_functions(SELFTEST_HEADER) == sorted(skv.SELFTEST_SYMBOLS)
+
+
 def test_library_exports_every_declared_symbol():
     lib = skv.load_library()
-    for name in _declared_functions():
+    for name in _declared_functions() + _declared_functions(SELFTEST_HEADER):
         assert hasattr(lib, name), name
     assert skv.version() == (1, 0)
 
