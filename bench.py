@@ -432,11 +432,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--S", type=int, default=None, help="smaller KV length of the same workload (profiling)")
     ap.add_argument("--B", type=int, default=None, help="smaller batch of the same workload (profiling)")
+    ap.add_argument("--Tq", type=int, default=None, help="fewer query rows of the same workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = workload_by_name(args.config)
-    over = {k: v for k, v in (("S", args.S), ("B", args.B)) if v is not None}
+    over = {k: v for k, v in (("S", args.S), ("B", args.B), ("Tq", args.Tq)) if v is not None}
     if over:
         w = W.scaled(w, **over)
     ws, rank, local = dist_setup()

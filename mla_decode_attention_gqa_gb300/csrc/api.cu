@@ -223,6 +223,15 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Shapes served by the tensor-core (tcgen05) attention kernel: bf16 KV, dk = dv = 128,
+// G dividing 128 and at least one full 128-row query tile per KV head.
+bool use_tc(const skv_desc* d) {
+  if (d->kv_dtype != SKV_KV_BF16 || d->dk != 128 || d->dv != 128) return false;
+  const int G = d->Hq / d->Hkv;
+  if (G > 128 || 128 % G) return false;
+  return static_cast<int64_t>(d->Tq) * G >= 128;
+}
+
 size_t ws_bytes_for(const skv_desc* d, int n_part) {
   const size_t rows = static_cast<size_t>(d->B) * d->Tq * d->Hq;
   return align_up(static_cast<size_t>(n_part) * rows * d->dv * 4, 256) + align_up(static_cast<size_t>(n_part) * rows * 4, 256);
@@ -316,6 +325,61 @@ skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, cons
   return SKV_OK;
 }
 
+// Query tensor map for the tensor-core kernel: dims (d, head, row, batch), box
+// (64, G, 128/G, 1) so that one box is a 128-row x 128-byte K-major tile.
+skv_status encode_q_map(CUtensorMap* map, const void* q, const skv_desc* d) {
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
+  const int G = d->Hq / d->Hkv;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(d->dk), static_cast<cuuint64_t>(d->Hq),
+                        static_cast<cuuint64_t>(d->Tq), static_cast<cuuint64_t>(d->B)};
+  int64_t sh = d->q_strides[2] * 2, st = d->q_strides[1] * 2, sb = d->q_strides[0] * 2;
+  if (sh == 0) sh = d->dk * 2;
+  if (d->Tq == 1 || st == 0) st = std::max<int64_t>(st, sh * d->Hq);
+  if (d->B == 1 || sb == 0) sb = std::max<int64_t>(sb, st * d->Tq);
+  cuuint64_t gstride[3] = {static_cast<cuuint64_t>(sh), static_cast<cuuint64_t>(st), static_cast<cuuint64_t>(sb)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), gdim, gstride, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (q) failed (CUresult %d)", static_cast<int>(r));
+    return fail(SKV_ECUDA, buf);
+  }
+  return SKV_OK;
+}
+
+// Tensor-core path: fused = one pass over every split (final bf16 out + lse), else one
+// fp32 partial per split straight into out_o / out_lse.
+skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                  const int32_t* bounds, int32_t n_split, int64_t causal_offset, bool fused, float* out_o,
+                  float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream) {
+  static thread_local PartialParams p;
+  Plan pl;
+  pl.n_chunk = 1;
+  pl.chunk_tiles = 1;
+  const int rows = tc_attn_rows_per_cta();
+  pl.m_tiles = static_cast<int>((static_cast<int64_t>(d->Tq) * (d->Hq / d->Hkv) + rows - 1) / rows);
+  skv_status st = fill_params(&p, d, pl, q, nullptr, nullptr, seq_lens, bounds, n_split, causal_offset, out_o,
+                              out_lse, true);
+  if (st != SKV_OK) return st;
+  TcAttnExtra x;
+  x.fused = fused ? 1 : 0;
+  x.out_bf16 = out_bf16;
+  x.out_lse = lse_final;
+  CUtensorMap tmq, tmk, tmv;
+  if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN)) != SKV_OK) return st;
+  const int64_t n_items = static_cast<int64_t>(d->B) * d->Hkv * (fused ? 1 : n_split) * pl.m_tiles;
+  cudaError_t e = launch_tc_attn(p, x, tmq, tmk, tmv, n_items, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core attention launch");
+  return SKV_OK;
+}
+
 skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const void* k, const void* v,
                        const float* ks, const float* vs, const int32_t* seq_lens, const int32_t* bounds,
                        int32_t n_split, int64_t causal_offset, float* out_o, float* out_lse, bool zero_empty,
@@ -385,6 +449,10 @@ skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* spli
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
+  if (use_tc(desc)) {
+    *bytes = 0;
+    return SKV_OK;
+  }
   const Plan pl = make_plan(desc, split_bounds, n_split);
   *bytes = pl.n_chunk > 1 ? ws_bytes_for(desc, pl.n_part) : 0;
   return SKV_OK;
@@ -399,8 +467,12 @@ skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
   if (!out_partial || !lse_partial) return fail(SKV_EINVAL, "out_partial and lse_partial must be non-NULL");
   if (!aligned(out_partial, 16) || !aligned(lse_partial, 4)) return fail(SKV_EINVAL, "outputs misaligned");
-  const Plan pl = make_plan(desc, split_bounds, n_split);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_tc(desc)) {
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, false, out_partial,
+                  lse_partial, nullptr, nullptr, s);
+  }
+  const Plan pl = make_plan(desc, split_bounds, n_split);
   if (pl.n_chunk == 1) {
     return run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
                        causal_offset, out_partial, lse_partial, true, s);
@@ -440,6 +512,10 @@ skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, const int32_t* s
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
+  if (use_tc(desc)) {  // the tensor-core path merges the splits on the fly: no partials
+    *bytes = 0;
+    return SKV_OK;
+  }
   const Plan pl = make_plan(desc, split_bounds, n_split);
   *bytes = ws_bytes_for(desc, pl.n_part);
   return SKV_OK;
@@ -454,11 +530,16 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
   if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
   if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_tc(desc)) {
+    if (!aligned(out, 16)) return fail(SKV_EINVAL, "out must be 16-byte aligned for this shape");
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, true, nullptr, nullptr,
+                  out, lse, s);
+  }
   const Plan pl = make_plan(desc, split_bounds, n_split);
   const size_t need = ws_bytes_for(desc, pl.n_part);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
     return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_workspace_size()");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
   float* ws_o = static_cast<float*>(workspace);
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +

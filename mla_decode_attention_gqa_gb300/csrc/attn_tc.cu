@@ -1,0 +1,415 @@
+// Tensor-core (tcgen05) split-KV attention for query tiles of 128+ rows: the ring
+// pass-KV prefill chunk and any GQA call with Tq * G >= 128 rows per KV head.
+//
+// What it computes: for each row (query row t, query head h of KV head g), exact softmax
+// attention over the visible tokens of a range, as a normalised output plus its
+// natural-log LSE -- per split ("Context Parallelism for Scalable Million-Token
+// Inference", section "Pass-KV keeps queries local and circulates keys and values": each
+// ring step's partial attention keeps a log-sum-exp), or over the union of all splits
+// at once, which equals their exact LSE merge (the same page's merge equation: the online
+// softmax below performs that merge tile by tile).  Causal visibility is by original
+// position ("现代大模型推理并行策略总览", section "序列布局"): row t sees token p iff
+// p <= causal_offset + t.
+//
+// GB300 design (one CTA per SM):
+//   * a CTA owns 256 rows = two 128-row query tiles of one KV head; rows are (query row,
+//     head) pairs, so a K/V tile read once serves the whole GQA group and both tiles;
+//   * warp 0: TMA producer (Q tiles once, 64-token K/V tiles into a 3-stage ring);
+//     warp 1: allocates 512 TMEM columns and issues every tcgen05.mma from one thread;
+//     warps 2-5 and 6-9: softmax for query tile 0 and 1, one thread per row (the TMEM lane
+//     of its row), so row max / sum need no shuffles;
+//   * TMEM: S0 | S1 (128 x 64 fp32 each) | O0 | O1 (128 x 128 fp32 each);
+//     P (bf16) goes through 128-byte-swizzled shared memory as the A operand of P V;
+//   * MMA order per KV tile: PV0(i), S0(i+1), PV1(i), S1(i+1), so each softmax group works
+//     while the tensor core serves the other group;
+//   * O is rescaled (TMEM load / scale / store) only when a row's running max rises by
+//     more than 2^8; otherwise p = 2^(s - m_used) <= 256 stays exact enough in bf16.
+#include <cuda_runtime.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+#include "tc_common.cuh"
+
+namespace skv {
+
+namespace {
+
+constexpr int kD = 128;         // dk = dv
+constexpr int kTN = 64;         // tokens per K/V tile
+constexpr int kNStage = 3;      // K/V ring depth
+constexpr int kRowsTile = 128;  // rows per query tile (MMA M)
+constexpr int kThreads = 10 * 32;
+constexpr int kQTileBytes = kRowsTile * kD * 2;  // 32 KB (two 16 KB boxes)
+constexpr int kKVBoxBytes = kTN * 128;           // 8 KB
+constexpr int kKTileBytes = 2 * kKVBoxBytes;     // 16 KB
+constexpr int kStageBytes = 2 * kKTileBytes;     // K + V
+constexpr int kPTileBytes = kRowsTile * kTN * 2;  // 16 KB
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
+constexpr int kOffP = kOffRing + kNStage * kStageBytes;
+constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+constexpr int kSmem = 1024 + kOffBar + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // S_k at kColS + 64 k
+constexpr uint32_t kColO = 128;  // O_k at kColO + 128 k
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kNStage];
+  uint64_t kv_empty[kNStage];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void tma_load_4d_nohint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                   int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_attn_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
+                   const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: (b, g, [split j,] 256-row tile mt)
+  int64_t item = blockIdx.x;
+  const int mt = static_cast<int>(item % p.m_tiles);
+  item /= p.m_tiles;
+  int j = 0;
+  if (!x.fused) {
+    j = static_cast<int>(item % p.n_split);
+    item /= p.n_split;
+  }
+  const int g = static_cast<int>(item % p.Hkv);
+  const int b = static_cast<int>(item / p.Hkv);
+  const int G = p.G;
+  const int seq_len = p.seq_lens[b];
+  const int* bnd = p.bounds + b * (p.n_split + 1);
+  const int lo = max(x.fused ? bnd[0] : bnd[j], 0);
+  int hi = min(min(x.fused ? bnd[p.n_split] : bnd[j + 1], seq_len), p.S_max);
+  const int rows_total = p.Tq * G;
+  const int m0 = mt * 2 * kRowsTile;
+  const int m_last = min(m0 + 2 * kRowsTile, rows_total) - 1;
+  {
+    const int64_t horizon = p.causal_offset + m_last / G;
+    if (horizon < static_cast<int64_t>(hi) - 1) hi = static_cast<int>(max(horizon + 1, (int64_t)lo));
+  }
+  const int r_lo = lo, r_hi = hi;
+  const int tile_begin = r_lo / kTN;
+  const int n_tiles = (r_hi > r_lo) ? ((r_hi + kTN - 1) / kTN - tile_begin) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kNStage; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bars->s_full[k], 1);
+      mbar_init(&bars->p_full[k], kRowsTile);
+      mbar_init(&bars->pv_done[k], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * kQTileBytes);
+      for (int k = 0; k < 2; ++k) {
+        const int t_start = (m0 + k * kRowsTile) / G;
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_4d_nohint(smem + kOffQ + k * kQTileBytes + bx * (kQTileBytes / 2), &tmq, &bars->q_full, bx * 64,
+                             g * G, t_start, b);
+      }
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kNStage;
+        if (i >= kNStage && !mbar_wait(&bars->kv_empty[s], ((i / kNStage) - 1) & 1, p.err, kDevErrEmptyWait)) break;
+        mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
+        uint8_t* st = smem + kOffRing + s * kStageBytes;
+        const int tok = (tile_begin + i) * kTN;
+        for (int bx = 0; bx < 2; ++bx) {
+          tma_load_4d_nohint(st + bx * kKVBoxBytes, &tmk, &bars->kv_full[s], bx * 64, tok, g, b);
+          tma_load_4d_nohint(st + kKTileBytes + bx * kKVBoxBytes, &tmv, &bars->kv_full[s], bx * 64, tok, g, b);
+        }
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kNStage); i < issued; ++i) {
+        if (!mbar_wait(&bars->kv_full[i % kNStage], (i / kNStage) & 1, p.err, kDevErrDrainWait)) break;
+      }
+      mbar_wait(&bars->q_full, 0, p.err, kDevErrDrainWait);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
+      const uint32_t idesc_pv = tc::idesc_f16(128, kD, true, false, true);
+      const uint32_t q_base = smem_u32(smem + kOffQ);
+      const uint32_t ring = smem_u32(smem + kOffRing);
+      const uint32_t p_base = smem_u32(smem + kOffP);
+      bool ok = mbar_wait(&bars->q_full, 0, p.err, kDevErrFullWait);
+      auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 64, K 128)
+        const uint32_t kt = ring + (i % kNStage) * kStageBytes;
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t ad =
+              tc::smem_desc_sw128(q_base + k * kQTileBytes + (ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(kt + (ks >> 2) * kKVBoxBytes + (ks & 3) * 32, 16, 1024);
+          tc::mma_f16_ss(tmem + kColS + 64 * k, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int k, int i) {  // O_k += P_k V_i  (M 128, N 128, K 64)
+        const uint32_t vt = ring + (i % kNStage) * kStageBytes + kKTileBytes;
+        for (int ks = 0; ks < kTN / 16; ++ks) {
+          const uint64_t ad = tc::smem_desc_sw128(p_base + k * kPTileBytes + ks * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(vt + ks * 2048, kKVBoxBytes, 1024);
+          tc::mma_f16_ss(tmem + kColO + 128 * k, ad, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, p.err, kDevErrFullWait);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0, 0);
+        tc::mma_commit(smem_u32(&bars->s_full[0]));
+        issue_s(1, 0);
+        tc::mma_commit(smem_u32(&bars->s_full[1]));
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          ok = mbar_wait(&bars->p_full[0], i & 1, p.err, kDevErrFullWait);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(0, i);
+          tc::mma_commit(smem_u32(&bars->pv_done[0]));
+          if (i + 1 < n_tiles) {
+            ok = mbar_wait(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1, p.err, kDevErrFullWait);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_s(0, i + 1);
+            tc::mma_commit(smem_u32(&bars->s_full[0]));
+          }
+          ok = mbar_wait(&bars->p_full[1], i & 1, p.err, kDevErrFullWait);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(1, i);
+          tc::mma_commit(smem_u32(&bars->pv_done[1]));
+          tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
+          if (i + 1 < n_tiles) {
+            issue_s(1, i + 1);
+            tc::mma_commit(smem_u32(&bars->s_full[1]));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int k = (warp - 2) >> 2;                 // query tile 0 or 1
+    const int lgrp = warp & 3;                     // TMEM lane group of this warp
+    const int row = lgrp * 32 + lane;              // row inside the query tile
+    const int m = m0 + k * kRowsTile + row;        // row of KV head g's row space
+    const bool valid = m < rows_total;
+    const int t_q = valid ? m / G : 0;
+    const int h = g * G + (valid ? m % G : 0);
+    const int64_t hz = p.causal_offset + t_q;
+    const int64_t hz_min = p.causal_offset + (m0 + k * kRowsTile + lgrp * 32) / G;  // smallest in this warp
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
+    uint8_t* p_tile = smem + kOffP + k * kPTileBytes;
+    float m_used = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+
+    for (int i = 0; i < n_tiles && ok; ++i) {
+      const int t0 = (tile_begin + i) * kTN;
+      ok = mbar_wait(&bars->s_full[k], i & 1, p.err, kDevErrFullWait);
+      if (!ok) break;
+      tc::fence_after_sync();
+      float s[kTN];
+#pragma unroll
+      for (int c = 0; c < kTN / 16; ++c) {
+        uint32_t r[16];
+        tc::tmem_ld16(t_lane + kColS + 64 * k + 16 * c, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) s[16 * c + e] = __uint_as_float(r[e]);
+      }
+      const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
+      const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTN; ++c) {
+        float y = s[c] * p.scale_log2;
+        if (need_mask) {
+          const int tok = t0 + c;
+          const bool vis = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
+          y = vis ? y : -INFINITY;
+        }
+        s[c] = y;
+        tmax = fmaxf(tmax, y);
+      }
+      const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
+      const float m_new = need ? fmaxf(m_used, tmax) : m_used;
+      bool pv_waited = false;
+      if (i > 0 && __any_sync(0xffffffffu, need)) {
+        ok = mbar_wait(&bars->pv_done[k], (i - 1) & 1, p.err, kDevErrFullWait);
+        pv_waited = true;
+        tc::fence_after_sync();
+        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t r[16];
+          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * c, r);
+        }
+        tc::tmem_wait_st();
+        l_sum *= alpha;
+      } else if (need) {
+        l_sum = 0.f;  // first visible tile of this row (nothing accumulated yet)
+      }
+      m_used = m_new;
+      const float base = (m_used == -INFINITY) ? 0.f : m_used;
+      if (i > 0 && !pv_waited) {  // P buffer is free once PV of the previous tile is done
+        ok = mbar_wait(&bars->pv_done[k], (i - 1) & 1, p.err, kDevErrFullWait);
+      }
+      // p = 2^(s - m_used) -> bf16 into the swizzled K-major P tile (row = query row)
+#pragma unroll
+      for (int cc = 0; cc < kTN / 8; ++cc) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pv[e] = fast_exp2(s[8 * cc + e] - base);
+          l_sum += pv[e];
+        }
+        const uint4 v = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                                   pack_bf16(pv[6], pv[7]));
+        *reinterpret_cast<uint4*>(p_tile + swz128(row, cc * 16)) = v;
+      }
+      if (k == 0 && !in_range) {
+        // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
+        // zero their V rows so that p = 0 really contributes nothing
+        const int tid = lgrp * 32 + lane;
+        const int s_idx = i % kNStage;
+        mbar_wait(&bars->kv_full[s_idx], (i / kNStage) & 1, p.err, kDevErrFullWait);
+        if (tid < kTN) {
+          const int tok = t0 + tid;
+          if (tok < r_lo || tok >= r_hi) {
+            uint8_t* vt = smem + kOffRing + s_idx * kStageBytes + kKTileBytes;
+            for (int bx = 0; bx < 2; ++bx)
+              for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4*>(vt + bx * kKVBoxBytes + tid * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->p_full[k]);
+    }
+
+    // ---- epilogue: O / l and lse
+    if (n_tiles > 0 && ok) {
+      ok = mbar_wait(&bars->pv_done[k], (n_tiles - 1) & 1, p.err, kDevErrFullWait);
+      tc::fence_after_sync();
+    }
+    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    constexpr float kLn2 = 0.6931471805599453f;
+    const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+    if (x.fused) {
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(x.out_bf16) +
+                            ((static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h) * kD;
+#pragma unroll 1
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t r[16];
+        if (n_tiles > 0) {
+          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = 0u;
+        }
+        if (valid) {
+          uint4 w0, w1;
+          w0.x = pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+          w0.y = pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+          w0.z = pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+          w0.w = pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+          w1.x = pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+          w1.y = pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+          w1.z = pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+          w1.w = pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
+          *reinterpret_cast<uint4*>(orow + 16 * c) = w0;
+          *reinterpret_cast<uint4*>(orow + 16 * c + 8) = w1;
+        }
+      }
+      if (valid) x.out_lse[(static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h] = lse;
+    } else {
+      const int64_t ro = ((static_cast<int64_t>(j) * p.B + b) * p.Tq + t_q) * p.Hq + h;
+      float* orow = p.out_o + ro * kD;
+      const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
+#pragma unroll 1
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t r[16];
+        if (n_tiles > 0) {
+          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = 0u;
+        }
+        if (write_o) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(orow + 16 * c + e) =
+                make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                            __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+        }
+      }
+      if (valid) p.out_lse[ro] = lse;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+int tc_attn_rows_per_cta() { return 2 * kRowsTile; }
+
+cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
+                           const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (n_items <= 0) return cudaSuccess;
+  tc_attn_kernel<<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

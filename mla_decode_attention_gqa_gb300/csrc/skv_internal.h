@@ -71,6 +71,19 @@ constexpr int kMlaTileN = 32;
 GqaLaunchInfo mla_launch_info();
 cudaError_t launch_mla_partial(const PartialParams& p, const CUtensorMap& tmk, int64_t n_items, cudaStream_t stream);
 
+// Tensor-core (tcgen05) attention for query tiles of >= 128 rows (see attn_tc.cu):
+// bf16 KV, dk = dv = 128, G = Hq / Hkv dividing 128.  Work item = (b, g, [split j,]
+// 256-row tile); `fused` processes the union of all splits and writes the final bf16
+// output and lse, otherwise one fp32 partial per split goes to p.out_o / p.out_lse.
+struct TcAttnExtra {
+  int32_t fused;
+  void* out_bf16;
+  float* out_lse;
+};
+int tc_attn_rows_per_cta();
+cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
+                           const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream);
+
 // tcgen05 self-test GEMM (see umma_selftest.cu).
 cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, float* C, int N, bool b_mn_major,
                                  unsigned int* err, cudaStream_t stream);

@@ -83,9 +83,9 @@ WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_P
 
 def scaled(w: Workload, **kw) -> Workload:
     """A smaller workload of the same structure (for parity at oracle-friendly sizes)."""
-    if "S" in kw and "causal_offset" not in kw and w.causal_offset != NO_CAUSAL:
+    if ("S" in kw or "Tq" in kw) and "causal_offset" not in kw and w.causal_offset != NO_CAUSAL:
         # keep the Q chunk at the end of the KV so the last split is the diagonal
-        kw["causal_offset"] = kw["S"] - kw.get("Tq", w.Tq)
+        kw["causal_offset"] = kw.get("S", w.S) - kw.get("Tq", w.Tq)
     return replace(w, **kw)
 
 
