@@ -21,13 +21,15 @@ extern "C" {
 /*
  * splitkv_selftest_umma_gemm -- C[128][N] = A[128][64] * op(B) in fp32 on one CTA.
  *   A  bf16 [128][64] row-major (device, 16-byte aligned)
- *   B  bf16; b_mn_major == 0: [N][64] row-major and op(B) = B^T (both operands K-major);
- *            b_mn_major != 0: [64][N] row-major and op(B) = B (B is MN-major)
+ *   B  bf16; (flags & 1) == 0: [N][64] row-major and op(B) = B^T (both operands K-major);
+ *            (flags & 1) != 0: [64][N] row-major and op(B) = B (B is MN-major)
  *   C  fp32 [128][N] row-major (device)
  *   N  64 or 128
+ *   flags  bit 0: B MN-major; bit 1: the MMA reads A from tensor memory (copied there from
+ *          the shared-memory tile) instead of from shared memory
  * Asynchronous on `stream`; returns SKV_EINVAL for bad arguments, SKV_ECUDA on launch errors.
  */
-skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, int32_t N, int32_t b_mn_major,
+skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, int32_t N, int32_t flags,
                                       void* stream);
 
 #ifdef __cplusplus

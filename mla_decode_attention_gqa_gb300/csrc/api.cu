@@ -423,8 +423,10 @@ skv_status splitkv_device_error(uint32_t* code) {
   return SKV_OK;
 }
 
-skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, int32_t N, int32_t b_mn_major,
+skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, int32_t N, int32_t flags,
                                       void* stream) {
+  const int32_t b_mn_major = flags & 1;
+  const bool a_tmem = (flags & 2) != 0;
   if (!A || !B || !C) return fail(SKV_EINVAL, "A, B and C must be non-NULL");
   if (N != 64 && N != 128) return fail(SKV_EINVAL, "N must be 64 or 128");
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return fail(SKV_EINVAL, "pointers must be 16-byte aligned");
@@ -439,7 +441,7 @@ skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, in
   cudaError_t e;
   unsigned int* err = device_error_word(&e);
   if (!err) return cuda_fail(e, "device error word");
-  e = launch_umma_selftest(ta, tb, C, N, b_mn_major != 0, err, static_cast<cudaStream_t>(stream));
+  e = launch_umma_selftest(ta, tb, C, N, b_mn_major != 0, a_tmem, err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 self-test launch");
   return SKV_OK;
 }

@@ -245,28 +245,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       float s[kTN];
+      {
+        uint32_t r[4][16];
 #pragma unroll
-      for (int c = 0; c < kTN / 16; ++c) {
-        uint32_t r[16];
-        tc::tmem_ld16(t_lane + kColS + 64 * k + 16 * c, r);
-        tc::tmem_wait_ld();
+        for (int c = 0; c < kTN / 16; ++c) tc::tmem_ld16(t_lane + kColS + 64 * k + 16 * c, r[c]);
+        tc::tmem_wait_ld();  // one wait for the four loads
 #pragma unroll
-        for (int e = 0; e < 16; ++e) s[16 * c + e] = __uint_as_float(r[e]);
+        for (int c = 0; c < kTN / 16; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) s[16 * c + e] = __uint_as_float(r[c][e]) * p.scale_log2;
       }
       const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
       const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
-      float tmax = -INFINITY;
+      if (need_mask) {
+        // visible columns of this row: [c_lo, c_hi)
+        const int c_lo = min(max(r_lo - t0, 0), kTN);
+        const int c_hi = static_cast<int>(min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0),
+                                              (int64_t)kTN));
+        const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
 #pragma unroll
-      for (int c = 0; c < kTN; ++c) {
-        float y = s[c] * p.scale_log2;
-        if (need_mask) {
-          const int tok = t0 + c;
-          const bool vis = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
-          y = vis ? y : -INFINITY;
-        }
-        s[c] = y;
-        tmax = fmaxf(tmax, y);
+        for (int c = 0; c < kTN; ++c) s[c] = (static_cast<unsigned>(c - c_lo) < span) ? s[c] : -INFINITY;
       }
+      float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int c = 4; c < kTN; c += 4) {
+        mx[0] = fmaxf(mx[0], s[c]);
+        mx[1] = fmaxf(mx[1], s[c + 1]);
+        mx[2] = fmaxf(mx[2], s[c + 2]);
+        mx[3] = fmaxf(mx[3], s[c + 3]);
+      }
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
       const float m_new = need ? fmaxf(m_used, tmax) : m_used;
       bool pv_waited = false;
@@ -276,13 +284,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
-          uint32_t r[16];
-          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
+        for (int c = 0; c < kD / 16; c += 2) {
+          uint32_t r[2][16];
+          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r[0]);
+          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * c, r);
+          for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[h2][e] = __float_as_uint(__uint_as_float(r[h2][e]) * alpha);
+          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * c, r[0]);
+          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
         }
         tc::tmem_wait_st();
         l_sum *= alpha;
@@ -295,18 +307,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->pv_done[k], (i - 1) & 1, p.err, kDevErrFullWait);
       }
       // p = 2^(s - m_used) -> bf16 into the swizzled K-major P tile (row = query row)
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t* p_row = p_tile + row * 128;
+      const uint32_t sw = static_cast<uint32_t>(row & 7);
 #pragma unroll
       for (int cc = 0; cc < kTN / 8; ++cc) {
         float pv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           pv[e] = fast_exp2(s[8 * cc + e] - base);
-          l_sum += pv[e];
+          ls[e & 3] += pv[e];
         }
         const uint4 v = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
                                    pack_bf16(pv[6], pv[7]));
-        *reinterpret_cast<uint4*>(p_tile + swz128(row, cc * 16)) = v;
+        *reinterpret_cast<uint4*>(p_row + ((static_cast<uint32_t>(cc) ^ sw) << 4)) = v;
       }
+      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (k == 0 && !in_range) {
         // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
         // zero their V rows so that p = 0 really contributes nothing
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (x.fused) {
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(x.out_bf16) +
                             ((static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h) * kD;
-#pragma unroll 1
+#pragma unroll 2
       for (int c = 0; c < kD / 16; ++c) {
         uint32_t r[16];
         if (n_tiles > 0) {

@@ -86,7 +86,7 @@ cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const C
 
 // tcgen05 self-test GEMM (see umma_selftest.cu).
 cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, float* C, int N, bool b_mn_major,
-                                 unsigned int* err, cudaStream_t stream);
+                                 bool a_tmem, unsigned int* err, cudaStream_t stream);
 
 // Merge n_in partials per output group: in_o [G_out][n_in][R][dv], in_lse [G_out][n_in][R]
 // -> out [G_out][R][dv] (fp32 or bf16) and out_lse [G_out][R].
