@@ -372,8 +372,8 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   x.out_lse = lse_final;
   CUtensorMap tmq, tmk, tmv;
   if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN)) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, tc_attn_kv_tile())) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, tc_attn_kv_tile())) != SKV_OK) return st;
   const int64_t n_items = static_cast<int64_t>(d->B) * d->Hkv * (fused ? 1 : n_split) * pl.m_tiles;
   cudaError_t e = launch_tc_attn(p, x, tmq, tmk, tmv, n_items, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core attention launch");

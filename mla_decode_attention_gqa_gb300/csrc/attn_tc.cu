@@ -14,14 +14,16 @@
 // GB300 design (one CTA per SM):
 //   * a CTA owns 256 rows = two 128-row query tiles of one KV head; rows are (query row,
 //     head) pairs, so a K/V tile read once serves the whole GQA group and both tiles;
-//   * warp 0: TMA producer (Q tiles once, 64-token K/V tiles into a 3-stage ring);
+//   * warp 0: TMA producer (Q tiles once, 128-token K/V tiles into a 2-stage ring);
 //     warp 1: allocates 512 TMEM columns and issues every tcgen05.mma from one thread;
 //     warps 2-5 and 6-9: softmax for query tile 0 and 1, one thread per row (the TMEM lane
 //     of its row), so row max / sum need no shuffles;
-//   * TMEM: S0 | S1 (128 x 64 fp32 each) | O0 | O1 (128 x 128 fp32 each);
-//     P (bf16) goes through 128-byte-swizzled shared memory as the A operand of P V;
+//   * TMEM: S0 | S1 (128 x 128 fp32 each) | O0 | O1 (128 x 128 fp32 each); P (bf16) is
+//     written over the first 64 columns of its S and read from TMEM as the A operand of
+//     P V, so P never touches shared memory;
 //   * MMA order per KV tile: PV0(i), S0(i+1), PV1(i), S1(i+1), so each softmax group works
-//     while the tensor core serves the other group;
+//     while the tensor core serves the other group.  MMAs from one thread run in order, so
+//     when S_k(i) has landed, PV_k(i-1) is complete: O_k may be rescaled and P_k rewritten;
 //   * O is rescaled (TMEM load / scale / store) only when a row's running max rises by
 //     more than 2^8; otherwise p = 2^(s - m_used) <= 256 stays exact enough in bf16.
 #include <cuda_runtime.h>
@@ -35,23 +37,21 @@ namespace skv {
 namespace {
 
 constexpr int kD = 128;         // dk = dv
-constexpr int kTN = 64;         // tokens per K/V tile
-constexpr int kNStage = 3;      // K/V ring depth
+constexpr int kTN = 128;        // tokens per K/V tile
+constexpr int kNStage = 2;      // K/V ring depth
 constexpr int kRowsTile = 128;  // rows per query tile (MMA M)
 constexpr int kThreads = 10 * 32;
 constexpr int kQTileBytes = kRowsTile * kD * 2;  // 32 KB (two 16 KB boxes)
-constexpr int kKVBoxBytes = kTN * 128;           // 8 KB
-constexpr int kKTileBytes = 2 * kKVBoxBytes;     // 16 KB
+constexpr int kKVBoxBytes = kTN * 128;           // 16 KB: 128 tokens x 64 dims
+constexpr int kKTileBytes = 2 * kKVBoxBytes;     // 32 KB
 constexpr int kStageBytes = 2 * kKTileBytes;     // K + V
-constexpr int kPTileBytes = kRowsTile * kTN * 2;  // 16 KB
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
-constexpr int kOffP = kOffRing + kNStage * kStageBytes;
-constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+constexpr int kOffBar = kOffRing + kNStage * kStageBytes;
 constexpr int kSmem = 1024 + kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S_k at kColS + 64 k
-constexpr uint32_t kColO = 128;  // O_k at kColO + 128 k
+constexpr uint32_t kColS = 0;    // S_k (and P_k over its first 64 columns) at kColS + 128 k
+constexpr uint32_t kColO = 256;  // O_k at kColO + 128 k
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = tc::idesc_f16(128, kD, true, false, true);
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
-      const uint32_t p_base = smem_u32(smem + kOffP);
       bool ok = mbar_wait(&bars->q_full, 0, p.err, kDevErrFullWait);
       auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 64, K 128)
         const uint32_t kt = ring + (i % kNStage) * kStageBytes;
@@ -179,15 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad =
               tc::smem_desc_sw128(q_base + k * kQTileBytes + (ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(kt + (ks >> 2) * kKVBoxBytes + (ks & 3) * 32, 16, 1024);
-          tc::mma_f16_ss(tmem + kColS + 64 * k, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          tc::mma_f16_ss(tmem + kColS + 128 * k, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int k, int i) {  // O_k += P_k V_i  (M 128, N 128, K 64)
+      auto issue_pv = [&](int k, int i) {  // O_k += P_k V_i  (M 128, N 128, K 128; P_k from TMEM)
         const uint32_t vt = ring + (i % kNStage) * kStageBytes + kKTileBytes;
         for (int ks = 0; ks < kTN / 16; ++ks) {
-          const uint64_t ad = tc::smem_desc_sw128(p_base + k * kPTileBytes + ks * 32, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(vt + ks * 2048, kKVBoxBytes, 1024);
-          tc::mma_f16_ss(tmem + kColO + 128 * k, ad, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16_ts(tmem + kColO + 128 * k, tmem + kColS + 128 * k + ks * 8, bd, idesc_pv,
+                         (i > 0 || ks > 0) ? 1u : 0u);
         }
       };
       if (ok) ok = mbar_wait(&bars->kv_full[0], 0, p.err, kDevErrFullWait);
@@ -235,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t hz = p.causal_offset + t_q;
     const int64_t hz_min = p.causal_offset + (m0 + k * kRowsTile + lgrp * 32) / G;  // smallest in this warp
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
-    uint8_t* p_tile = smem + kOffP + k * kPTileBytes;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
 
@@ -244,84 +242,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(&bars->s_full[k], i & 1, p.err, kDevErrFullWait);
       if (!ok) break;
       tc::fence_after_sync();
-      float s[kTN];
-      {
-        uint32_t r[4][16];
-#pragma unroll
-        for (int c = 0; c < kTN / 16; ++c) tc::tmem_ld16(t_lane + kColS + 64 * k + 16 * c, r[c]);
-        tc::tmem_wait_ld();  // one wait for the four loads
-#pragma unroll
-        for (int c = 0; c < kTN / 16; ++c)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) s[16 * c + e] = __uint_as_float(r[c][e]) * p.scale_log2;
-      }
       const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
       const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
-      if (need_mask) {
-        // visible columns of this row: [c_lo, c_hi)
-        const int c_lo = min(max(r_lo - t0, 0), kTN);
-        const int c_hi = static_cast<int>(min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0),
-                                              (int64_t)kTN));
-        const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
-#pragma unroll
-        for (int c = 0; c < kTN; ++c) s[c] = (static_cast<unsigned>(c - c_lo) < span) ? s[c] : -INFINITY;
-      }
-      float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int c = 4; c < kTN; c += 4) {
-        mx[0] = fmaxf(mx[0], s[c]);
-        mx[1] = fmaxf(mx[1], s[c + 1]);
-        mx[2] = fmaxf(mx[2], s[c + 2]);
-        mx[3] = fmaxf(mx[3], s[c + 3]);
-      }
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
-      const float m_new = need ? fmaxf(m_used, tmax) : m_used;
-      bool pv_waited = false;
-      if (i > 0 && __any_sync(0xffffffffu, need)) {
-        ok = mbar_wait(&bars->pv_done[k], (i - 1) & 1, p.err, kDevErrFullWait);
-        pv_waited = true;
-        tc::fence_after_sync();
-        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < kD / 16; c += 2) {
-          uint32_t r[2][16];
-          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r[0]);
-          tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) r[h2][e] = __float_as_uint(__uint_as_float(r[h2][e]) * alpha);
-          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * c, r[0]);
-          tc::tmem_st16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
-        }
-        tc::tmem_wait_st();
-        l_sum *= alpha;
-      } else if (need) {
-        l_sum = 0.f;  // first visible tile of this row (nothing accumulated yet)
-      }
-      m_used = m_new;
-      const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      if (i > 0 && !pv_waited) {  // P buffer is free once PV of the previous tile is done
-        ok = mbar_wait(&bars->pv_done[k], (i - 1) & 1, p.err, kDevErrFullWait);
-      }
-      // p = 2^(s - m_used) -> bf16 into the swizzled K-major P tile (row = query row)
+      // visible columns of this row: [c_lo, c_lo + span)
+      const int c_lo = min(max(r_lo - t0, 0), kTN);
+      const int c_hi = static_cast<int>(
+          min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTN));
+      const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
+      const uint32_t s_col = t_lane + kColS + 128 * k;
+      const float sl = p.scale_log2;
+
+      // Optimistic pass: p = 2^(scale*s - m_used) with the running max, the tile max
+      // tracked alongside; P stays packed in registers until the max is known to be fine.
+      uint32_t pk[kTN / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint8_t* p_row = p_tile + row * 128;
-      const uint32_t sw = static_cast<uint32_t>(row & 7);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const float base0 = (m_used == -INFINITY) ? 0.f : m_used;
 #pragma unroll
-      for (int cc = 0; cc < kTN / 8; ++cc) {
-        float pv[8];
+      for (int cc = 0; cc < kTN / 32; ++cc) {
+        uint32_t r[2][16];
+        tc::tmem_ld16(s_col + 32 * cc, r[0]);
+        tc::tmem_ld16(s_col + 32 * cc + 16, r[1]);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv[e] = fast_exp2(s[8 * cc + e] - base);
-          ls[e & 3] += pv[e];
+        for (int e = 0; e < 16; ++e) {
+          const int col = 32 * cc + 2 * e;
+          float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
+          float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
+          if (need_mask) {
+            v0 = (static_cast<unsigned>(col - c_lo) < span) ? v0 : -INFINITY;
+            v1 = (static_cast<unsigned>(col + 1 - c_lo) < span) ? v1 : -INFINITY;
+          }
+          mx[(2 * e) & 3] = fmaxf(mx[(2 * e) & 3], v0);
+          mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], v1);
+          const float p0 = fast_exp2(fmaf(v0, sl, -base0));
+          const float p1 = fast_exp2(fmaf(v1, sl, -base0));
+          ls[(2 * e) & 3] += p0;
+          ls[(2 * e + 1) & 3] += p1;
+          pk[16 * cc + e] = pack_bf16(p0, p1);
         }
-        const uint4 v = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                                   pack_bf16(pv[6], pv[7]));
-        *reinterpret_cast<uint4*>(p_row + ((static_cast<uint32_t>(cc) ^ sw) << 4)) = v;
       }
+      // scores are scaled after the max (the scale is positive)
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
+      const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
+      if (__any_sync(0xffffffffu, need)) {
+        // rare: a row's max rose by more than 2^8 (always on a row's first visible tile):
+        // rescale O and l to the new max and redo this tile's P from S (still in TMEM)
+        const float m_new = need ? fmaxf(m_used, tmax) : m_used;
+        if (i > 0) {
+          // PV_k(i-1) ran before S_k(i) on the in-order tensor pipe, so O_k is final here
+          const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < kD / 16; c += 2) {
+            uint32_t r[2][16];
+            tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r[0]);
+            tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int e = 0; e < 16; ++e) r[h2][e] = __float_as_uint(__uint_as_float(r[h2][e]) * alpha);
+            tc::tmem_st16(t_lane + kColO + 128 * k + 16 * c, r[0]);
+            tc::tmem_st16(t_lane + kColO + 128 * k + 16 * (c + 1), r[1]);
+          }
+          tc::tmem_wait_st();
+          l_sum *= alpha;
+        } else {
+          l_sum = 0.f;
+        }
+        m_used = m_new;
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kTN / 32; ++cc) {
+          uint32_t r[2][16];
+          tc::tmem_ld16(s_col + 32 * cc, r[0]);
+          tc::tmem_ld16(s_col + 32 * cc + 16, r[1]);
+          tc::tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = 32 * cc + 2 * e;
+            float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
+            float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
+            if (need_mask) {
+              v0 = (static_cast<unsigned>(col - c_lo) < span) ? v0 : -INFINITY;
+              v1 = (static_cast<unsigned>(col + 1 - c_lo) < span) ? v1 : -INFINITY;
+            }
+            const float p0 = fast_exp2(fmaf(v0, sl, -base));
+            const float p1 = fast_exp2(fmaf(v1, sl, -base));
+            ls[(2 * e) & 3] += p0;
+            ls[(2 * e + 1) & 3] += p1;
+            w[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(s_col + 16 * cc, w);  // S columns 32cc.. were read before P 16cc.. is written
+        }
+      } else {
+        // common case: the optimistic P is exact; S is fully read, so P may overwrite it
+#pragma unroll
+        for (int cc = 0; cc < kTN / 32; ++cc) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pk[16 * cc + e];
+          tc::tmem_st16(s_col + 16 * cc, w);
+        }
+      }
+      tc::tmem_wait_st();
       l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (k == 0 && !in_range) {
         // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
@@ -338,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(vt + bx * kKVBoxBytes + tid * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc::fence_before_sync();
       mbar_arrive(&bars->p_full[k]);
     }
@@ -414,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int tc_attn_rows_per_cta() { return 2 * kRowsTile; }
+int tc_attn_kv_tile() { return kTN; }
 
 cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream) {

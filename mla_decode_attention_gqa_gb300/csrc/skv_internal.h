@@ -81,6 +81,7 @@ struct TcAttnExtra {
   float* out_lse;
 };
 int tc_attn_rows_per_cta();
+int tc_attn_kv_tile();  // tokens per K/V tile = rows of the K/V tensor-map box
 cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream);
 
