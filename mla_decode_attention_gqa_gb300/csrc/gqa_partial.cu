@@ -37,8 +37,9 @@ namespace skv {
 
 namespace {
 
-template <bool FP8_, int D_, int WM_, int WN_, int NSTAGE_, int MINB_>
+template <bool FP8_, int D_, int WM_, int WN_, int NSTAGE_, int MINB_, int SUB_ = kTileN>
 struct GqaCfg {
+  static constexpr int SUB = SUB_;  // tokens per online-softmax step (a tile is TN / SUB steps)
   static constexpr bool FP8 = FP8_;
   static constexpr int D = D_;  // dk = dv
   static constexpr int WM = WM_;
@@ -69,6 +70,7 @@ struct GqaCfg {
   // phase ahead of the last completed one, or the parity wait would alias an older
   // phase.  With NSTAGE >= WN the tile NSTAGE before its next one has always landed.
   static_assert(NSTAGE >= WN, "need at least one ring stage per consumer warp column");
+  static_assert(kTileN % SUB_ == 0 && SUB_ % 16 == 0, "softmax step must divide the tile");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -241,18 +243,23 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     if (!mbar_wait(&full[s], (i / NSTAGE) & 1, p.err, kDevErrFullWait)) break;
     const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
     const uint32_t vbase = kbase + C::TILE_BYTES;
-
-    // ---- S = Q K^T  (16 x 64)
-    float sc[TN / 8][4];
-#pragma unroll
-    for (int i2 = 0; i2 < TN / 8; ++i2) sc[i2][0] = sc[i2][1] = sc[i2][2] = sc[i2][3] = 0.f;
     const int mi = lane >> 3;
+    constexpr int NS = C::SUB;
+#pragma unroll 1
+    for (int sub = 0; sub < TN / NS; ++sub) {
+    const int t0s = t0 + sub * NS;
+    const int tb = sub * NS;  // first token of this step inside the tile
+
+    // ---- S = Q K^T  (16 x NS)
+    float sc[NS / 8][4];
+#pragma unroll
+    for (int i2 = 0; i2 < NS / 8; ++i2) sc[i2][0] = sc[i2][1] = sc[i2][2] = sc[i2][3] = 0.f;
     if constexpr (!C::FP8) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-        for (int np = 0; np < TN / 16; ++np) {
-          const uint32_t tok = 16 * np + (mi >> 1) * 8 + (lane & 7);
+        for (int np = 0; np < NS / 16; ++np) {
+          const uint32_t tok = tb + 16 * np + (mi >> 1) * 8 + (lane & 7);
           const uint32_t byte = (2 * ks + (mi & 1)) * 16;
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
@@ -268,31 +275,36 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         const uint32_t qa0[4] = {qv0.x, qv0.y, qv0.z, qv0.w};
         const uint32_t qa1[4] = {qv1.x, qv1.y, qv1.z, qv1.w};
 #pragma unroll
-        for (int np = 0; np < TN / 16; ++np) {
-          const uint32_t tok = 16 * np + (mi >> 1) * 8 + (lane & 7);
+        for (int np = 0; np < NS / 16; ++np) {
+          const uint32_t tok = tb + 16 * np + (mi >> 1) * 8 + (lane & 7);
           const uint32_t byte = (ks + (mi & 1)) * 16;
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
-          mma_f16(sc[2 * np], qa0, e4m3x2_to_f16x2(r0 & 0xFFFF), e4m3x2_to_f16x2(r0 >> 16));
-          mma_f16(sc[2 * np], qa1, e4m3x2_to_f16x2(r1 & 0xFFFF), e4m3x2_to_f16x2(r1 >> 16));
-          mma_f16(sc[2 * np + 1], qa0, e4m3x2_to_f16x2(r2 & 0xFFFF), e4m3x2_to_f16x2(r2 >> 16));
-          mma_f16(sc[2 * np + 1], qa1, e4m3x2_to_f16x2(r3 & 0xFFFF), e4m3x2_to_f16x2(r3 >> 16));
+          uint32_t k0l, k0h, k1l, k1h, k2l, k2h, k3l, k3h;
+          e4m3x4_to_f16x2x2(r0, k0l, k0h);
+          e4m3x4_to_f16x2x2(r1, k1l, k1h);
+          e4m3x4_to_f16x2x2(r2, k2l, k2h);
+          e4m3x4_to_f16x2x2(r3, k3l, k3h);
+          mma_f16(sc[2 * np], qa0, k0l, k0h);
+          mma_f16(sc[2 * np], qa1, k1l, k1h);
+          mma_f16(sc[2 * np + 1], qa0, k2l, k2h);
+          mma_f16(sc[2 * np + 1], qa1, k3l, k3h);
         }
       }
     }
 
     // ---- scale, mask, online softmax
     const float sl = p.scale_log2 * ksc;
-    const bool in_range = (t0 >= r_lo) && (t0 + TN <= r_hi);
-    const bool need_mask = !in_range || (static_cast<int64_t>(t0) + TN - 1 > hz_min);
+    const bool in_range = (t0s >= r_lo) && (t0s + NS <= r_hi);
+    const bool need_mask = !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < TN / 8; ++nt) {
+    for (int nt = 0; nt < NS / 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float x = sc[nt][e] * sl;
         if (need_mask) {
-          const int tok = t0 + 8 * nt + 2 * tq + (e & 1);
+          const int tok = t0s + 8 * nt + 2 * tq + (e & 1);
           const int64_t hz = (e < 2) ? hz0 : hz1;
           const bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
           x = ok ? x : -INFINITY;
@@ -313,17 +325,34 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       lrun[r] *= alpha[r];
     }
     if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {  // a row max moved
+      if constexpr (!C::FP8) {
 #pragma unroll
-      for (int i2 = 0; i2 < D / 8; ++i2) {
-        o[i2][0] *= alpha[0];
-        o[i2][1] *= alpha[0];
-        o[i2][2] *= alpha[1];
-        o[i2][3] *= alpha[1];
+        for (int i2 = 0; i2 < D / 8; ++i2) {
+          o[i2][0] *= alpha[0];
+          o[i2][1] *= alpha[0];
+          o[i2][2] *= alpha[1];
+          o[i2][3] *= alpha[1];
+        }
+      } else {
+        // O^T: this thread's columns are rows 2tq, 2tq+1 (+8) of the row set
+        float ar[2][2];
+        ar[0][0] = __shfl_sync(0xffffffffu, alpha[0], 8 * tq);
+        ar[0][1] = __shfl_sync(0xffffffffu, alpha[0], 8 * tq + 4);
+        ar[1][0] = __shfl_sync(0xffffffffu, alpha[1], 8 * tq);
+        ar[1][1] = __shfl_sync(0xffffffffu, alpha[1], 8 * tq + 4);
+#pragma unroll
+        for (int i2 = 0; i2 < D / 8; ++i2) {
+          const int n = i2 & 1;
+          o[i2][0] *= ar[n][0];
+          o[i2][1] *= ar[n][1];
+          o[i2][2] *= ar[n][0];
+          o[i2][3] *= ar[n][1];
+        }
       }
     }
-    uint32_t pa[TN / 16][4];
+    uint32_t pa[NS / 16][4];
 #pragma unroll
-    for (int nt = 0; nt < TN / 8; ++nt) {
+    for (int nt = 0; nt < NS / 8; ++nt) {
       const float p0 = fast_exp2(sc[nt][0] - base[0]);
       const float p1 = fast_exp2(sc[nt][1] - base[0]);
       const float p2 = fast_exp2(sc[nt][2] - base[1]);
@@ -343,17 +372,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     // ---- O += P V
     const bool vmask = !in_range;
 #pragma unroll
-    for (int kk = 0; kk < TN / 16; ++kk) {
+    for (int kk = 0; kk < NS / 16; ++kk) {
       if constexpr (!C::FP8) {
         uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
         if (vmask) {
-          const int ta = t0 + 16 * kk + 2 * tq, tb = ta + 8;
+          const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
           mlo = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
-          mhi = half_mask(tb >= r_lo && tb < r_hi, tb + 1 >= r_lo && tb + 1 < r_hi);
+          mhi = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
         }
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
-          const uint32_t tok = 16 * kk + (mi & 1) * 8 + (lane & 7);
+          const uint32_t tok = tb + 16 * kk + (mi & 1) * 8 + (lane & 7);
           const uint32_t byte = (2 * dp + (mi >> 1)) * 16;
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
@@ -361,26 +390,32 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
           mma_bf16(o[2 * dp + 1], pa[kk], r2 & mlo, r3 & mhi);
         }
       } else {
-        bool ok0 = true, ok1 = true;
+        // O^T[dv x rows] += V^T[dv x tok] P^T[tok x rows]: ldmatrix.trans of the e4m3 tile
+        // (16-bit view) gives each lane bytes V[2tq][2gq], V[2tq][2gq+1], V[2tq+1][2gq],
+        // V[2tq+1][2gq+1]; one byte permute pairs them by dv, so the A rows gq / gq+8 of a
+        // 16-dv chunk c are dv 16c+2gq / 16c+2gq+1, and P's fragments are already the B
+        // operand (columns = the 16 rows).
+        uint32_t m0 = 0xFFFFFFFFu, m1 = 0xFFFFFFFFu;
         if (vmask) {
-          const int ta = t0 + 16 * kk + gq, tb = ta + 8;
-          ok0 = ta >= r_lo && ta < r_hi;
-          ok1 = tb >= r_lo && tb < r_hi;
+          const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
+          m0 = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
+          m1 = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
         }
+        const uint32_t b00 = pa[kk][0], b01 = pa[kk][2], b10 = pa[kk][1], b11 = pa[kk][3];
 #pragma unroll
         for (int cc = 0; cc < D / 16; ++cc) {
-          const uint32_t tok = 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const uint32_t tok = tb + 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
           uint32_t r0, r1;
-          ldsm_x2(vbase + tile_off<C>(tok, cc * 16), r0, r1);
-          r0 = ok0 ? r0 : 0u;
-          r1 = ok1 ? r1 : 0u;
-          const uint32_t h0v = e4m3x2_to_f16x2(r0 & 0xFFFF), h1v = e4m3x2_to_f16x2(r0 >> 16);
-          const uint32_t h2v = e4m3x2_to_f16x2(r1 & 0xFFFF), h3v = e4m3x2_to_f16x2(r1 >> 16);
-          mma_f16(o[2 * cc], pa[kk], movmatrix_t(h0v), movmatrix_t(h2v));
-          mma_f16(o[2 * cc + 1], pa[kk], movmatrix_t(h1v), movmatrix_t(h3v));
+          ldsm_x2_t(vbase + tile_off<C>(tok, cc * 16), r0, r1);
+          uint32_t a[4];
+          e4m3x4_to_f16x2x2(prmt(r0 & m0, 0u, 0x3120u), a[0], a[1]);
+          e4m3x4_to_f16x2x2(prmt(r1 & m1, 0u, 0x3120u), a[2], a[3]);
+          mma_f16(o[2 * cc], a, b00, b01);
+          mma_f16(o[2 * cc + 1], a, b10, b11);
         }
       }
     }
+    }  // sub-steps
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -402,18 +437,34 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const float inv1 = lrun[1] > 0.f ? 1.f / lrun[1] : 0.f;
     const bool w0 = v0 && (lrun[0] > 0.f || p.zero_empty);
     const bool w1 = v1 && (lrun[1] > 0.f || p.zero_empty);
-    float* o0 = p.out_o + row_out(tq0, h0) * D;
-    float* o1 = p.out_o + row_out(tq1, h1) * D;
+    if constexpr (!C::FP8) {
+      float* o0 = p.out_o + row_out(tq0, h0) * D;
+      float* o1 = p.out_o + row_out(tq1, h1) * D;
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      int d;
-      if constexpr (!C::FP8) {
-        d = 8 * nt + 2 * tq;
-      } else {
-        d = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1);
+      for (int nt = 0; nt < D / 8; ++nt) {
+        const int d = 8 * nt + 2 * tq;
+        if (w0) *reinterpret_cast<float2*>(o0 + d) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
+        if (w1) *reinterpret_cast<float2*>(o1 + d) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
       }
-      if (w0) *reinterpret_cast<float2*>(o0 + d) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-      if (w1) *reinterpret_cast<float2*>(o1 + d) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+    } else {
+      // O^T: this thread holds rows (8n + 2tq + {0,1}) at dv 16c + 2gq + {0,1}
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int src = 4 * (2 * tq + e);
+          const float inv = __shfl_sync(0xffffffffu, n ? inv1 : inv0, src);
+          const bool wr = __shfl_sync(0xffffffffu, (n ? w1 : w0) ? 1 : 0, src) != 0;
+          const int tq_r = __shfl_sync(0xffffffffu, n ? tq1 : tq0, src);
+          const int h_r = __shfl_sync(0xffffffffu, n ? h1 : h0, src);
+          float* orow = p.out_o + row_out(tq_r, h_r) * D;
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            const float* ov = o[2 * c + n];
+            if (wr) *reinterpret_cast<float2*>(orow + 16 * c + 2 * gq) = make_float2(ov[e] * inv, ov[2 + e] * inv);
+          }
+        }
+      }
     }
     if (tq == 0) {
       if (v0) p.out_lse[row_out(tq0, h0)] = lrun[0] > 0.f ? (mrun[0] + __log2f(lrun[0])) * kLn2 : -INFINITY;
@@ -445,16 +496,30 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       f[r] = (L > 0.f) ? fast_exp2(mrun[r] - M) / L : 0.f;
     }
     float* obuf = reinterpret_cast<float*>(smem);  // [WN][ROWS][D]
+    if constexpr (!C::FP8) {
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      int d;
-      if constexpr (!C::FP8) {
-        d = 8 * nt + 2 * tq;
-      } else {
-        d = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1);
+      for (int nt = 0; nt < D / 8; ++nt) {
+        const int d = 8 * nt + 2 * tq;
+        *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr0) * D + d) =
+            make_float2(o[nt][0] * f[0], o[nt][1] * f[0]);
+        *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr1) * D + d) =
+            make_float2(o[nt][2] * f[1], o[nt][3] * f[1]);
       }
-      *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr0) * D + d) = make_float2(o[nt][0] * f[0], o[nt][1] * f[0]);
-      *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr1) * D + d) = make_float2(o[nt][2] * f[1], o[nt][3] * f[1]);
+    } else {
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float fr = __shfl_sync(0xffffffffu, n ? f[1] : f[0], 4 * (2 * tq + e));
+          const int lr = wm * 16 + 8 * n + 2 * tq + e;
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            const float* ov = o[2 * c + n];
+            *reinterpret_cast<float2*>(obuf + (wn * C::ROWS + lr) * D + 16 * c + 2 * gq) =
+                make_float2(ov[e] * fr, ov[2 + e] * fr);
+          }
+        }
+      }
     }
     named_bar_sync(1, NCT);
     const int tid = threadIdx.x;  // < NCT

@@ -50,15 +50,26 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ in
   for (int d = lane * 4; d < dv; d += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (m != -INFINITY) {
-      for (int s = 0; s < n_in; ++s) {
-        const float ls = lse_base[static_cast<int64_t>(s) * R];
-        if (ls == -INFINITY) continue;
-        const float w = __expf(ls - m);
-        const float4 x = *reinterpret_cast<const float4*>(o_base + static_cast<int64_t>(s) * R * dv + d);
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
+      // partials in batches of 8: all loads of a batch are in flight together
+      constexpr int kBatch = 8;
+      for (int s0 = 0; s0 < n_in; s0 += kBatch) {
+        float w[kBatch];
+        float4 x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int s = s0 + u;
+          const float ls = (s < n_in) ? lse_base[static_cast<int64_t>(s) * R] : -INFINITY;
+          w[u] = (ls == -INFINITY) ? 0.f : __expf(ls - m);
+          x[u] = (w[u] != 0.f) ? *reinterpret_cast<const float4*>(o_base + static_cast<int64_t>(s) * R * dv + d)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          acc.x += w[u] * x[u].x;
+          acc.y += w[u] * x[u].y;
+          acc.z += w[u] * x[u].z;
+          acc.w += w[u] * x[u].w;
+        }
       }
     }
     acc.x *= inv;
