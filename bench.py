@@ -53,6 +53,20 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def config_of(w, ws=1):
+    """The `config` object both arms print: the workload by name and sizes."""
+    esz = 1 if w.kv_dtype == "fp8_e4m3" else 2
+    alloc = w.B * w.Hkv * w.S * (w.dk if w.mla else w.dk + w.dv) * esz
+    return {"workload": w.name, "B": w.B, "Tq": w.Tq, "Hq": w.Hq, "Hkv": w.Hkv, "dk": w.dk, "dv": w.dv, "S": w.S,
+            "kv_dtype": w.kv_dtype, "n_split": w.n_split, "ragged": w.ragged,
+            "l2": ("no flush: a tensor-bound prefill chunk (%.2f GB of KV, re-read from L2 per query tile by "
+                   "design)" % (alloc / 1e9)) if w.Tq > 1 else
+                  ("no flush: each step streams the resident KV cache (%.2f GB allocated), far above the 129 MB L2"
+                   % (alloc / 1e9)) if alloc > 4 * 129e6 else
+                  ("KV (%.4f GB) fits in L2: a parity-size workload, not a bench line" % (alloc / 1e9)),
+            "parallelism": f"replicas x{ws}"}
+
+
 def workload_by_name(name):
     for w in W.WORKLOADS:
         if w.name == name:
@@ -257,7 +271,7 @@ def reference_arm(args, w, ws, rank):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs_total / len(steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "config": config_of(w, ws),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -279,9 +293,6 @@ def ours_arm(args, w, ws, rank, local):
     kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, inp["seq_lens_host"], bounds, mla=w.mla,
                            scale_block=w.scale_block)
     flops = RL.attn_flops(w.Tq, w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, w.causal_offset)
-    src = [inp["q"], inp["k"]] if w.mla else [inp["q"], inp["k"], inp["v"], inp["k_scale"], inp["v_scale"]]
-    in_bytes = sum(t.numel() * t.element_size() for t in src if t is not None)  # MLA: V is a view
-    del src
     out = torch.empty((w.B, w.Tq, w.Hq, w.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Tq, w.Hq), dtype=torch.float32, device=dev)
 
@@ -367,8 +378,6 @@ def ours_arm(args, w, ws, rank, local):
 
     if rank != 0:
         return
-    l2_note = ("no flush: every step reads %.2f GB of inputs (KV %.2f GB) and writes the partials, "
-               "above the 129 MB L2" % (in_bytes / 1e9, kv_bytes / 1e9))
     # dominant kernel: the split-KV partial kernel (the merge kernel is ~2% of the step);
     # its per-launch time is taken as the measured step time, which also holds the merge
     step_s = statistics.mean(step_ms) * 1e-3
@@ -405,10 +414,7 @@ def ours_arm(args, w, ws, rank, local):
         "vs_baseline": None,
         "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 KV, bf16 q",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V)",
-        "config": {"workload": w.name, "B": w.B, "Tq": w.Tq, "Hq": w.Hq, "Hkv": w.Hkv, "dk": w.dk, "dv": w.dv,
-                   "S": w.S, "kv_dtype": w.kv_dtype, "n_split": w.n_split,
-                   "l2": l2_note,
-                   "parallelism": f"replicas x{ws}"},
+        "config": config_of(w, ws),
         "roofline": roof,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
