@@ -23,9 +23,9 @@
 //   * QK^T and PV run on mma.sync m16n8k16 tensor-core tiles with fp32 accumulation;
 //     the online softmax (running max / sum, rescale) is kept in registers with
 //     quad shuffles; exponentials are base-2 with log2(e) folded into the scale;
-//   * decode variants spread the item's tiles over 4 consumer warps and combine
-//     their (m, l, O) in shared memory at the end; prefill variants give each of
-//     4 warps its own 16 rows and share every tile.
+//   * decode variants spread the item's tiles over 4 (bf16 d=128: 3) consumer warps
+//     and combine their (m, l, O) in shared memory at the end; prefill variants give
+//     each of 4 warps its own 16 rows and share every tile.
 //   * fp8: K/V codes are widened to fp16 in registers (exact), q is used in fp16,
 //     the K block scale multiplies the score and the V block scale multiplies p.
 #include <cuda_runtime.h>
@@ -58,7 +58,10 @@ struct GqaCfg {
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int ROWS = 16 * WM;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
-  static constexpr int BAR_BYTES = 2 * NSTAGE * 8;
+  // Full barriers are per consumer warp column, DW of them each (see full_slot).
+  static constexpr int DW = (NSTAGE + WN - 1) / WN;
+  static constexpr int NFULL = WN * DW;
+  static constexpr int BAR_BYTES = ((NFULL + NSTAGE) * 8 + 15) / 16 * 16;
   static constexpr int ML_BYTES = WN * ROWS * 2 * 4;
   // fp8 variants keep their fp16 q fragments in shared memory ([WM][D/16][32 lanes] x 16 B)
   static constexpr int QF_BYTES = FP8 ? WM * (D / 16) * 32 * 16 : 0;
@@ -66,10 +69,7 @@ struct GqaCfg {
   static_assert(ROW_BYTES % 128 == 0, "token rows must be whole 128-byte boxes");
   static_assert(WN == 1 || WN * ROWS * D * 4 <= RING_BYTES, "combine buffer must fit in the ring");
   static_assert(D % 16 == 0, "head dim must be a multiple of 16");
-  // A consumer warp takes tiles WN apart; it must never wait on a stage more than one
-  // phase ahead of the last completed one, or the parity wait would alias an older
-  // phase.  With NSTAGE >= WN the tile NSTAGE before its next one has always landed.
-  static_assert(NSTAGE >= WN, "need at least one ring stage per consumer warp column");
+  static_assert(NFULL >= NSTAGE, "a full barrier is re-armed only after its previous tile was consumed");
   static_assert(kTileN % SUB_ == 0 && SUB_ % 16 == 0, "softmax step must divide the tile");
 };
 
@@ -83,6 +83,26 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t tok, uint32_t byte) {
   return (byte >> 7) * C::BOX_BYTES + swz128(tok, byte & 127u);
 }
 
+// Tile i lands in data stage i % NSTAGE but signals its own full barrier: consumer warp
+// column wn = i % WN owns barriers [wn*DW, wn*DW + DW) and uses them in turn.  A parity
+// wait is exact only when the barrier is at most one phase away from the awaited one.
+// With one barrier per stage that fails once WN does not divide NSTAGE: the stage's
+// previous tile belongs to another warp and its copy can land after this warp's own
+// previous tile, so the wait would match that older phase and return early.  With
+// per-column barriers the previous phase of tile i's barrier is tile i - WN*DW of the
+// same warp (already observed), and the next phase (tile i + WN*DW) cannot start
+// early: the producer issues tiles in order and waits, before issuing tile x, until
+// tile x - NSTAGE was consumed, so by the time it reaches tile i + WN*DW >= i + NSTAGE
+// tile i has been consumed.
+template <class C>
+__device__ __forceinline__ int full_slot(int i) {
+  return (i % C::WN) * C::DW + (i / C::WN) % C::DW;
+}
+template <class C>
+__device__ __forceinline__ uint32_t full_parity(int i) {
+  return static_cast<uint32_t>((i / C::WN) / C::DW) & 1u;
+}
+
 __device__ __forceinline__ uint32_t half_mask(bool lo, bool hi) {
   return (lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u);
 }
@@ -94,9 +114,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   constexpr int D = C::D, TN = C::TN, NSTAGE = C::NSTAGE, WN = C::WN, WM = C::WM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
-  uint64_t* empty = full + NSTAGE;
-  float* ml = reinterpret_cast<float*>(empty + NSTAGE);  // [WN][ROWS][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);  // [NFULL]
+  uint64_t* empty = full + C::NFULL;                                     // [NSTAGE]
+  float* ml = reinterpret_cast<float*>(smem + C::RING_BYTES + C::BAR_BYTES);  // [WN][ROWS][2]
   uint4* qfrag = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ml) + C::ML_BYTES);  // fp8 only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,10 +152,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int n_tiles = (r_hi > r_lo) ? ((r_hi + TN - 1) / TN - tile_begin) : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], WM);
-    }
+    for (int s = 0; s < C::NFULL; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&empty[s], WM);
     fence_mbar_init();
   }
   __syncthreads();
@@ -150,20 +168,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % NSTAGE;
         if (i >= NSTAGE && !mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1, p.err, kDevErrEmptyWait)) break;
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        uint64_t* fb = &full[full_slot<C>(i)];
+        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
         uint8_t* ks = smem + s * C::STAGE_BYTES;
         uint8_t* vs = ks + C::TILE_BYTES;
         const int tok = (tile_begin + i) * TN;
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
-          tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, &full[s], bx * C::BOX_ELEMS, tok, g, b, pol);
-          tma_load_4d(vs + bx * C::BOX_BYTES, &tmv, &full[s], bx * C::BOX_ELEMS, tok, g, b, pol);
+          tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, fb, bx * C::BOX_ELEMS, tok, g, b, pol);
+          tma_load_4d(vs + bx * C::BOX_BYTES, &tmv, fb, bx * C::BOX_ELEMS, tok, g, b, pol);
         }
         issued = i + 1;
       }
-      // drain: every issued copy must have landed before this CTA may exit
+      // drain: every issued copy must have landed before this CTA may exit (tiles before
+      // issued - NSTAGE were consumed before their stage was refilled)
       for (int i = max(0, issued - NSTAGE); i < issued; ++i) {
-        if (!mbar_wait(&full[i % NSTAGE], (i / NSTAGE) & 1, p.err, kDevErrDrainWait)) break;
+        if (!mbar_wait(&full[full_slot<C>(i)], full_parity<C>(i), p.err, kDevErrDrainWait)) break;
       }
     }
     return;
@@ -240,7 +260,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       ksc = __ldg(kscale_row + t0 / p.scale_block);
       vsc = __ldg(vscale_row + t0 / p.scale_block);
     }
-    if (!mbar_wait(&full[s], (i / NSTAGE) & 1, p.err, kDevErrFullWait)) break;
+    if (!mbar_wait(&full[full_slot<C>(i)], full_parity<C>(i), p.err, kDevErrFullWait)) break;
     const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
     const uint32_t vbase = kbase + C::TILE_BYTES;
     const int mi = lane >> 3;
@@ -559,7 +579,7 @@ using CfgBf16D128Dec = GqaCfg<false, 128, 1, 3, 3, 2>;
 using CfgFp8D128Dec = GqaCfg<true, 128, 1, 4, 6, 2>;
 using CfgBf16D64Pre = GqaCfg<false, 64, 4, 1, 6, 2>;
 using CfgBf16D128Pre = GqaCfg<false, 128, 4, 1, 3, 2>;
-using CfgFp8D128Pre = GqaCfg<true, 128, 4, 1, 6, 2>;
+using CfgFp8D128Pre = GqaCfg<true, 128, 4, 1, 5, 2>;
 
 template <class C>
 GqaLaunchInfo info_of() {
