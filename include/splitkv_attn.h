@@ -97,6 +97,14 @@ const char* splitkv_last_error(void);
 skv_status splitkv_device_error(uint32_t* code);
 
 /*
+ * Read and clear the whole device error record (8 words, blocking): [0] the code as above,
+ * [1] nonzero if the first failure was described, [2] its block index, [3] its thread
+ * index, [4] the shared-memory address of the barrier it waited on, [5] the phase parity it
+ * waited for | code << 8.  For diagnosing a wait that gave up.
+ */
+skv_status splitkv_device_error_detail(uint32_t* record);
+
+/*
  * attn_partial -- one partial attention output per split.
  *
  *   q            bf16, logical [B][Tq][Hq][dk] with desc->q_strides

@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "splitkv_version",
     "splitkv_last_error",
     "splitkv_device_error",
+    "splitkv_device_error_detail",
     "attn_partial_workspace_size",
     "attn_partial",
     "attn_merge_lse",
@@ -81,6 +82,8 @@ def _load():
     lib.splitkv_last_error.restype = ctypes.c_char_p
     lib.splitkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.splitkv_device_error.restype = I32
+    lib.splitkv_device_error_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.splitkv_device_error_detail.restype = I32
     for name in ("attn_partial_workspace_size", "gqa_decode_attn_workspace_size"):
         f = getattr(lib, name)
         f.argtypes = [D, I32P, I32, ctypes.POINTER(SZ)]
@@ -125,11 +128,25 @@ def last_error():
     return _lib.splitkv_last_error().decode()
 
 
+last_device_error_detail = None
+
+
 def device_error():
-    """Read and clear the device error word (blocking); 0 means no kernel gave up a wait."""
-    code = ctypes.c_uint32(0)
-    _check(_lib.splitkv_device_error(ctypes.byref(code)))
-    return int(code.value)
+    """Read and clear the device error record (blocking); 0 means no kernel gave up a wait.
+    A nonzero code also leaves the record (block, thread, barrier, parity) in
+    ``last_device_error_detail`` and prints it to stderr."""
+    global last_device_error_detail
+    rec = (ctypes.c_uint32 * 8)()
+    _check(_lib.splitkv_device_error_detail(rec))
+    code = int(rec[0])
+    if code:
+        last_device_error_detail = {"code": code, "block": int(rec[2]), "thread": int(rec[3]),
+                                    "barrier_smem_addr": int(rec[4]), "parity": int(rec[5]) & 0xFF,
+                                    "first_code": (int(rec[5]) >> 8) & 0xFF}
+        import sys as _sys
+
+        print(f"device error record: {last_device_error_detail}", file=_sys.stderr)
+    return code
 
 
 def _check(status):

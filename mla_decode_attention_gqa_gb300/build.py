@@ -18,7 +18,7 @@ LIB_NAME = "libsplitkv_attn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "gqa_partial.cu", "mla_partial.cu", "merge_lse.cu", "umma_selftest.cu", "attn_tc.cu"]
+SOURCES = ["api.cu", "gqa_partial.cu", "mla_partial.cu", "merge_lse.cu", "umma_selftest.cu", "attn_tc.cu", "mla_tc.cu"]
 
 
 def _nvcc():

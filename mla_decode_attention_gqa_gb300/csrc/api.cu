@@ -14,10 +14,12 @@
 
 #include "../../include/splitkv_attn.h"
 #include "../../include/splitkv_attn_selftest.h"
+#include "skv_common.cuh"
 #include "skv_internal.h"
 
-// Device error word written by kernels whose bounded waits gave up.
-__device__ unsigned int g_skv_device_error = 0;
+// Device error record written by kernels whose bounded waits gave up (layout: see
+// DevErrWord in skv_common.cuh).
+__device__ unsigned int g_skv_device_error[skv::kDevErrWords] = {0};
 
 namespace {
 
@@ -103,6 +105,12 @@ bool is_mla_shape(const skv_desc* d) {
   return d->dk == 576 && d->dv == 512 && d->Hkv == 1 && d->kv_dtype == SKV_KV_BF16;
 }
 
+// The MLA latent with a head count dividing 128 runs on the tensor-core cluster kernel.
+bool use_mla_tc(const skv_desc* d) {
+  const int G = d->Hq / d->Hkv;
+  return is_mla_shape(d) && G <= 128 && 128 % G == 0;
+}
+
 bool is_gqa_shape(const skv_desc* d) {
   if (d->dk != d->dv) return false;
   if (d->kv_dtype == SKV_KV_BF16) return d->dk == 64 || d->dk == 128;
@@ -180,7 +188,8 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
     pl.variant = decode ? GqaVariant::kBf16D64Decode : GqaVariant::kBf16D64Prefill;
   else
     pl.variant = decode ? GqaVariant::kBf16D128Decode : GqaVariant::kBf16D128Prefill;
-  const GqaLaunchInfo li = pl.mla ? mla_launch_info() : gqa_launch_info(pl.variant);
+  GqaLaunchInfo li = pl.mla ? mla_launch_info() : gqa_launch_info(pl.variant);
+  if (pl.mla && use_mla_tc(d)) li = GqaLaunchInfo{mla_tc_rows_per_item(), 192, 0, 1, 2};
   pl.rows_per_cta = li.rows_per_cta;
   const int64_t rows = static_cast<int64_t>(d->Tq) * G;
   pl.m_tiles = static_cast<int>((rows + li.rows_per_cta - 1) / li.rows_per_cta);
@@ -196,7 +205,8 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
     }
   }
   const int64_t base = static_cast<int64_t>(d->B) * d->Hkv * n_split * pl.m_tiles;
-  const int64_t slots = static_cast<int64_t>(device_sm_count()) * li.ctas_per_sm;  // resident CTAs
+  const int64_t slots =  // work items resident at once
+      std::max<int64_t>(1, static_cast<int64_t>(device_sm_count()) * li.ctas_per_sm / li.ctas_per_item);
   pl.n_chunk = 1;
   pl.chunk_tiles = static_cast<int>(std::max<int64_t>(max_tiles, 1));
   if (max_tiles > 1 && base < 4 * slots) {
@@ -391,6 +401,20 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
   CUtensorMap tmk, tmv;
   cudaError_t e;
   if (pl.mla) {
+    if (use_mla_tc(d)) {
+      // one latent map (64-dim x 64-token boxes) serves K and V; each CTA of the pair
+      // loads its own slice of dims
+      CUtensorMap tmq;
+      if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
+      if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, mla_tc_kv_tile())) != SKV_OK) return st;
+      TcAttnExtra x;
+      x.fused = 0;
+      x.out_bf16 = nullptr;
+      x.out_lse = nullptr;
+      e = launch_mla_tc(p, x, tmq, tmk, pl.n_items, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "MLA tensor-core attention launch");
+      return SKV_OK;
+    }
     // one latent map serves K (all 576 columns) and V (its first 512 columns)
     if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kMlaTileN)) != SKV_OK) return st;
     e = launch_mla_partial(p, tmk, pl.n_items, stream);
@@ -412,14 +436,23 @@ int32_t splitkv_version(void) { return (1 << 16) | 0; }
 
 const char* splitkv_last_error(void) { return t_last_error.c_str(); }
 
+skv_status splitkv_device_error_detail(uint32_t* record) {
+  if (!record) return fail(SKV_EINVAL, "record is NULL");
+  unsigned int v[kDevErrWords] = {0}, zero[kDevErrWords] = {0};
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_skv_device_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error record");
+  e = cudaMemcpyToSymbol(g_skv_device_error, zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error record");
+  for (int i = 0; i < kDevErrWords; ++i) record[i] = v[i];
+  return SKV_OK;
+}
+
 skv_status splitkv_device_error(uint32_t* code) {
   if (!code) return fail(SKV_EINVAL, "code is NULL");
-  unsigned int v = 0, zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_skv_device_error, sizeof(v));
-  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  e = cudaMemcpyToSymbol(g_skv_device_error, &zero, sizeof(zero));
-  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
-  *code = v;
+  uint32_t rec[kDevErrWords];
+  skv_status st = splitkv_device_error_detail(rec);
+  if (st != SKV_OK) return st;
+  *code = rec[0];
   return SKV_OK;
 }
 

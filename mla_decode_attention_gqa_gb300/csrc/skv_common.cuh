@@ -20,8 +20,15 @@ enum DevError : unsigned int {
   kDevErrDrainWait = 4u,  // the final drain of in-flight copies gave up
 };
 
-// Time limit of every spin-wait in the library's kernels (globaltimer ns).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Time limit of every spin-wait in the library's kernels, in SM clock cycles (the
+// per-SM cycle counter is monotonic; about 2 s at 2 GHz).
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
+// Layout of the device error record (unsigned int words): [0] OR of error codes,
+// [1] set once the first failure is described, [2] blockIdx.x, [3] threadIdx.x,
+// [4] shared-memory address of the barrier, [5] parity | code << 8 | kernel id << 16.
+enum DevErrWord : int { kErrCode = 0, kErrTaken = 1, kErrBlock = 2, kErrThread = 3, kErrBar = 4, kErrWhat = 5 };
+constexpr int kDevErrWords = 8;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -64,17 +71,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false (and sets
-// `code` in *err) if it has not completed within kWaitLimitNs.
+// Record a wait that gave up: OR the code into err[0]; the first failure also records
+// where it happened (block, thread, barrier address, parity / code).
+__device__ __forceinline__ void record_wait_failure(unsigned int* err, unsigned int code, uint32_t bar_addr,
+                                                    uint32_t parity) {
+  atomicOr(err + kErrCode, code);
+  if (atomicCAS(err + kErrTaken, 0u, 1u) == 0u) {
+    err[kErrBlock] = blockIdx.x;
+    err[kErrThread] = threadIdx.x;
+    err[kErrBar] = bar_addr;
+    err[kErrWhat] = parity | (code << 8);
+  }
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and records the
+// failure in err) if it has not completed within kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
                                           unsigned int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const long long c0 = clock64();
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, code);
+    if ((++spins & 255u) == 0u && clock64() - c0 > kWaitLimitCycles) {
+      record_wait_failure(err, code, smem_u32(bar), parity);
       return false;
     }
   }

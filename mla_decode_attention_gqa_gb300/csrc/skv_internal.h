@@ -54,10 +54,11 @@ enum class GqaVariant {
 };
 
 struct GqaLaunchInfo {
-  int rows_per_cta;  // M rows handled by one CTA
+  int rows_per_cta;  // M rows handled by one work item
   int threads;
   int smem_bytes;
-  int ctas_per_sm;  // resident CTAs per SM the variant is built for
+  int ctas_per_sm;    // resident CTAs per SM the variant is built for
+  int ctas_per_item = 1;  // CTAs that share one work item (2: a cluster pair)
 };
 
 GqaLaunchInfo gqa_launch_info(GqaVariant v);
@@ -84,6 +85,13 @@ int tc_attn_rows_per_cta();
 int tc_attn_kv_tile();  // tokens per K/V tile = rows of the K/V tensor-map box
 cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream);
+
+// Tensor-core MLA latent attention (see mla_tc.cu): a cluster pair per work item of the
+// partial decomposition (b, split j, chunk c, 128-row tile), writing fp32 partials.
+int mla_tc_rows_per_item();
+int mla_tc_kv_tile();
+cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
+                          const CUtensorMap& tml, int64_t n_items, cudaStream_t stream);
 
 // tcgen05 self-test GEMM (see umma_selftest.cu).
 cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, float* C, int N, bool b_mn_major,

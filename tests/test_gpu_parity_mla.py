@@ -66,3 +66,22 @@ def test_mla_absorbed_full_size_sampled():
         ro_p, rl_p = io.oracle_rows(inp, w, b, 0, [0])
         ro, rl = oracle.merge_lse(ro_p, rl_p)
         io.assert_close(out[b, [0]], lse[b, [0]], ro, rl, io.TOL_BF16, f"b={b}")
+
+
+def test_mla_64_heads_half_row_tile():
+    """64 heads: the 128-row tensor-core tile is half empty."""
+    w = W.scaled(W.MLA_ABSORBED, B=2, Hq=64, S=700, n_split=2)
+    _all_paths(w, W.make_inputs(w, DEV))
+
+
+def test_mla_two_query_rows_causal():
+    """Two query rows per sequence (two 128-row tiles), causal by position."""
+    w = W.Workload("mla_tq2", B=2, Tq=2, Hq=128, Hkv=1, dk=576, dv=512, S=500, n_split=3, mla=True,
+                   softmax_scale=W.MLA_ABSORBED.softmax_scale, causal_offset=300, seed=1013)
+    _all_paths(w, W.make_inputs(w, DEV))
+
+
+def test_mla_single_split_chunked_long():
+    """One long split that the planner cuts into chunks to fill the GPU."""
+    w = W.scaled(W.MLA_ABSORBED, B=1, S=9000, n_split=1)
+    _all_paths(w, W.make_inputs(w, DEV))
