@@ -172,21 +172,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
       bool ok = mbar_wait(&bars->q_full, 0, p.err, kDevErrFullWait);
-      auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 64, K 128)
-        const uint32_t kt = ring + (i % kNStage) * kStageBytes;
+      // Descriptors are built once per call and the k-steps add compile-time offsets: a
+      // single issuing thread that recomputes them per step cannot keep the tensor pipe fed.
+      auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 128 tokens, K 128)
+        const uint64_t ad0 = tc::smem_desc_sw128(q_base + k * kQTileBytes, 16, 1024);
+        const uint64_t bd0 = tc::smem_desc_sw128(ring + (i % kNStage) * kStageBytes, 16, 1024);
+        const uint32_t d = tmem + kColS + 128 * k;
+#pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint64_t ad =
-              tc::smem_desc_sw128(q_base + k * kQTileBytes + (ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(kt + (ks >> 2) * kKVBoxBytes + (ks & 3) * 32, 16, 1024);
-          tc::mma_f16_ss(tmem + kColS + 128 * k, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          const uint64_t ad = ad0 + static_cast<uint64_t>(((ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32) >> 4);
+          const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kKVBoxBytes + (ks & 3) * 32) >> 4);
+          tc::mma_f16_ss(d, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int k, int i) {  // O_k += P_k V_i  (M 128, N 128, K 128; P_k from TMEM)
-        const uint32_t vt = ring + (i % kNStage) * kStageBytes + kKTileBytes;
+        const uint64_t bd0 =
+            tc::smem_desc_sw128(ring + (i % kNStage) * kStageBytes + kKTileBytes, kKVBoxBytes, 1024);
+        const uint32_t d = tmem + kColO + 128 * k;
+        const uint32_t a = tmem + kColS + 128 * k;
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+#pragma unroll
         for (int ks = 0; ks < kTN / 16; ++ks) {
-          const uint64_t bd = tc::smem_desc_sw128(vt + ks * 2048, kKVBoxBytes, 1024);
-          tc::mma_f16_ts(tmem + kColO + 128 * k, tmem + kColS + 128 * k + ks * 8, bd, idesc_pv,
-                         (i > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16_ts(d, a + ks * 8, bd0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv,
+                         ks > 0 ? 1u : acc0);
         }
       };
       if (ok) ok = mbar_wait(&bars->kv_full[0], 0, p.err, kDevErrFullWait);

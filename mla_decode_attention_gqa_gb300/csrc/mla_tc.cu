@@ -9,20 +9,22 @@
 // (the online softmax over their union), written as the final bf16 output.
 //
 // GB300 design: a cluster of two CTAs on two SMs serves one (sequence, split, chunk)
-// item.  The output O = P V of 128 heads x 512 dims in fp32 would fill all 512 TMEM
-// columns of one SM, so the pair splits the latent's dims:
-//   CTA 0 holds dims [0, 256): its slice of Q, its slice of every latent tile, and
-//          accumulates O[:, 0:256);
-//   CTA 1 holds dims [256, 576): its slice of Q and of every latent tile, and
-//          accumulates O[:, 256:512) (V dims 256..511 lie inside its slice).
-// Every latent byte is therefore loaded exactly once.  Each CTA computes a partial score
-// S_r = Q_r K_r^T (M 128, N 64 tokens, K 256 / 320) into TMEM; the partials are swapped
-// through distributed shared memory (DSMEM) and both CTAs run the same online softmax on
-// S = S_0 + S_1 (identical in both: fp32 addition commutes), write P (bf16) into TMEM
-// and accumulate their half of O with tcgen05.mma (A = P from TMEM, B = the MN-major V
-// slice, N = 256).  Warp roles per CTA: TMA producer, one MMA-issuing thread, four
-// softmax warps (one thread per head = TMEM lane).  S is double-buffered so S(i+1)
-// overlaps the softmax of tile i.  Every wait is bounded.
+// item.  The output O = P V of 128 heads x 512 dims in fp32 fills all 512 TMEM columns
+// of one SM, and the scores need the whole 576-dim contraction, so the pair splits the
+// two products instead of the dims:
+//   CTA 0 (scores) keeps Q (128 x 576) in tensor memory, streams the 576-dim latent
+//          tiles, computes S = Q K^T (M 128, N 64 tokens, A from TMEM), runs the online
+//          softmax (one thread per head = TMEM lane) and pushes P (bf16, already the
+//          MMA operand) plus one rescale factor per head into CTA 1's shared memory
+//          with bulk DSMEM copies;
+//   CTA 1 (values) streams the same tiles' first 512 dims (the second read of each
+//          tile hits L2), applies the rescale factors to O in tensor memory when a
+//          row maximum moved, and accumulates O += P V (A = P from shared memory,
+//          B = the MN-major V tile, two N = 256 halves).
+// Tensor work per 64-token tile: 36 k-steps of N = 64 on CTA 0, 8 of N = 256 on CTA 1.
+// Only bf16 P (16 KB per tile) crosses between the SMs, one way.  Warp roles per CTA:
+// TMA producer, one MMA-issuing thread, four row warps (softmax on CTA 0; rescale,
+// boundary-row zeroing and the epilogue on CTA 1).  Every wait is bounded.
 #include <cuda_runtime.h>
 
 #include "skv_common.cuh"
@@ -33,40 +35,61 @@ namespace skv {
 
 namespace {
 
-constexpr int kDk = 576;
-constexpr int kHalfDv = 256;   // value dims per CTA
-constexpr int kTN = 64;        // tokens per latent tile
-constexpr int kNStage = 2;
-constexpr int kRows = 128;     // heads per item (MMA M)
+constexpr int kTN = 64;          // tokens per latent tile
+constexpr int kRows = 128;       // heads per item (MMA M)
 constexpr int kThreads = 6 * 32;
-constexpr int kBoxBytes = kTN * 128;       // 64 tokens x 64 dims
-constexpr int kQBoxBytes = kRows * 128;    // 128 heads x 64 dims
-constexpr int kMaxBoxes = 5;               // CTA 1 holds 320 dims
-constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
-constexpr int kXBytes = kRows * kTN * 4;            // one S partial, 32 KB
-constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kMaxBoxes * kQBoxBytes;  // 80 KB
-constexpr int kOffX = kOffRing + kNStage * kStageBytes;   // +80 KB
-constexpr int kOffBar = kOffX + kXBytes;                  // +32 KB
+constexpr int kKBoxes = 9;       // 64-dim boxes of the 576-dim key
+constexpr int kVBoxes = 8;       // 64-dim boxes of the 512-dim value
+constexpr int kBoxBytes = kTN * 128;     // 64 tokens x 64 dims
+constexpr int kQBoxBytes = kRows * 128;  // 128 heads x 64 dims
+// CTA 0 (scores): Q staging, then a 2-stage ring of whole 576-dim tiles in the same bytes
+constexpr int kNStage0 = 2;
+constexpr int kStage0Bytes = kKBoxes * kBoxBytes;  // 72 KB
+constexpr int kOffPStage = kNStage0 * kStage0Bytes;  // 144 KB: P staging, 2 slots x 16 KB
+constexpr int kPBytes = kRows * 128;                 // 128 heads x 64 tokens bf16
+constexpr int kOffAStage = kOffPStage + 2 * kPBytes;  // rescale factors, 2 slots x 512 B
+constexpr int kOffLStage = kOffAStage + 2 * kRows * 4;  // final row sums, 512 B
+// CTA 1 (values): a 3-stage ring of 512-dim tiles, P / factor / row-sum receive buffers
+constexpr int kNStage1 = 3;
+constexpr int kStage1Bytes = kVBoxes * kBoxBytes;  // 64 KB
+constexpr int kOffPRecv = kNStage1 * kStage1Bytes;  // 192 KB
+constexpr int kOffARecv = kOffPRecv + 2 * kPBytes;
+constexpr int kOffLRecv = kOffARecv + 2 * kRows * 4;
+constexpr int kOffBar = kOffLRecv + kRows * 4;
 constexpr int kSmem = 1024 + kOffBar + 256;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S buffer b at kColS + 64 b (b = 0, 1)
-constexpr uint32_t kColP = 128;  // P buffer b at kColP + 32 b (bf16 pairs)
-constexpr uint32_t kColO = 256;  // O half: 256 columns
-constexpr float kRescaleThreshold = 8.0f;
+static_assert(kKBoxes * kQBoxBytes == kNStage0 * kStage0Bytes, "Q staging reuses the ring bytes");
+static_assert(kOffLStage + kRows * 4 <= kOffBar, "CTA 0 layout fits below the barriers");
+static_assert(kOffPStage % 1024 == 0 && kOffPRecv % 1024 == 0, "P tiles need 1024-byte swizzle atoms");
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // CTA 0: S buffer b at kColS + 64 b (b = 0, 1)
+constexpr uint32_t kColQ = 128;  // CTA 0: Q, 288 columns (two bf16 per column)
+constexpr uint32_t kColO = 0;    // CTA 1: O, 512 columns
+constexpr uint32_t kPMsgBytes = 4 * (32 * 128 + 32 * 4);  // P rows + factors, four warps
+constexpr float kRescaleThreshold = 8.0f;
 
+// One barrier block at the same offset in both CTAs (remote arrivals address a peer's
+// barrier by this CTA's own offset).
 struct MlaBars {
-  uint64_t q_full;
-  uint64_t kv_full[kNStage];
-  uint64_t kv_empty[kNStage];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done;
-  uint64_t x_full;   // the peer's S partial has landed in this CTA's exchange buffer
-  uint64_t x_empty;  // the peer has read its exchange buffer: this CTA may write it again
+  // CTA 0
+  uint64_t q_full;        // Q staged in shared memory
+  uint64_t q_moved;       // Q copied into TMEM by the four row warps; staging bytes free
+  uint64_t kv_full0[kNStage0];
+  uint64_t kv_empty0[kNStage0];
+  uint64_t s_full[2];     // S(i) in TMEM buffer i & 1
+  uint64_t s_free[2];     // the row warps have read S buffer b
+  uint64_t p_empty[2];    // CTA 1 finished PV with P slot b (arrived by CTA 1's MMA commit)
+  // CTA 1
+  uint64_t kv_full1[kNStage1];
+  uint64_t kv_empty1[kNStage1];
+  uint64_t p_full[2];     // P slot b and its factors landed (bulk copies from CTA 0)
+  uint64_t o_ready[2];    // rescale / boundary zeroing for tile i done (slot i & 1)
+  uint64_t pv_done;       // every PV issued so far completed
+  uint64_t o_final;       // the last PV completed
+  uint64_t l_full;        // the final row sums landed
   uint32_t tmem_base;
 };
+static_assert(sizeof(MlaBars) <= 256, "barrier block");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -81,45 +104,28 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
   return d;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
-}
-
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
+// Bulk copy from this CTA's shared memory into a peer's, completing on the peer's barrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
-  return ok != 0;
 }
 
-// Bounded wait on a barrier that the peer CTA arrives on (cluster-scope acquire).
-__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, unsigned int* err) {
-  if (try_wait_cluster(bar, parity)) return true;
-  const long long c0 = clock64();
-  uint32_t spins = 0;
-  while (true) {
-    if (try_wait_cluster(bar, parity)) return true;
-    if ((++spins & 255u) == 0u && clock64() - c0 > kWaitLimitCycles) {
-      record_wait_failure(err, kDevErrFullWait, smem_u32(bar), parity);
-      return false;
-    }
-  }
+// One arrive, on the barrier at this offset in every CTA of cta_mask, when all MMAs this
+// thread issued so far have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t mbar_smem_addr, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          mbar_smem_addr),
+      "h"(cta_mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
@@ -131,18 +137,20 @@ __device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* 
       : "memory");
 }
 
+// A warp's wait: every lane polls, and the warp leaves together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+  const bool ok = mbar_wait(bar, parity, err, kDevErrFullWait);
+  return __all_sync(0xffffffffu, ok);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
                   const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tml) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + kOffBar);
-  float* xbuf = reinterpret_cast<float*>(smem + kOffX);  // [128 rows][64 tokens]: the peer's S partial
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const uint32_t peer = rank ^ 1u;
-  const int nbox = rank == 0 ? 4 : 5;  // 64-dim boxes of this CTA's latent slice
-  const int dim0 = rank == 0 ? 0 : 256;
 
   // ---- work item of the pair: (b, [split j,] chunk c, row tile mt)
   int64_t item = blockIdx.x >> 1;
@@ -176,17 +184,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kNStage; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    mbar_init(&bars->q_moved, 4);
+    for (int s = 0; s < kNStage0; ++s) {
+      mbar_init(&bars->kv_full0[s], 1);
+      mbar_init(&bars->kv_empty0[s], 1);
+    }
+    for (int s = 0; s < kNStage1; ++s) {
+      mbar_init(&bars->kv_full1[s], 1);
+      mbar_init(&bars->kv_empty1[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&bars->s_full[k], 1);
-      mbar_init(&bars->p_full[k], kRows);
+      mbar_init(&bars->s_free[k], 4);
+      mbar_init(&bars->p_empty[k], 1);
+      mbar_init(&bars->p_full[k], 1);
+      mbar_init(&bars->o_ready[k], 4);
     }
     mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->x_full, kRows);  // one arrive per softmax thread of the peer
-    mbar_init(&bars->x_empty, kRows);
+    mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->l_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -196,166 +212,294 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
   const uint32_t tmem = bars->tmem_base;
+  const int lgrp = warp & 3;         // row warps 2..5 -> TMEM lane groups 2, 3, 0, 1
+  const int row = lgrp * 32 + lane;  // head row of the item (row warps)
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tml);
-      mbar_arrive_expect_tx(&bars->q_full, nbox * kQBoxBytes);
-      const int t_start = m0 / p.G;  // G = Hq = 128 rows per query row
-      for (int bx = 0; bx < nbox; ++bx)
-        tma_load_4d_plain(smem + kOffQ + bx * kQBoxBytes, &tmq, &bars->q_full, dim0 + bx * 64, 0, t_start, b);
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kNStage;
-        if (i >= kNStage && !mbar_wait(&bars->kv_empty[s], ((i / kNStage) - 1) & 1, p.err, kDevErrEmptyWait)) break;
-        mbar_arrive_expect_tx(&bars->kv_full[s], nbox * kBoxBytes);
-        uint8_t* st = smem + kOffRing + s * kStageBytes;
-        const int tok = (tile_begin + i) * kTN;
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full[s], dim0 + bx * 64, tok, 0, b);
-        issued = i + 1;
-      }
-      for (int i = max(0, issued - kNStage); i < issued; ++i) {
-        if (!mbar_wait(&bars->kv_full[i % kNStage], (i / kNStage) & 1, p.err, kDevErrDrainWait)) break;
-      }
-      mbar_wait(&bars->q_full, 0, p.err, kDevErrDrainWait);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
-      const uint32_t idesc_pv = tc::idesc_f16(128, kHalfDv, true, false, true);
-      const uint32_t q_base = smem_u32(smem + kOffQ);
-      const uint32_t ring = smem_u32(smem + kOffRing);
-      const int ksteps = nbox * 4;  // 16 elements per step
-      auto issue_s = [&](int i) {  // S_r(i) = Q_r K_r(i)^T into S buffer i & 1
-        const uint32_t kt = ring + (i % kNStage) * kStageBytes;
-        for (int ks = 0; ks < ksteps; ++ks) {
-          const uint64_t ad = tc::smem_desc_sw128(q_base + (ks >> 2) * kQBoxBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-          tc::mma_f16_ss(tmem + kColS + 64 * (i & 1), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+  if (rank == 0) {
+    // ================================================================ CTA 0: scores
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0 && n_tiles > 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tml);
+        mbar_arrive_expect_tx(&bars->q_full, kKBoxes * kQBoxBytes);
+        const int t_start = m0 / p.G;
+        for (int bx = 0; bx < kKBoxes; ++bx)
+          tma_load_4d_plain(smem + bx * kQBoxBytes, &tmq, &bars->q_full, bx * 64, 0, t_start, b);
+        bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
+        int issued = 0;
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          const int s = i % kNStage0;
+          if (i >= kNStage0 && !mbar_wait(&bars->kv_empty0[s], ((i / kNStage0) - 1) & 1, p.err, kDevErrEmptyWait))
+            break;
+          mbar_arrive_expect_tx(&bars->kv_full0[s], kStage0Bytes);
+          uint8_t* st = smem + s * kStage0Bytes;
+          const int tok = (tile_begin + i) * kTN;
+          for (int bx = 0; bx < kKBoxes; ++bx)
+            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, tok, 0, b);
+          issued = i + 1;
         }
-      };
-      auto issue_pv = [&](int i) {  // O_r += P(i) V_r(i)   (M 128, N 256, K 64)
-        const uint32_t vt = ring + (i % kNStage) * kStageBytes;  // V = the first 4 boxes of the slice
-        for (int ks = 0; ks < kTN / 16; ++ks) {
-          const uint64_t bd = tc::smem_desc_sw128(vt + ks * 2048, kBoxBytes, 1024);
-          tc::mma_f16_ts(tmem + kColO, tmem + kColP + 32 * (i & 1) + ks * 8, bd, idesc_pv,
-                         (i > 0 || ks > 0) ? 1u : 0u);
+        for (int i = max(0, issued - kNStage0); i < issued; ++i) {
+          if (!mbar_wait(&bars->kv_full0[i % kNStage0], (i / kNStage0) & 1, p.err, kDevErrDrainWait)) break;
         }
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, p.err, kDevErrFullWait);
-      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, p.err, kDevErrFullWait);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0);
-        tc::mma_commit(smem_u32(&bars->s_full[0]));
+        if (!ok) mbar_wait(&bars->q_full, 0, p.err, kDevErrDrainWait);  // Q copy still in flight
       }
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        if (i + 1 < n_tiles) {  // S(i+1) overlaps the softmax of tile i
-          ok = mbar_wait(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1, p.err, kDevErrFullWait);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer: S = Q K^T
+      if (lane == 0 && n_tiles > 0) {
+        const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
+        const uint32_t ring = smem_u32(smem);
+        bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrFullWait);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          const int s = i % kNStage0;
+          ok = mbar_wait(&bars->kv_full0[s], (i / kNStage0) & 1, p.err, kDevErrFullWait);
+          if (ok && i >= 2) ok = mbar_wait(&bars->s_free[i & 1], ((i >> 1) - 1) & 1, p.err, kDevErrFullWait);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_s(i + 1);
-          tc::mma_commit(smem_u32(&bars->s_full[(i + 1) & 1]));
+          // descriptor built once per tile; the k-steps add compile-time offsets (the issue
+          // loop, not the tensor pipe, bounds small-N MMAs when it does more)
+          const uint64_t bd0 = tc::smem_desc_sw128(ring + s * kStage0Bytes, 16, 1024);
+          const uint32_t d = tmem + kColS + 64 * (i & 1);
+#pragma unroll
+          for (int ks = 0; ks < kKBoxes * 4; ++ks) {
+            const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+            tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(smem_u32(&bars->s_full[i & 1]));
+          tc::mma_commit(smem_u32(&bars->kv_empty0[s]));
         }
-        ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
+      }
+    } else {
+      // ---------------------------------------------------------- row warps: softmax
+      const int m = m0 + row;
+      const bool valid = m < rows_total;
+      const int t_q = valid ? m / p.G : 0;
+      const int h = valid ? m % p.G : 0;
+      const int64_t hz = p.causal_offset + t_q;
+      const int64_t hz_min = p.causal_offset + (m0 + lgrp * 32) / p.G;
+      const uint32_t peer_p_full0 = map_to_rank(smem_u32(&bars->p_full[0]), 1);
+      const uint32_t peer_p_full1 = map_to_rank(smem_u32(&bars->p_full[1]), 1);
+      const uint32_t peer_precv = map_to_rank(smem_u32(smem + kOffPRecv), 1);
+      const uint32_t peer_arecv = map_to_rank(smem_u32(smem + kOffARecv), 1);
+      float m_used = -INFINITY, l_sum = 0.f;
+      bool ok = true;
+
+      if (n_tiles > 0) {
+        // Q row -> TMEM columns kColQ + 32 bx + (0..31): the A operand of every S MMA
+        ok = warp_wait(&bars->q_full, 0, p.err);
+        if (ok) {
+#pragma unroll 1
+          for (int bx = 0; bx < kKBoxes; ++bx) {
+            const uint8_t* qb = smem + bx * kQBoxBytes;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t w[16];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint4 v = *reinterpret_cast<const uint4*>(qb + swz128(row, (hf * 4 + u) * 16));
+                w[4 * u] = v.x;
+                w[4 * u + 1] = v.y;
+                w[4 * u + 2] = v.z;
+                w[4 * u + 3] = v.w;
+              }
+              tc::tmem_st16(t_lane + kColQ + 32 * bx + 16 * hf, w);
+            }
+          }
+          tc::tmem_wait_st();
+        }
+        fence_proxy_async_smem();  // the staging reads come before the ring's TMA writes
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->q_moved);
+      }
+
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int t0 = (tile_begin + i) * kTN;
+        ok = warp_wait(&bars->s_full[i & 1], (i >> 1) & 1, p.err);
         if (!ok) break;
         tc::fence_after_sync();
-        issue_pv(i);
-        tc::mma_commit(smem_u32(&bars->pv_done));
-        tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
+        float sv[kTN];
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(t_lane + kColS + 64 * (i & 1) + 16 * cc, r[cc]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[16 * cc + e] = __uint_as_float(r[cc][e]);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[i & 1]);
+
+        // ---- mask, running maximum (moved only when it rises by more than 2^8)
+        const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
+        const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+        if (need_mask) {
+          const int c_lo = min(max(r_lo - t0, 0), kTN);
+          const int c_hi = static_cast<int>(
+              min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTN));
+          const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
+#pragma unroll
+          for (int cc = 0; cc < kTN; ++cc) sv[cc] = (static_cast<unsigned>(cc - c_lo) < span) ? sv[cc] : -INFINITY;
+        }
+        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int cc = 4; cc < kTN; cc += 4) {
+          mx[0] = fmaxf(mx[0], sv[cc]);
+          mx[1] = fmaxf(mx[1], sv[cc + 1]);
+          mx[2] = fmaxf(mx[2], sv[cc + 2]);
+          mx[3] = fmaxf(mx[3], sv[cc + 3]);
+        }
+        const float sl = p.scale_log2;
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
+        float alpha = 1.f;  // factor CTA 1 applies to O before adding P(i) V(i)
+        if ((tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold)) {
+          const float m_new = fmaxf(m_used, tmax);
+          alpha = (i > 0) ? fast_exp2(m_used - m_new) : 1.f;
+          l_sum *= alpha;
+          m_used = m_new;
+        }
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+
+        // ---- P(i) into staging slot i & 1 (SW128 K-major rows); the slot's previous
+        // copy has landed once CTA 1 finished PV(i - 2) with it
+        if (i >= 2) {
+          ok = warp_wait(&bars->p_empty[i & 1], ((i >> 1) - 1) & 1, p.err);
+          if (!ok) break;
+        }
+        uint8_t* pst = smem + kOffPStage + (i & 1) * kPBytes;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ch = 0; ch < kTN / 8; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = fast_exp2(fmaf(sv[8 * ch + 2 * e], sl, -base));
+            const float p1 = fast_exp2(fmaf(sv[8 * ch + 2 * e + 1], sl, -base));
+            ls[(2 * e) & 3] += p0;
+            ls[(2 * e + 1) & 3] += p1;
+            w[e] = pack_bf16(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(pst + swz128(row, ch * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        float* ast = reinterpret_cast<float*>(smem + kOffAStage + (i & 1) * kRows * 4);
+        ast[row] = alpha;
+        fence_proxy_async_smem();  // generic writes before the bulk copy reads them
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bar = (i & 1) ? peer_p_full1 : peer_p_full0;
+          const uint32_t off = static_cast<uint32_t>((i & 1) * kPBytes + lgrp * 32 * 128);
+          bulk_copy_to_peer(peer_precv + off, smem_u32(smem + kOffPStage + off), 32 * 128, bar);
+          const uint32_t aoff = static_cast<uint32_t>((i & 1) * kRows * 4 + lgrp * 32 * 4);
+          bulk_copy_to_peer(peer_arecv + aoff, smem_u32(smem + kOffAStage + aoff), 32 * 4, bar);
+        }
+      }
+
+      // ---- final row sums to CTA 1 (it normalises O); lse from here
+      float* lst = reinterpret_cast<float*>(smem + kOffLStage);
+      lst[row] = l_sum;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_copy_to_peer(map_to_rank(smem_u32(smem + kOffLRecv + lgrp * 32 * 4), 1), smem_u32(lst + lgrp * 32),
+                          32 * 4, map_to_rank(smem_u32(&bars->l_full), 1));
+      }
+      constexpr float kLn2 = 0.6931471805599453f;
+      const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+      if (valid) {
+        if (x.fused) {
+          x.out_lse[(static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h] = lse;
+        } else {
+          const int part = j * p.n_chunk + c;
+          p.out_lse[((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h] = lse;
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int lgrp = warp & 3;          // warps 2..5 -> TMEM lane groups 2, 3, 0, 1
-    const int row = lgrp * 32 + lane;   // head row of the item
-    const int m = m0 + row;
-    const bool valid = m < rows_total;
-    const int t_q = valid ? m / p.G : 0;
-    const int h = valid ? m % p.G : 0;
-    const int64_t hz = p.causal_offset + t_q;
-    const int64_t hz_min = p.causal_offset + (m0 + lgrp * 32) / p.G;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
-    const uint32_t x_row_local = smem_u32(xbuf + row * kTN);
-    const uint32_t x_row_peer = map_to_rank(x_row_local, peer);
-    const uint32_t peer_x_full = map_to_rank(smem_u32(&bars->x_full), peer);
-    const uint32_t peer_x_empty = map_to_rank(smem_u32(&bars->x_empty), peer);
-    float m_used = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int t0 = (tile_begin + i) * kTN;
-      ok = mbar_wait(&bars->s_full[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
-      if (!ok) break;
-      tc::fence_after_sync();
-      const uint32_t s_col = t_lane + kColS + 64 * (i & 1);
-      float sv[kTN];
-      {
-        uint32_t r[4][16];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(s_col + 16 * cc, r[cc]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sv[16 * cc + e] = __uint_as_float(r[cc][e]);
+    // ================================================================ CTA 1: values
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0 && n_tiles > 0) {
+        tma_prefetch_desc(&tml);
+        int issued = 0;
+        for (int i = 0; i < n_tiles; ++i) {
+          const int s = i % kNStage1;
+          if (i >= kNStage1 && !mbar_wait(&bars->kv_empty1[s], ((i / kNStage1) - 1) & 1, p.err, kDevErrEmptyWait))
+            break;
+          mbar_arrive_expect_tx(&bars->kv_full1[s], kStage1Bytes);
+          uint8_t* st = smem + s * kStage1Bytes;
+          const int tok = (tile_begin + i) * kTN;
+          for (int bx = 0; bx < kVBoxes; ++bx)
+            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, tok, 0, b);
+          issued = i + 1;
+        }
+        for (int i = max(0, issued - kNStage1); i < issued; ++i) {
+          if (!mbar_wait(&bars->kv_full1[i % kNStage1], (i / kNStage1) & 1, p.err, kDevErrDrainWait)) break;
+        }
       }
-      // swap partial scores with the peer: my partial -> its buffer, its partial <- mine
-      if (i > 0) ok = wait_cluster(&bars->x_empty, (i - 1) & 1, p.err);  // the peer read its buffer
-      if (!ok) break;
-#pragma unroll
-      for (int q4 = 0; q4 < kTN / 4; ++q4)
-        st_cluster_v4(x_row_peer + 16 * q4, sv[4 * q4], sv[4 * q4 + 1], sv[4 * q4 + 2], sv[4 * q4 + 3]);
-      arrive_remote(peer_x_full);  // release: this thread's row is visible to the peer
-      ok = wait_cluster(&bars->x_full, i & 1, p.err);
-      if (!ok) break;
-      const float* xr = xbuf + row * kTN;
-#pragma unroll
-      for (int q4 = 0; q4 < kTN / 4; ++q4) {
-        const float4 v = *reinterpret_cast<const float4*>(xr + 4 * q4);
-        sv[4 * q4] += v.x;
-        sv[4 * q4 + 1] += v.y;
-        sv[4 * q4 + 2] += v.z;
-        sv[4 * q4 + 3] += v.w;
-      }
-      arrive_remote(peer_x_empty);  // this thread's row of my buffer may be written again
-
-      // ---- softmax on S = S_0 + S_1 (identical in both CTAs)
-      const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
-      const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
-      if (need_mask) {
-        const int c_lo = min(max(r_lo - t0, 0), kTN);
-        const int c_hi = static_cast<int>(
-            min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTN));
-        const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
-#pragma unroll
-        for (int cc = 0; cc < kTN; ++cc) sv[cc] = (static_cast<unsigned>(cc - c_lo) < span) ? sv[cc] : -INFINITY;
-      }
-      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-      for (int cc = 4; cc < kTN; cc += 4) {
-        mx[0] = fmaxf(mx[0], sv[cc]);
-        mx[1] = fmaxf(mx[1], sv[cc + 1]);
-        mx[2] = fmaxf(mx[2], sv[cc + 2]);
-        mx[3] = fmaxf(mx[3], sv[cc + 3]);
-      }
-      const float sl = p.scale_log2;
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
-      const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? fmaxf(m_used, tmax) : m_used;
-        if (i > 0) {
-          ok = mbar_wait(&bars->pv_done, (i - 1) & 1, p.err, kDevErrFullWait);  // O final up to tile i-1
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer: O += P V
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->l_full, kRows * 4);
+        const uint32_t idesc_pv = tc::idesc_f16(128, 256, true, false, true);
+        const uint32_t ring = smem_u32(smem);
+        const uint32_t precv = smem_u32(smem + kOffPRecv);
+        static_assert((kOffBar + 1024) < (1 << 18), "descriptor start addresses (>> 4) fit 14 bits");
+        bool ok = true;
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          const int s = i % kNStage1;
+          mbar_arrive_expect_tx(&bars->p_full[i & 1], kPMsgBytes);
+          ok = mbar_wait(&bars->kv_full1[s], (i / kNStage1) & 1, p.err, kDevErrFullWait);
+          if (ok) ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
+          if (ok) ok = mbar_wait(&bars->o_ready[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
+          if (!ok) break;
           tc::fence_after_sync();
-          const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+          const uint64_t vd0 = tc::smem_desc_sw128(ring + s * kStage1Bytes, kBoxBytes, 1024);
+          const uint64_t ad0 = tc::smem_desc_sw128(precv + (i & 1) * kPBytes, 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < kTN / 16; ++ks) {
+            const uint64_t ad = ad0 + static_cast<uint64_t>((ks * 32) >> 4);
+            const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+            tc::mma_f16_ss(tmem + kColO, ad, vd0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv, acc);
+            tc::mma_f16_ss(tmem + kColO + 256, ad, vd0 + static_cast<uint64_t>((4 * kBoxBytes + ks * 2048) >> 4),
+                           idesc_pv, acc);
+          }
+          tc::mma_commit(smem_u32(&bars->pv_done));
+          tc::mma_commit(smem_u32(&bars->kv_empty1[s]));
+          // CTA 0 may refill P slot i & 1 (it waits for this only when a tile i + 2 exists)
+          if (i + 2 < n_tiles) mma_commit_multicast(smem_u32(&bars->p_empty[i & 1]), 0x1);
+          if (i == n_tiles - 1) tc::mma_commit(smem_u32(&bars->o_final));
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- row warps
+      const int m = m0 + row;
+      const bool valid = m < rows_total;
+      const int t_q = valid ? m / p.G : 0;
+      const int h = valid ? m % p.G : 0;
+      const float* arecv = reinterpret_cast<const float*>(smem + kOffARecv);
+      bool ok = true;
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int s = i % kNStage1;
+        const int t0 = (tile_begin + i) * kTN;
+        ok = warp_wait(&bars->kv_full1[s], (i / kNStage1) & 1, p.err);
+        if (ok) ok = warp_wait(&bars->p_full[i & 1], (i >> 1) & 1, p.err);
+        if (!ok) break;
+        const float alpha = arecv[(i & 1) * kRows + row];
+        if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
+          // O rows of this warp *= alpha once PV(i - 1) has completed (PV(i - 2) has: P(i)
+          // was sent only after it)
+          ok = warp_wait(&bars->pv_done, (i - 1) & 1, p.err);
+          if (!ok) break;
+          tc::fence_after_sync();
 #pragma unroll 1
-          for (int cc = 0; cc < kHalfDv / 16; cc += 2) {
+          for (int cc = 0; cc < 512 / 16; cc += 2) {
             uint32_t r[2][16];
             tc::tmem_ld16(t_lane + kColO + 16 * cc, r[0]);
             tc::tmem_ld16(t_lane + kColO + 16 * (cc + 1), r[1]);
@@ -368,117 +512,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::tmem_st16(t_lane + kColO + 16 * (cc + 1), r[1]);
           }
           tc::tmem_wait_st();
-          l_sum *= alpha;
-        } else {
-          l_sum = 0.f;
         }
-        m_used = m_new;
-      }
-      const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      // P(i) goes to P buffer i & 1; its previous user PV(i-2) finished before S(i) ran
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int cc = 0; cc < kTN / 32; ++cc) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(sv[32 * cc + 2 * e], sl, -base));
-          const float p1 = fast_exp2(fmaf(sv[32 * cc + 2 * e + 1], sl, -base));
-          ls[(2 * e) & 3] += p0;
-          ls[(2 * e + 1) & 3] += p1;
-          w[e] = pack_bf16(p0, p1);
+        if (!((t0 >= r_lo) && (t0 + kTN <= r_hi))) {
+          // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
+          // zero their V rows so that p = 0 contributes nothing
+          if (row < kTN) {
+            const int tok = t0 + row;
+            if (tok < r_lo || tok >= r_hi) {
+              uint8_t* vt = smem + s * kStage1Bytes;
+              for (int bx = 0; bx < kVBoxes; ++bx)
+                for (int q = 0; q < 8; ++q)
+                  *reinterpret_cast<uint4*>(vt + bx * kBoxBytes + row * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async_smem();
         }
-        tc::tmem_st16(t_lane + kColP + 32 * (i & 1) + 16 * cc, w);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_ready[i & 1]);
       }
-      tc::tmem_wait_st();
-      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (!in_range) {
-        // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
-        // zero their rows of this CTA's V slice so that p = 0 contributes nothing
-        const int s_idx = i % kNStage;
-        mbar_wait(&bars->kv_full[s_idx], (i / kNStage) & 1, p.err, kDevErrFullWait);
-        if (row < kTN) {
-          const int tok = t0 + row;
-          if (tok < r_lo || tok >= r_hi) {
-            uint8_t* vt = smem + kOffRing + s_idx * kStageBytes;
-            for (int bx = 0; bx < 4; ++bx)
-              for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4*>(vt + bx * kBoxBytes + row * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+
+      // ---- epilogue: O / l for all 512 dims of this CTA's rows
+      if (ok && n_tiles > 0) {
+        ok = warp_wait(&bars->o_final, 0, p.err);
+        tc::fence_after_sync();
+      }
+      const bool got_l = warp_wait(&bars->l_full, 0, p.err);
+      const float l_sum = got_l ? reinterpret_cast<const float*>(smem + kOffLRecv)[row] : 0.f;
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const bool have_o = ok && n_tiles > 0;
+      constexpr int kDv = 512;
+      if (x.fused) {
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(x.out_bf16) + ((static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h) * kDv;
+#pragma unroll 1
+        for (int cc = 0; cc < kDv / 16; ++cc) {
+          uint32_t r[16];
+          if (have_o) {
+            tc::tmem_ld16(t_lane + kColO + 16 * cc, r);
+            tc::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = 0u;
+          }
+          if (valid) {
+            uint4 w0, w1;
+            w0.x = pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+            w0.y = pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+            w0.z = pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+            w0.w = pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+            w1.x = pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+            w1.y = pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+            w1.z = pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+            w1.w = pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
+            *reinterpret_cast<uint4*>(orow + 16 * cc) = w0;
+            *reinterpret_cast<uint4*>(orow + 16 * cc + 8) = w1;
           }
         }
-        fence_proxy_async_smem();
-      }
-      tc::fence_before_sync();
-      mbar_arrive(&bars->p_full[i & 1]);
-    }
-
-    // ---- epilogue: this CTA's 256 dims of O / l; CTA 0 writes lse
-    if (n_tiles > 0 && ok) {
-      ok = mbar_wait(&bars->pv_done, (n_tiles - 1) & 1, p.err, kDevErrFullWait);
-      tc::fence_after_sync();
-    }
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    constexpr float kLn2 = 0.6931471805599453f;
-    const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
-    const int dv_total = 2 * kHalfDv;
-    if (x.fused) {
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(x.out_bf16) +
-                            ((static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h) * dv_total + rank * kHalfDv;
+      } else {
+        const int part = j * p.n_chunk + c;
+        const int64_t ro = ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
+        float* orow = p.out_o + ro * kDv;
+        const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
 #pragma unroll 1
-      for (int cc = 0; cc < kHalfDv / 16; ++cc) {
-        uint32_t r[16];
-        if (n_tiles > 0) {
-          tc::tmem_ld16(t_lane + kColO + 16 * cc, r);
-          tc::tmem_wait_ld();
-        } else {
+        for (int cc = 0; cc < kDv / 16; ++cc) {
+          uint32_t r[16];
+          if (have_o) {
+            tc::tmem_ld16(t_lane + kColO + 16 * cc, r);
+            tc::tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = 0u;
-        }
-        if (valid) {
-          uint4 w0, w1;
-          w0.x = pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-          w0.y = pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-          w0.z = pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-          w0.w = pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-          w1.x = pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
-          w1.y = pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
-          w1.z = pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
-          w1.w = pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
-          *reinterpret_cast<uint4*>(orow + 16 * cc) = w0;
-          *reinterpret_cast<uint4*>(orow + 16 * cc + 8) = w1;
+            for (int e = 0; e < 16; ++e) r[e] = 0u;
+          }
+          if (write_o) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(orow + 16 * cc + e) =
+                  make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                              __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+          }
         }
       }
-      if (valid && rank == 0) x.out_lse[(static_cast<int64_t>(b) * p.Tq + t_q) * p.Hq + h] = lse;
-    } else {
-      const int part = j * p.n_chunk + c;
-      const int64_t ro = ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
-      float* orow = p.out_o + ro * dv_total + rank * kHalfDv;
-      const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
-#pragma unroll 1
-      for (int cc = 0; cc < kHalfDv / 16; ++cc) {
-        uint32_t r[16];
-        if (n_tiles > 0) {
-          tc::tmem_ld16(t_lane + kColO + 16 * cc, r);
-          tc::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = 0u;
-        }
-        if (write_o) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(orow + 16 * cc + e) =
-                make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                            __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
-        }
-      }
-      if (valid && rank == 0) p.out_lse[ro] = lse;
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  cluster_sync();  // the peer no longer touches this CTA's shared memory
+  cluster_sync();  // no copy or remote arrive into the peer is still pending
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
