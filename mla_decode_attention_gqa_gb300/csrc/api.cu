@@ -189,7 +189,7 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
   else
     pl.variant = decode ? GqaVariant::kBf16D128Decode : GqaVariant::kBf16D128Prefill;
   GqaLaunchInfo li = pl.mla ? mla_launch_info() : gqa_launch_info(pl.variant);
-  if (pl.mla && use_mla_tc(d)) li = GqaLaunchInfo{mla_tc_rows_per_item(), 192, 0, 1, 2};
+  if (pl.mla && use_mla_tc(d)) li = GqaLaunchInfo{mla_tc_rows_per_item(), 224, 0, 1, 2};
   pl.rows_per_cta = li.rows_per_cta;
   const int64_t rows = static_cast<int64_t>(d->Tq) * G;
   pl.m_tiles = static_cast<int>((rows + li.rows_per_cta - 1) / li.rows_per_cta);

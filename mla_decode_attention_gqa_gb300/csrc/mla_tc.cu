@@ -21,10 +21,11 @@
 //          tile hits L2), applies the rescale factors to O in tensor memory when a
 //          row maximum moved, and accumulates O += P V (A = P from shared memory,
 //          B = the MN-major V tile, two N = 256 halves).
-// Tensor work per 64-token tile: 36 k-steps of N = 64 on CTA 0, 8 of N = 256 on CTA 1.
-// Only bf16 P (16 KB per tile) crosses between the SMs, one way.  Warp roles per CTA:
-// TMA producer, one MMA-issuing thread, four row warps (softmax on CTA 0; rescale,
-// boundary-row zeroing and the epilogue on CTA 1).  Every wait is bounded.
+// Tensor work per 64-token tile: 36 k-steps of N = 64 on CTA 0 (split over two issuing
+// warps: one thread cannot issue N = 64 MMAs fast enough to keep the pipe busy), 8 of
+// N = 256 on CTA 1.  Only bf16 P (16 KB per tile) crosses between the SMs, one way.
+// Warp roles per CTA: TMA producer, MMA issuer(s), four row warps (softmax on CTA 0;
+// rescale, boundary-row zeroing and the epilogue on CTA 1).  Every wait is bounded.
 #include <cuda_runtime.h>
 
 #include "skv_common.cuh"
@@ -37,7 +38,7 @@ namespace {
 
 constexpr int kTN = 64;          // tokens per latent tile
 constexpr int kRows = 128;       // heads per item (MMA M)
-constexpr int kThreads = 6 * 32;
+constexpr int kThreads = 7 * 32;  // warp 6: second score-MMA issuer on CTA 0
 constexpr int kKBoxes = 9;       // 64-dim boxes of the 576-dim key
 constexpr int kVBoxes = 8;       // 64-dim boxes of the 512-dim value
 constexpr int kBoxBytes = kTN * 128;     // 64 tokens x 64 dims
@@ -49,6 +50,8 @@ constexpr int kOffPStage = kNStage0 * kStage0Bytes;  // 144 KB: P staging, 2 slo
 constexpr int kPBytes = kRows * 128;                 // 128 heads x 64 tokens bf16
 constexpr int kOffAStage = kOffPStage + 2 * kPBytes;  // rescale factors, 2 slots x 512 B
 constexpr int kOffLStage = kOffAStage + 2 * kRows * 4;  // final row sums, 512 B
+constexpr int kOffQRope = 182272;  // Q dims 512..575 (the rope part), 16 KB, kept in shared memory
+constexpr int kQTmemBoxes = 8;     // Q dims 0..511 live in TMEM
 // CTA 1 (values): a 3-stage ring of 512-dim tiles, P / factor / row-sum receive buffers
 constexpr int kNStage1 = 3;
 constexpr int kStage1Bytes = kVBoxes * kBoxBytes;  // 64 KB
@@ -57,13 +60,20 @@ constexpr int kOffARecv = kOffPRecv + 2 * kPBytes;
 constexpr int kOffLRecv = kOffARecv + 2 * kRows * 4;
 constexpr int kOffBar = kOffLRecv + kRows * 4;
 constexpr int kSmem = 1024 + kOffBar + 256;
-static_assert(kKBoxes * kQBoxBytes == kNStage0 * kStage0Bytes, "Q staging reuses the ring bytes");
+static_assert(kQTmemBoxes * kQBoxBytes <= kNStage0 * kStage0Bytes, "Q staging reuses the ring bytes");
+static_assert(kOffQRope % 1024 == 0 && kOffQRope >= kOffLStage + kRows * 4 && kOffQRope + kQBoxBytes <= kOffBar,
+              "CTA 0's rope Q sits between its staging buffers and the barriers");
 static_assert(kOffLStage + kRows * 4 <= kOffBar, "CTA 0 layout fits below the barriers");
 static_assert(kOffPStage % 1024 == 0 && kOffPRecv % 1024 == 0, "P tiles need 1024-byte swizzle atoms");
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // CTA 0: S buffer b at kColS + 64 b (b = 0, 1)
-constexpr uint32_t kColQ = 128;  // CTA 0: Q, 288 columns (two bf16 per column)
+// CTA 0: S buffer b at kColS + 128 b holds two partial sums, columns +0 (k-steps 0..17,
+// issued by warp 1) and +64 (k-steps 18..35, issued by warp 6): a single issuing thread
+// cannot keep the tensor pipe busy with N = 64 MMAs, two can.
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColQ = 256;  // CTA 0: Q dims 0..511, 256 columns (two bf16 per column)
+constexpr int kKSteps = kKBoxes * 4;     // 36 k-steps of 16 dims
+constexpr int kKStepsA = kKSteps / 2;    // warp 1: k-steps 0..17; warp 6: 18..35
 constexpr uint32_t kColO = 0;    // CTA 1: O, 512 columns
 constexpr uint32_t kPMsgBytes = 4 * (32 * 128 + 32 * 4);  // P rows + factors, four warps
 constexpr float kRescaleThreshold = 8.0f;
@@ -76,7 +86,7 @@ struct MlaBars {
   uint64_t q_moved;       // Q copied into TMEM by the four row warps; staging bytes free
   uint64_t kv_full0[kNStage0];
   uint64_t kv_empty0[kNStage0];
-  uint64_t s_full[2];     // S(i) in TMEM buffer i & 1
+  uint64_t s_full[2];     // S(i) in TMEM buffer i & 1 (one commit from each issuing warp)
   uint64_t s_free[2];     // the row warps have read S buffer b
   uint64_t p_empty[2];    // CTA 1 finished PV with P slot b (arrived by CTA 1's MMA commit)
   // CTA 1
@@ -187,14 +197,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_moved, 4);
     for (int s = 0; s < kNStage0; ++s) {
       mbar_init(&bars->kv_full0[s], 1);
-      mbar_init(&bars->kv_empty0[s], 1);
+      mbar_init(&bars->kv_empty0[s], 2);  // both score-MMA warps release the stage
     }
     for (int s = 0; s < kNStage1; ++s) {
       mbar_init(&bars->kv_full1[s], 1);
       mbar_init(&bars->kv_empty1[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars->s_full[k], 1);
+      mbar_init(&bars->s_full[k], 2);
       mbar_init(&bars->s_free[k], 4);
       mbar_init(&bars->p_empty[k], 1);
       mbar_init(&bars->p_full[k], 1);
@@ -228,7 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->q_full, kKBoxes * kQBoxBytes);
         const int t_start = m0 / p.G;
         for (int bx = 0; bx < kKBoxes; ++bx)
-          tma_load_4d_plain(smem + bx * kQBoxBytes, &tmq, &bars->q_full, bx * 64, 0, t_start, b);
+          tma_load_4d_plain(smem + (bx < kQTmemBoxes ? bx * kQBoxBytes : kOffQRope), &tmq, &bars->q_full, bx * 64, 0,
+                            t_start, b);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
         int issued = 0;
         for (int i = 0; i < n_tiles && ok; ++i) {
@@ -247,11 +258,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!ok) mbar_wait(&bars->q_full, 0, p.err, kDevErrDrainWait);  // Q copy still in flight
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer: S = Q K^T
+    } else if (warp == 1 || warp == 6) {
+      // ---------------------------------------------------------- MMA issuers: S = Q K^T
+      // warp 1: k-steps 0..17 into S buffer + 0; warp 6: k-steps 18..35 into S buffer + 64
+      // (its last four, the rope dims, take A = Q from shared memory)
       if (lane == 0 && n_tiles > 0) {
         const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
         const uint32_t ring = smem_u32(smem);
+        const uint64_t qrope_d0 = tc::smem_desc_sw128(smem_u32(smem + kOffQRope), 16, 1024);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrFullWait);
         for (int i = 0; i < n_tiles && ok; ++i) {
           const int s = i % kNStage0;
@@ -259,14 +273,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ok && i >= 2) ok = mbar_wait(&bars->s_free[i & 1], ((i >> 1) - 1) & 1, p.err, kDevErrFullWait);
           if (!ok) break;
           tc::fence_after_sync();
-          // descriptor built once per tile; the k-steps add compile-time offsets (the issue
-          // loop, not the tensor pipe, bounds small-N MMAs when it does more)
+          // descriptors built once per tile; the k-steps add compile-time offsets
           const uint64_t bd0 = tc::smem_desc_sw128(ring + s * kStage0Bytes, 16, 1024);
-          const uint32_t d = tmem + kColS + 64 * (i & 1);
+          if (warp == 1) {
+            const uint32_t d = tmem + kColS + 128 * (i & 1);
 #pragma unroll
-          for (int ks = 0; ks < kKBoxes * 4; ++ks) {
-            const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
-            tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kKStepsA; ++ks) {
+              const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+              tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
+            }
+          } else {
+            const uint32_t d = tmem + kColS + 128 * (i & 1) + 64;
+#pragma unroll
+            for (int ks = kKStepsA; ks < kKSteps; ++ks) {
+              const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+              const uint32_t acc = ks > kKStepsA ? 1u : 0u;
+              if (ks < kQTmemBoxes * 4) {
+                tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, acc);
+              } else {
+                const uint64_t ad = qrope_d0 + static_cast<uint64_t>(((ks & 3) * 32) >> 4);
+                tc::mma_f16_ss(d, ad, bd, idesc_s, acc);
+              }
+            }
           }
           tc::mma_commit(smem_u32(&bars->s_full[i & 1]));
           tc::mma_commit(smem_u32(&bars->kv_empty0[s]));
@@ -288,11 +316,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
 
       if (n_tiles > 0) {
-        // Q row -> TMEM columns kColQ + 32 bx + (0..31): the A operand of every S MMA
+        // Q row, dims 0..511 -> TMEM columns kColQ + 32 bx + (0..31): the A operand of the
+        // TMEM-fed S MMAs
         ok = warp_wait(&bars->q_full, 0, p.err);
         if (ok) {
 #pragma unroll 1
-          for (int bx = 0; bx < kKBoxes; ++bx) {
+          for (int bx = 0; bx < kQTmemBoxes; ++bx) {
             const uint8_t* qb = smem + bx * kQBoxBytes;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -324,13 +353,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float sv[kTN];
         {
           uint32_t r[4][16];
+          const uint32_t sc = t_lane + kColS + 128 * (i & 1);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(t_lane + kColS + 64 * (i & 1) + 16 * cc, r[cc]);
+          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(sc + 16 * cc, r[cc]);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int e = 0; e < 16; ++e) sv[16 * cc + e] = __uint_as_float(r[cc][e]);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(sc + 64 + 16 * cc, r[cc]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[16 * cc + e] += __uint_as_float(r[cc][e]);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -477,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (i == n_tiles - 1) tc::mma_commit(smem_u32(&bars->o_final));
         }
       }
-    } else {
+    } else if (warp <= 5) {
       // ---------------------------------------------------------- row warps
       const int m = m0 + row;
       const bool valid = m < rows_total;
