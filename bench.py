@@ -46,6 +46,7 @@ METRIC = "decode attn µs/layer & KV-read HBM GB/s (fraction of GB300 peak) at S
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+# sources a traffic record was measured with, when the record does not list its own
 KERNEL_SOURCES = ["mla_decode_attention_gqa_gb300/csrc/gqa_partial.cu", "mla_decode_attention_gqa_gb300/csrc/skv_common.cuh"]
 
 
@@ -94,9 +95,9 @@ def bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -109,9 +110,10 @@ def ncu_traffic(workload_name):
         with open(TRAFFIC_PATH) as f:
             rec = json.load(f)
         e = rec[workload_name]
-        if e.get("kernel_source_sha") != kernel_source_sha():
+        if e.get("kernel_source_sha") != kernel_source_sha(e.get("kernel_sources")):
             return None
-        return float(e["dram_bytes_per_launch"])
+        v = e.get("dram_bytes_per_launch")
+        return None if v is None else float(v)
     except Exception:
         return None
 
@@ -338,7 +340,10 @@ def ours_arm(args, w, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         host = {}
-        for key in ("q", "k", "v", "k_scale", "v_scale", "seq_lens"):
+        # the MLA value cache is a view of the latent (k): it is copied once, as k
+        keys = ("q", "k", "k_scale", "v_scale", "seq_lens") if w.mla else ("q", "k", "v", "k_scale", "v_scale",
+                                                                            "seq_lens")
+        for key in keys:
             t = inp[key]
             host[key] = None if t is None else t.cpu().pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
@@ -346,6 +351,8 @@ def ours_arm(args, w, ws, rank, local):
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
         dev_bufs = {k2: (None if t is None else torch.empty_like(t, device=dev)) for k2, t in host.items()}
+        if w.mla:
+            dev_bufs["v"] = dev_bufs["k"][..., : w.dv]
         del inp
         torch.cuda.empty_cache()
 
