@@ -16,6 +16,10 @@ Input recipe (per workload, seed = 1000 + index):
     e4m3 0x7F) so that any read past the end of a sequence shows up in the output.
   * MLA workloads hold one latent buffer [B, 1, S, dk]; V is the view of its first
     ``dv`` columns (same storage, row stride dk).
+  * Zigzag / striped ring-prefill workloads store each of the n_split ranks' tokens in
+    the rank's layout order (``layout_positions``); the KV cache is the ranks' shards
+    one after another and the query chunk is rank ``cp_rank``'s tokens.  The original
+    positions go with them as int32 arrays q_pos [B, Tq] and k_pos [B, S].
 
 Shapes follow the pages' workloads: Llama-405B-like GQA heads (Hq=128, Hkv=8,
 d=128) from the Helix and context-parallel pages, a DeepSeek-style absorbed MLA
@@ -49,6 +53,8 @@ class Workload:
     softmax_scale: float = 0.0  # 0 -> 1/sqrt(dk)
     mla: bool = False
     seed: int = 1000
+    layout: str = "contiguous"  # "contiguous" | "zigzag" | "striped" (position-array workloads)
+    cp_rank: int = 0            # the emulated rank whose query chunk is computed
 
     @property
     def scale(self) -> float:
@@ -62,6 +68,31 @@ class Workload:
         """[B][n_split+1] contiguous, equal sequence shards of the allocated S."""
         row = [(j * self.S) // self.n_split for j in range(self.n_split + 1)]
         return [list(row) for _ in range(self.B)]
+
+
+def layout_positions(layout, S, cp, rank):
+    """Original positions of the tokens that rank ``rank`` of ``cp`` stores, in storage
+    order ("现代大模型推理并行策略总览", section "序列布局：Contiguous、Zigzag 与 Striped";
+    "Context Parallelism for Scalable Million-Token Inference", section "Load-balanced
+    sharding makes causal work and memory land evenly"):
+      contiguous: [r m, (r + 1) m) with m = S / cp;
+      zigzag:     2 cp blocks of S / (2 cp); rank r holds block r, then block 2 cp - 1 - r;
+      striped:    positions r, r + cp, r + 2 cp, ...
+    """
+    if S % cp:
+        raise ValueError("S must be a multiple of cp")
+    if layout == "contiguous":
+        m = S // cp
+        return list(range(rank * m, (rank + 1) * m))
+    if layout == "zigzag":
+        if S % (2 * cp):
+            raise ValueError("zigzag needs S to be a multiple of 2 cp")
+        blk = S // (2 * cp)
+        late = 2 * cp - 1 - rank
+        return list(range(rank * blk, (rank + 1) * blk)) + list(range(late * blk, (late + 1) * blk))
+    if layout == "striped":
+        return list(range(rank, S, cp))
+    raise ValueError(f"unknown layout {layout}")
 
 
 # The five workloads, in the order they are numbered (0..4).
@@ -78,7 +109,15 @@ MLA_ABSORBED = Workload("mla_absorbed_decode_s32k", B=16, Tq=1, Hq=128, Hkv=1, d
 RING_PREFILL = Workload("ring_prefill_chunk_8x4096", B=1, Tq=4096, Hq=128, Hkv=8, dk=128,
                         dv=128, S=8 * 4096, n_split=8, causal_offset=7 * 4096, seed=1004)
 
-WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL]
+# The ring prefill chunk with load-balanced layouts: rank 0's 4096 query tokens (zigzag:
+# blocks 0 and 15 of 16; striped: every 8th token) against all 8 ranks' shards.
+RING_PREFILL_ZIGZAG = Workload("ring_prefill_zigzag_8x4096", B=1, Tq=4096, Hq=128, Hkv=8, dk=128, dv=128,
+                               S=8 * 4096, n_split=8, layout="zigzag", cp_rank=0, seed=1005)
+RING_PREFILL_STRIPED = Workload("ring_prefill_striped_8x4096", B=1, Tq=4096, Hq=128, Hkv=8, dk=128, dv=128,
+                                S=8 * 4096, n_split=8, layout="striped", cp_rank=0, seed=1006)
+
+WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL, RING_PREFILL_ZIGZAG,
+             RING_PREFILL_STRIPED]
 
 
 def scaled(w: Workload, **kw) -> Workload:
@@ -118,6 +157,8 @@ def make_inputs(w: Workload, device="cpu", poison=True):
       seq_lens int32 [B] (on ``device``)
       seq_lens_host  list[int]
       split_bounds   list[list[int]]  ([B][n_split+1])
+      q_pos, k_pos   int32 [B, Tq], [B, S] original positions (layout workloads), else None
+      q_pos_host, k_pos_host  the same as lists, or None
     """
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
@@ -167,6 +208,18 @@ def make_inputs(w: Workload, device="cpu", poison=True):
     else:
         raise ValueError(f"unknown kv dtype {w.kv_dtype}")
 
+    q_pos = k_pos = None
+    q_pos_host = k_pos_host = None
+    if w.layout != "contiguous":
+        if w.S % w.n_split or w.Tq != w.S // w.n_split:
+            raise ValueError("a layout workload holds one rank's chunk: Tq = S / n_split")
+        k_row = [p for r in range(w.n_split) for p in layout_positions(w.layout, w.S, w.n_split, r)]
+        q_row = layout_positions(w.layout, w.S, w.n_split, w.cp_rank)
+        q_pos_host = [list(q_row) for _ in range(B)]
+        k_pos_host = [list(k_row) for _ in range(B)]
+        q_pos = torch.tensor(q_pos_host, dtype=torch.int32, device=dev)
+        k_pos = torch.tensor(k_pos_host, dtype=torch.int32, device=dev)
+
     return {
         "q": q,
         "k": k,
@@ -176,4 +229,8 @@ def make_inputs(w: Workload, device="cpu", poison=True):
         "seq_lens": seq.to(torch.int32),
         "seq_lens_host": seq_host,
         "split_bounds": w.split_bounds(),
+        "q_pos": q_pos,
+        "k_pos": k_pos,
+        "q_pos_host": q_pos_host,
+        "k_pos_host": k_pos_host,
     }

@@ -27,7 +27,11 @@ natural log of the softmax denominator over *scaled* scores; a partial output is
 normalised by its own denominator; the merged LSE is m + ln(den); a split with no
 visible token has o = 0 and lse = -inf and weight 0 in the merge; query row i of a
 chunk sits at global position causal_offset + i and sees KV position t iff
-t <= causal_offset + i.
+t <= causal_offset + i.  When the tokens are stored out of sequence order (the
+zigzag and striped layouts of [Survey] section "序列布局：Contiguous、Zigzag 与
+Striped"), every stored query row and KV token carries its original position and the
+same rule applies to those positions: a token is visible iff its position is at most
+the row's.
 """
 
 import numpy as np
@@ -38,6 +42,12 @@ def kv_head_of(h, Hq, Hkv):
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     return h // (Hq // Hkv)
+
+
+def visible_mask(q_pos, kv_pos):
+    """[R, n] bool: KV token t is visible to query row i iff kv_pos[t] <= q_pos[i]
+    (causal mask by original position, [Survey] section "序列布局")."""
+    return np.asarray(kv_pos)[None, :] <= np.asarray(q_pos)[:, None]
 
 
 def attend(q, k, v, scale, q_pos=None, kv_pos=None):
@@ -65,8 +75,7 @@ def attend(q, k, v, scale, q_pos=None, kv_pos=None):
         return o, lse
     s = scale * (q @ k.T)  # [R, n] scores
     if q_pos is not None and kv_pos is not None:
-        visible = np.asarray(kv_pos)[None, :] <= np.asarray(q_pos)[:, None]
-        s = np.where(visible, s, -np.inf)  # invisible tokens take no part
+        s = np.where(visible_mask(q_pos, kv_pos), s, -np.inf)  # invisible tokens take no part
     m = s.max(axis=1)
     has = np.isfinite(m)  # rows with at least one visible token
     m_safe = np.where(has, m, 0.0)
@@ -83,7 +92,7 @@ def _visible_range(lo, hi, seq_len):
     return max(lo, 0), min(hi, seq_len)
 
 
-def split_attention(q, k, v, seq_lens, split_bounds, causal_offset, scale):
+def split_attention(q, k, v, seq_lens, split_bounds, causal_offset, scale, q_positions=None, k_positions=None):
     """Partial attention of every split of the KV cache ([Helix], [CP]).
 
     q : [B, Tq, Hq, dk] float64
@@ -93,6 +102,9 @@ def split_attention(q, k, v, seq_lens, split_bounds, causal_offset, scale):
     split_bounds : [B][n_split + 1] ints; split j of batch b is [b_j, b_{j+1})
     causal_offset : query row i sits at global position causal_offset + i
     scale : softmax scale
+    q_positions, k_positions : optional [B][Tq] and [B][S] original positions of the
+        stored query rows and KV tokens (zigzag / striped storage); when given they
+        replace causal_offset + i and t in the causal rule.
 
     Returns (o [n_split, B, Tq, Hq, dv], lse [n_split, B, Tq, Hq]).
     """
@@ -102,13 +114,14 @@ def split_attention(q, k, v, seq_lens, split_bounds, causal_offset, scale):
     n_split = bounds.shape[1] - 1
     o = np.zeros((n_split, B, Tq, Hq, dv))
     lse = np.full((n_split, B, Tq, Hq), -np.inf)
-    q_pos = causal_offset + np.arange(Tq)
+    positional = q_positions is not None and k_positions is not None
     for b in range(B):
+        q_pos = np.asarray(q_positions[b], dtype=np.int64) if positional else causal_offset + np.arange(Tq)
         for j in range(n_split):
             lo, hi = _visible_range(int(bounds[b, j]), int(bounds[b, j + 1]), int(seq_lens[b]))
             if hi <= lo:
                 continue
-            kv_pos = np.arange(lo, hi)
+            kv_pos = np.asarray(k_positions[b], dtype=np.int64)[lo:hi] if positional else np.arange(lo, hi)
             for h in range(Hq):
                 g = kv_head_of(h, Hq, Hkv)
                 oo, ll = attend(q[b, :, h, :], k[b, g, lo:hi], v[b, g, lo:hi], scale, q_pos, kv_pos)
@@ -117,11 +130,11 @@ def split_attention(q, k, v, seq_lens, split_bounds, causal_offset, scale):
     return o, lse
 
 
-def full_attention(q, k, v, seq_lens, causal_offset, scale):
+def full_attention(q, k, v, seq_lens, causal_offset, scale, q_positions=None, k_positions=None):
     """Unsplit attention over every existing token: the result the merge must equal."""
     B = q.shape[0]
     bounds = [[0, int(seq_lens[b])] for b in range(B)]
-    o, lse = split_attention(q, k, v, seq_lens, bounds, causal_offset, scale)
+    o, lse = split_attention(q, k, v, seq_lens, bounds, causal_offset, scale, q_positions, k_positions)
     return o[0], lse[0]
 
 

@@ -12,9 +12,11 @@ import oracle
 from oracle import attention as A
 from oracle import formats as F
 import tests.test_oracle_pins as P
+import tests.test_oracle_layouts as L
 
 _orig_attend = A.attend
 _orig_merge = A.merge_lse
+_orig_split = A.split_attention
 
 
 def _attend_no_scale(q, k, v, scale, q_pos=None, kv_pos=None):
@@ -58,6 +60,25 @@ def _split_ignores_seq_len(lo, hi, seq_len):
     return max(lo, 0), hi
 
 
+def _visible_strict(q_pos, kv_pos):
+    return np.asarray(kv_pos)[None, :] < np.asarray(q_pos)[:, None]  # t < p instead of t <= p
+
+
+def _split_ignores_positions(q, k, v, seq_lens, split_bounds, causal_offset, scale, q_positions=None,
+                             k_positions=None):
+    return _orig_split(q, k, v, seq_lens, split_bounds, causal_offset, scale)  # storage index as position
+
+
+def _split_swaps_positions(q, k, v, seq_lens, split_bounds, causal_offset, scale, q_positions=None,
+                           k_positions=None):
+    # each KV token's position taken from the wrong rank: the query chunk's layout repeated
+    if q_positions is not None:
+        S = np.asarray(k_positions).shape[1]
+        reps = -(-S // np.asarray(q_positions).shape[1])
+        k_positions = np.tile(np.asarray(q_positions), (1, reps))[:, :S]
+    return _orig_split(q, k, v, seq_lens, split_bounds, causal_offset, scale, q_positions, k_positions)
+
+
 MUTANTS = [
     ("attend without softmax scale", [(A, "attend", _attend_no_scale), (oracle, "attend", _attend_no_scale)],
      [P.test_golden_closed_forms]),
@@ -77,6 +98,12 @@ MUTANTS = [
      [P.test_e4m3_all_codes_match_torch]),
     ("split not clipped to seq_len", [(A, "_visible_range", _split_ignores_seq_len)],
      [P.test_split_past_seq_len_is_empty_and_poison_is_never_read]),
+    ("positional mask strict", [(A, "visible_mask", _visible_strict)],
+     [L.test_every_zigzag_rank_processes_132_kv_positions, L.test_layout_attention_brute_force_tiny]),
+    ("positions ignored", [(A, "split_attention", _split_ignores_positions)],
+     [L.test_layout_attention_equals_original_order_attention]),
+    ("KV positions from the wrong rank", [(A, "split_attention", _split_swaps_positions)],
+     [L.test_layout_attention_equals_original_order_attention]),
 ]
 
 
@@ -85,7 +112,10 @@ def _run_pin(fn):
     import json
     import os
 
-    if fn is P.test_golden_closed_forms:
+    if fn is L.test_layout_attention_equals_original_order_attention:
+        fn("zigzag", 32, 4)
+        fn("striped", 24, 3)
+    elif fn is P.test_golden_closed_forms:
         cases = json.load(open(os.path.join(P.GOLDEN, "closed_form_attention.json")))["cases"]
         for c in cases:
             fn(c)
