@@ -65,7 +65,8 @@ def config_of(w, ws=1):
                   ("no flush: each step streams the resident KV cache (%.2f GB allocated), far above the 129 MB L2"
                    % (alloc / 1e9)) if alloc > 4 * 129e6 else
                   ("KV (%.4f GB) fits in L2: a parity-size workload, not a bench line" % (alloc / 1e9)),
-            "parallelism": f"replicas x{ws}"}
+            "parallelism": f"replicas x{ws}",
+            **({"layout": w.layout, "query_rank": w.cp_rank} if w.layout != "contiguous" else {})}
 
 
 def workload_by_name(name):
@@ -229,6 +230,10 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
     gen = torch.Generator().manual_seed(w.seed)
     G = w.Hq // w.Hkv
     bounds = w.split_bounds()[0]
+    pos = {}
+    if w.layout != "contiguous":  # tokens stored in a zigzag / striped layout
+        pos = {"q_positions": [W.layout_positions(w.layout, w.S, w.n_split, w.cp_rank)],
+               "k_positions": [[p for r in range(w.n_split) for p in W.layout_positions(w.layout, w.S, w.n_split, r)]]}
     done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
     while elapsed < budget_s and (max_groups is None or groups < max_groups):
         S = w.S
@@ -246,7 +251,8 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
         else:
             kf = oracle.bf16_bits_to_f64(k.view(torch.int16).numpy())
             vf = oracle.bf16_bits_to_f64(v.view(torch.int16).numpy())
-        o, lse = oracle.split_attention(qf, kf[None, None], vf[None, None], [S], [bounds], w.causal_offset, w.scale)
+        o, lse = oracle.split_attention(qf, kf[None, None], vf[None, None], [S], [bounds], w.causal_offset, w.scale,
+                                        **pos)
         oracle.merge_lse(o, lse)
         elapsed += time.perf_counter() - t0
         done_bytes += RL.kv_bytes(1, w.dk, w.dv, w.kv_dtype, [S], [bounds], mla=w.mla, scale_block=w.scale_block)
@@ -294,13 +300,22 @@ def ours_arm(args, w, ws, rank, local):
     bounds = inp["split_bounds"]
     kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, inp["seq_lens_host"], bounds, mla=w.mla,
                            scale_block=w.scale_block)
-    flops = RL.attn_flops(w.Tq, w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, w.causal_offset)
+    positional = inp["q_pos"] is not None  # zigzag / striped storage: the *_pos entry point
+    if positional:
+        flops = RL.attn_flops_positions(w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, inp["q_pos_host"],
+                                        inp["k_pos_host"])
+    else:
+        flops = RL.attn_flops(w.Tq, w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, w.causal_offset)
     out = torch.empty((w.B, w.Tq, w.Hq, w.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Tq, w.Hq), dtype=torch.float32, device=dev)
 
     def step():
-        skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, out=out,
-                            lse=lse, **kw)
+        if positional:
+            skv.gqa_decode_attn_pos(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, inp["q_pos"], inp["k_pos"],
+                                    out=out, lse=lse, **kw)
+        else:
+            skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, out=out,
+                                lse=lse, **kw)
 
     for _ in range(args.warmup):
         step()
@@ -342,7 +357,7 @@ def ours_arm(args, w, ws, rank, local):
         host = {}
         # the MLA value cache is a view of the latent (k): it is copied once, as k
         keys = ("q", "k", "k_scale", "v_scale", "seq_lens") if w.mla else ("q", "k", "v", "k_scale", "v_scale",
-                                                                            "seq_lens")
+                                                                            "seq_lens", "q_pos", "k_pos")
         for key in keys:
             t = inp[key]
             host[key] = None if t is None else t.cpu().pin_memory()
@@ -360,9 +375,14 @@ def ours_arm(args, w, ws, rank, local):
             for k2, t in host.items():
                 if t is not None:
                     dev_bufs[k2].copy_(t, non_blocking=True)
-            skv.gqa_decode_attn(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
-                                w.causal_offset, k_scale=dev_bufs["k_scale"], v_scale=dev_bufs["v_scale"],
-                                softmax_scale=w.scale, scale_block=w.scale_block, out=out, lse=lse)
+            e2e_kw = dict(k_scale=dev_bufs["k_scale"], v_scale=dev_bufs["v_scale"], softmax_scale=w.scale,
+                          scale_block=w.scale_block, out=out, lse=lse)
+            if positional:
+                skv.gqa_decode_attn_pos(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
+                                        dev_bufs["q_pos"], dev_bufs["k_pos"], **e2e_kw)
+            else:
+                skv.gqa_decode_attn(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
+                                    w.causal_offset, **e2e_kw)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 

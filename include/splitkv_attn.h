@@ -183,6 +183,38 @@ skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* q, const vo
                                    const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
                                    float* lse, void* stream);
 
+/*
+ * attn_partial_pos / gqa_decode_attn_pos -- attn_partial and gqa_decode_attn for tokens
+ * stored out of sequence order.  The causal rule is taken from original positions instead
+ * of causal_offset: token t of sequence b is visible to query row i iff
+ * k_pos[b * S_max + t] <= q_pos[b * Tq + i] (besides lying in its split and below
+ * seq_len[b]).  This is the mask by original position of the zigzag and striped layouts
+ * ("现代大模型推理并行策略总览", section "序列布局：Contiguous、Zigzag 与 Striped"; rank r of
+ * a zigzag layout holds chunks r and 2N-1-r, "Context Parallelism for Scalable Million-Token
+ * Inference", section "Load-balanced sharding makes causal work and memory land evenly"):
+ * a ring-prefill step whose query chunk and KV shards come from such a layout passes their
+ * positions here.
+ *
+ *   q_pos  DEVICE int32 [B][Tq], contiguous, 4-byte aligned.
+ *   k_pos  DEVICE int32 [B][S_max], contiguous, 16-byte aligned, S_max a multiple of 4.
+ * Every other argument, the workspace (sizes from attn_partial_workspace_size and
+ * gqa_decode_attn_workspace_size), the outputs and the ownership rules are those of
+ * attn_partial / gqa_decode_attn.  Fully masked tiles are still streamed (no tile
+ * skipping by position).  Errors: SKV_EINVAL for NULL or misaligned positions or S_max
+ * not a multiple of 4; SKV_EUNSUPPORTED for the MLA latent shape.
+ */
+skv_status attn_partial_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                            const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
+                            const int32_t* k_pos, float* out_partial, float* lse_partial, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                               const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
+                               const int32_t* k_pos, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

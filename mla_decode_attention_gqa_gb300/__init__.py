@@ -39,6 +39,8 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attn_workspace_size",
     "gqa_decode_attn",
     "gqa_decode_attn_noalloc",
+    "attn_partial_pos",
+    "gqa_decode_attn_pos",
 )
 
 # Every symbol declared in include/splitkv_attn_selftest.h (hardware self-tests).
@@ -95,6 +97,11 @@ def _load():
     lib.gqa_decode_attn.restype = I32
     lib.attn_merge_lse.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P]
     lib.attn_merge_lse.restype = I32
+    common_pos = [D, P, P, P, P, P, P, I32P, I32, P, P]  # q_pos, k_pos replace causal_offset
+    lib.attn_partial_pos.argtypes = common_pos + [P, P, P, SZ, P]
+    lib.attn_partial_pos.restype = I32
+    lib.gqa_decode_attn_pos.argtypes = common_pos + [P, P, P, SZ, P]
+    lib.gqa_decode_attn_pos.restype = I32
     return lib
 
 
@@ -305,10 +312,59 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=N
     return out, lse
 
 
+def _positions(q_pos, k_pos, d):
+    _require_cuda(q_pos, k_pos)
+    for t, shape, name in ((q_pos, (d.B, d.Tq), "q_pos"), (k_pos, (d.B, d.S_max), "k_pos")):
+        if t.dtype != torch.int32 or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be contiguous int32 of shape {shape}")
+
+
+def attn_partial_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, k_scale=None, v_scale=None,
+                     softmax_scale=None, scale_block=64, out_partial=None, lse_partial=None):
+    """attn_partial with the causal rule taken from original positions: token t is visible to
+    row i iff k_pos[b, t] <= q_pos[b, i] (q_pos int32 [B,Tq], k_pos int32 [B,S], on the GPU)."""
+    d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
+                               scale_block)
+    _positions(q_pos, k_pos, d)
+    dev = q.device
+    if out_partial is None:
+        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    ws = _workspace(nbytes, dev)
+    _check(_lib.attn_partial_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(seq_lens), bounds, n_split, _ptr(q_pos), _ptr(k_pos),
+                                 _ptr(out_partial), _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
+    return out_partial, lse_partial
+
+
+def gqa_decode_attn_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, k_scale=None, v_scale=None,
+                        softmax_scale=None, scale_block=64, out=None, lse=None, workspace=None):
+    """gqa_decode_attn with the causal rule taken from original positions (see attn_partial_pos)."""
+    d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
+                               scale_block)
+    _positions(q_pos, k_pos, d)
+    dev = q.device
+    if out is None:
+        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
+    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    _check(_lib.gqa_decode_attn_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(seq_lens), bounds, n_split, _ptr(q_pos), _ptr(k_pos),
+                                    _ptr(out), _ptr(lse), _ptr(ws), nbytes if workspace is None else workspace.numel(),
+                                    _stream()))
+    return out, lse
+
+
 __all__ = [
     "attn_partial",
+    "attn_partial_pos",
     "attn_merge_lse",
     "gqa_decode_attn",
+    "gqa_decode_attn_pos",
     "make_desc",
     "device_error",
     "last_error",

@@ -302,7 +302,8 @@ skv_status encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, ui
 // Fill the launch parameters common to every GQA partial launch.
 skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, const void* q, const float* ks,
                        const float* vs, const int32_t* seq_lens, const int32_t* bounds, int32_t n_split,
-                       int64_t causal_offset, float* out_o, float* out_lse, bool zero_empty) {
+                       int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos, float* out_o,
+                       float* out_lse, bool zero_empty) {
   std::memset(p, 0, sizeof(*p));
   cudaError_t e;
   p->err = device_error_word(&e);
@@ -318,7 +319,10 @@ skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, cons
   p->seq_lens = seq_lens;
   p->out_o = out_o;
   p->out_lse = out_lse;
-  p->causal_offset = causal_offset;
+  // positions replace the offset rule: no contiguous horizon to cut tiles at
+  p->causal_offset = q_pos ? SKV_NO_CAUSAL : causal_offset;
+  p->q_pos = q_pos;
+  p->k_pos = k_pos;
   p->scale_log2 = d->softmax_scale * 1.4426950408889634f;
   p->B = d->B;
   p->Tq = d->Tq;
@@ -365,7 +369,8 @@ skv_status encode_q_map(CUtensorMap* map, const void* q, const skv_desc* d) {
 // Tensor-core path: fused = one pass over every split (final bf16 out + lse), else one
 // fp32 partial per split straight into out_o / out_lse.
 skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v, const int32_t* seq_lens,
-                  const int32_t* bounds, int32_t n_split, int64_t causal_offset, bool fused, float* out_o,
+                  const int32_t* bounds, int32_t n_split, int64_t causal_offset, const int32_t* q_pos,
+                  const int32_t* k_pos, bool fused, float* out_o,
                   float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream) {
   static thread_local PartialParams p;
   Plan pl;
@@ -373,8 +378,8 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   pl.chunk_tiles = 1;
   const int rows = tc_attn_rows_per_cta();
   pl.m_tiles = static_cast<int>((static_cast<int64_t>(d->Tq) * (d->Hq / d->Hkv) + rows - 1) / rows);
-  skv_status st = fill_params(&p, d, pl, q, nullptr, nullptr, seq_lens, bounds, n_split, causal_offset, out_o,
-                              out_lse, true);
+  skv_status st = fill_params(&p, d, pl, q, nullptr, nullptr, seq_lens, bounds, n_split, causal_offset, q_pos,
+                              k_pos, out_o, out_lse, true);
   if (st != SKV_OK) return st;
   TcAttnExtra x;
   x.fused = fused ? 1 : 0;
@@ -392,15 +397,16 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
 
 skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const void* k, const void* v,
                        const float* ks, const float* vs, const int32_t* seq_lens, const int32_t* bounds,
-                       int32_t n_split, int64_t causal_offset, float* out_o, float* out_lse, bool zero_empty,
-                       cudaStream_t stream) {
+                       int32_t n_split, int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos,
+                       float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream) {
   static thread_local PartialParams p;  // ~8 KB: keep it off the stack
-  skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, out_o, out_lse,
-                              zero_empty);
+  skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, q_pos, k_pos, out_o,
+                              out_lse, zero_empty);
   if (st != SKV_OK) return st;
   CUtensorMap tmk, tmv;
   cudaError_t e;
   if (pl.mla) {
+    if (q_pos) return fail(SKV_EUNSUPPORTED, "position-masked attention is not supported for the MLA latent shape");
     if (use_mla_tc(d)) {
       // one latent map (64-dim x 64-token boxes) serves K and V; each CTA of the pair
       // loads its own slice of dims
@@ -493,10 +499,24 @@ skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* spli
   return SKV_OK;
 }
 
-skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
-                        const float* k_scale, const float* v_scale, const int32_t* seq_lens,
-                        const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
-                        float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Positions of a *_pos call: both arrays present, aligned for the kernels' vector loads.
+skv_status validate_positions(const skv_desc* d, const int32_t* q_pos, const int32_t* k_pos) {
+  if (!q_pos || !k_pos) return fail(SKV_EINVAL, "q_pos and k_pos must be non-NULL");
+  if (!aligned(q_pos, 4) || !aligned(k_pos, 16)) return fail(SKV_EINVAL, "q_pos must be 4-byte, k_pos 16-byte aligned");
+  if (d->S_max % 4) return fail(SKV_EINVAL, "S_max must be a multiple of 4 with k_pos");
+  if (is_mla_shape(d)) return fail(SKV_EUNSUPPORTED, "position-masked attention is not supported for the MLA latent shape");
+  return SKV_OK;
+}
+
+skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                             const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
+                             const int32_t* q_pos, const int32_t* k_pos, float* out_partial, float* lse_partial,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
@@ -504,13 +524,13 @@ skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache
   if (!aligned(out_partial, 16) || !aligned(lse_partial, 4)) return fail(SKV_EINVAL, "outputs misaligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc(desc)) {
-    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, false, out_partial,
-                  lse_partial, nullptr, nullptr, s);
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, false,
+                  out_partial, lse_partial, nullptr, nullptr, s);
   }
   const Plan pl = make_plan(desc, split_bounds, n_split);
   if (pl.n_chunk == 1) {
     return run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
-                       causal_offset, out_partial, lse_partial, true, s);
+                       causal_offset, q_pos, k_pos, out_partial, lse_partial, true, s);
   }
   const size_t need = ws_bytes_for(desc, pl.n_part);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
@@ -520,12 +540,69 @@ skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
   st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   ws_o, ws_l, false, s);
+                   q_pos, k_pos, ws_o, ws_l, false, s);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge(ws_o, ws_l, pl.n_chunk, n_split, static_cast<int64_t>(rows), desc->dv, out_partial,
                                false, lse_partial, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk merge launch");
   return SKV_OK;
+}
+
+skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                                const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
+                                const int32_t* q_pos, const int32_t* k_pos, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
+  if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
+  if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_tc(desc)) {
+    if (!aligned(out, 16)) return fail(SKV_EINVAL, "out must be 16-byte aligned for this shape");
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, true,
+                  nullptr, nullptr, out, lse, s);
+  }
+  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const size_t need = ws_bytes_for(desc, pl.n_part);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_workspace_size()");
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
+  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
+                   q_pos, k_pos, ws_o, ws_l, false, s);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                        const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
+                        float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                           causal_offset, nullptr, nullptr, out_partial, lse_partial, workspace, workspace_bytes,
+                           stream);
+}
+
+skv_status attn_partial_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                            const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
+                            const int32_t* k_pos, float* out_partial, float* lse_partial, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
+  return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
+                           k_pos, out_partial, lse_partial, workspace, workspace_bytes, stream);
 }
 
 skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, int32_t dv, const float* out_partials,
@@ -560,31 +637,20 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
                            const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
                            float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                              causal_offset, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                               const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
+                               const int32_t* k_pos, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream) {
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
-  if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
-  if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
-  if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (use_tc(desc)) {
-    if (!aligned(out, 16)) return fail(SKV_EINVAL, "out must be 16-byte aligned for this shape");
-    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, true, nullptr, nullptr,
-                  out, lse, s);
-  }
-  const Plan pl = make_plan(desc, split_bounds, n_split);
-  const size_t need = ws_bytes_for(desc, pl.n_part);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
-    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_workspace_size()");
-  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
-  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   ws_o, ws_l, false, s);
-  if (st != SKV_OK) return st;
-  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return SKV_OK;
+  if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
+  return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
+                              k_pos, out, lse, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
@@ -656,7 +722,7 @@ extern "C" skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* 
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
   st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   ws_o, ws_l, false, s);
+                   nullptr, nullptr, ws_o, ws_l, false, s);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

@@ -26,6 +26,7 @@
 //     when S_k(i) has landed, PV_k(i-1) is complete: O_k may be rescaled and P_k rewritten;
 //   * O is rescaled (TMEM load / scale / store) only when a row's running max rises by
 //     more than 2^8; otherwise p = 2^(s - m_used) <= 256 stays exact enough in bf16.
+#include <climits>
 #include <cuda_runtime.h>
 
 #include "skv_common.cuh"
@@ -75,6 +76,8 @@ __device__ __forceinline__ void tma_load_4d_nohint(void* dst, const CUtensorMap*
 }
 
 
+// POS: the causal rule comes from position arrays (tokens stored out of sequence order)
+template <bool POS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attn_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
                    const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -241,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = g * G + (valid ? m % G : 0);
     const int64_t hz = p.causal_offset + t_q;
     const int64_t hz_min = p.causal_offset + (m0 + k * kRowsTile + lgrp * 32) / G;  // smallest in this warp
+    // tokens stored out of sequence order: column t is visible iff k_pos[t] <= q_pos[row]
+    const int32_t* kpos_b = POS ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
+    const int qp = (POS && valid) ? __ldg(p.q_pos + b * p.Tq + t_q) : 0;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
@@ -251,12 +257,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
-      const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+      const bool need_mask = POS || !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
       // visible columns of this row: [c_lo, c_lo + span)
       const int c_lo = min(max(r_lo - t0, 0), kTN);
       const int c_hi = static_cast<int>(
           min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTN));
       const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
+      // position mode: bit c of vis[c / 32] = column c visible (in range and k_pos <= q_pos);
+      // the tile's positions are the same for every lane (L1 broadcast)
+      uint32_t vis[kTN / 32];
+      if constexpr (POS) {
+#pragma unroll
+        for (int w4 = 0; w4 < kTN / 32; ++w4) {
+          uint32_t bits = 0u;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const int col = 32 * w4 + 4 * q4;
+            // S_max and t0 are multiples of 4: the four positions exist together or not at all
+            const int4 kp = (t0 + col < p.S_max) ? __ldg(reinterpret_cast<const int4*>(kpos_b + t0 + col))
+                                                 : make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
+            bits |= static_cast<uint32_t>(kp.x <= qp && static_cast<unsigned>(col - c_lo) < span) << (4 * q4);
+            bits |= static_cast<uint32_t>(kp.y <= qp && static_cast<unsigned>(col + 1 - c_lo) < span) << (4 * q4 + 1);
+            bits |= static_cast<uint32_t>(kp.z <= qp && static_cast<unsigned>(col + 2 - c_lo) < span) << (4 * q4 + 2);
+            bits |= static_cast<uint32_t>(kp.w <= qp && static_cast<unsigned>(col + 3 - c_lo) < span) << (4 * q4 + 3);
+          }
+          vis[w4] = bits;
+        }
+      }
+      auto visible = [&](int col) -> bool {
+        if constexpr (POS) return ((vis[col >> 5] >> (col & 31)) & 1u) != 0u;
+        return static_cast<unsigned>(col - c_lo) < span;
+      };
       const uint32_t s_col = t_lane + kColS + 128 * k;
       const float sl = p.scale_log2;
 
@@ -278,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
           float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
           if (need_mask) {
-            v0 = (static_cast<unsigned>(col - c_lo) < span) ? v0 : -INFINITY;
-            v1 = (static_cast<unsigned>(col + 1 - c_lo) < span) ? v1 : -INFINITY;
+            v0 = visible(col) ? v0 : -INFINITY;
+            v1 = visible(col + 1) ? v1 : -INFINITY;
           }
           mx[(2 * e) & 3] = fmaxf(mx[(2 * e) & 3], v0);
           mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], v1);
@@ -334,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
             float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
             if (need_mask) {
-              v0 = (static_cast<unsigned>(col - c_lo) < span) ? v0 : -INFINITY;
-              v1 = (static_cast<unsigned>(col + 1 - c_lo) < span) ? v1 : -INFINITY;
+              v0 = visible(col) ? v0 : -INFINITY;
+              v1 = visible(col + 1) ? v1 : -INFINITY;
             }
             const float p0 = fast_exp2(fmaf(v0, sl, -base));
             const float p1 = fast_exp2(fmaf(v1, sl, -base));
@@ -454,12 +485,17 @@ cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const C
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   if (n_items <= 0) return cudaSuccess;
-  tc_attn_kernel<<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  if (p.k_pos)
+    tc_attn_kernel<true><<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  else
+    tc_attn_kernel<false><<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
   return cudaGetLastError();
 }
 

@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int h0 = g * p.G + (v0 ? mrow0 % p.G : 0), h1 = g * p.G + (v1 ? mrow1 % p.G : 0);
   const int64_t hz0 = p.causal_offset + tq0, hz1 = p.causal_offset + tq1;
   const int64_t hz_min = p.causal_offset + (m0 + wm * 16) / p.G;
+  // tokens stored out of sequence order: visible iff k_pos[t] <= q_pos[row]
+  const int32_t* kpos_b = p.k_pos ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
+  const int qp0 = p.q_pos ? __ldg(p.q_pos + b * p.Tq + tq0) : 0;
+  const int qp1 = p.q_pos ? __ldg(p.q_pos + b * p.Tq + tq1) : 0;
 
   // ---- Q fragments (A operand, 16 rows x D): registers for bf16, shared memory for fp8
   uint32_t qa[C::FP8 ? 1 : D / 16][4];
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     // ---- scale, mask, online softmax
     const float sl = p.scale_log2 * ksc;
     const bool in_range = (t0s >= r_lo) && (t0s + NS <= r_hi);
-    const bool need_mask = !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
+    const bool need_mask = kpos_b != nullptr || !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NS / 8; ++nt) {
@@ -326,7 +330,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         if (need_mask) {
           const int tok = t0s + 8 * nt + 2 * tq + (e & 1);
           const int64_t hz = (e < 2) ? hz0 : hz1;
-          const bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
+          const bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz &&
+                          (kpos_b == nullptr || __ldg(kpos_b + tok) <= ((e < 2) ? qp0 : qp1));
           x = ok ? x : -INFINITY;
         }
         sc[nt][e] = x;

@@ -35,6 +35,8 @@ struct PartialParams {
   float* out_lse;
   unsigned int* err;  // device error word
   int64_t causal_offset;
+  const int32_t* q_pos;  // original positions [B][Tq] / [B][S_max] (NULL: rows at
+  const int32_t* k_pos;  // causal_offset + i, tokens at their index)
   float scale_log2;  // softmax_scale * log2(e)
   int32_t B, Tq, Hq, Hkv, G;
   int32_t S_max;  // tokens at or past S_max do not exist

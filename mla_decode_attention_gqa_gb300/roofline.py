@@ -70,3 +70,22 @@ def attn_flops(Tq, Hq, dk, dv, seq_lens, split_bounds, causal_offset=NO_CAUSAL):
                 # row i sees tokens t <= causal_offset + i
                 pairs += sum(_visible_per_row(lo, hi, L, causal_offset, i) for i in range(Tq))
     return 2 * (dk + dv) * Hq * pairs
+
+
+def attn_flops_positions(Hq, dk, dv, seq_lens, split_bounds, q_positions, k_positions):
+    """Algorithmic flops when the causal rule comes from original positions (zigzag /
+    striped storage): 2*(dk+dv) per (row, head, token) with k_pos[t] <= q_pos[row]."""
+    import numpy as np
+
+    n_split = len(split_bounds[0]) - 1
+    pairs = 0
+    for b, L in enumerate(seq_lens):
+        qp = np.asarray(q_positions[b], dtype=np.int64)
+        kp = np.asarray(k_positions[b], dtype=np.int64)
+        for j in range(n_split):
+            lo, hi = max(split_bounds[b][j], 0), min(split_bounds[b][j + 1], L)
+            if hi <= lo:
+                continue
+            ks = np.sort(kp[lo:hi])
+            pairs += int(np.searchsorted(ks, qp, side="right").sum())
+    return 2 * (dk + dv) * Hq * pairs

@@ -9,6 +9,11 @@ import oracle
 # Parity bars (written in the tests): max-abs error of the output and of the LSE.
 TOL_BF16 = {"out": 1e-2, "lse": 1e-3}
 TOL_FP8 = {"out": 4e-2, "lse": 4e-2}
+# The bars apply to the computed output.  An output stored in bf16 is further rounded to
+# nearest: at most half an ulp, 2^-8 * |o| (0.0156 at |o| = 4, where a row that sees one
+# token returns a raw V row), so bf16 outputs get that term on top of the bar; fp32
+# outputs (the partials) are held to the bare bar.
+BF16_STORE_REL = 2.0 ** -8
 
 
 def tol_for(w):
@@ -36,7 +41,10 @@ def oracle_group(inp, w, b, g, bounds=None, causal_offset=None):
     qb = q_f64(inp["q"][b : b + 1, :, g * G : (g + 1) * G])
     kb = kv_f64(inp, w, "k", b, g)[None, None]
     vb = kv_f64(inp, w, "v", b, g)[None, None]
-    o, lse = oracle.split_attention(qb, kb, vb, [inp["seq_lens_host"][b]], [bounds[b]], causal, w.scale)
+    pos = {}
+    if inp.get("q_pos_host") is not None:  # tokens stored out of sequence order
+        pos = {"q_positions": [inp["q_pos_host"][b]], "k_positions": [inp["k_pos_host"][b]]}
+    o, lse = oracle.split_attention(qb, kb, vb, [inp["seq_lens_host"][b]], [bounds[b]], causal, w.scale, **pos)
     return o[:, 0], lse[:, 0]
 
 
@@ -58,6 +66,7 @@ def oracle_all(inp, w, bounds=None, causal_offset=None):
 def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
     """Element-wise parity: |o - o_ref| <= tol['out'], |lse - lse_ref| <= tol['lse'];
     rows with lse_ref = -inf must have lse = -inf and o = 0."""
+    stored_bf16 = got_o.dtype == torch.bfloat16
     go = got_o.detach().float().cpu().numpy().astype(np.float64)
     gl = got_lse.detach().float().cpu().numpy().astype(np.float64)
     assert go.shape == ref_o.shape, (what, go.shape, ref_o.shape)
@@ -70,7 +79,13 @@ def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
     full = ~empty
     err_o = float(np.max(np.abs(go - ref_o))) if go.size else 0.0
     err_l = float(np.max(np.abs(gl[full] - ref_lse[full]))) if full.any() else 0.0
-    assert err_o <= tol["out"], f"{what}: out max-abs err {err_o:.3e} > {tol['out']}"
+    if stored_bf16:
+        # element-wise: |o - o_ref| <= bar + 2^-8 |o_ref|; report the excess over the bar
+        excess = float(np.max(np.abs(go - ref_o) - BF16_STORE_REL * np.abs(ref_o))) if go.size else 0.0
+        assert excess <= tol["out"], (f"{what}: out err beyond bf16 storage rounding {excess:.3e} > {tol['out']} "
+                                      f"(max-abs {err_o:.3e})")
+    else:
+        assert err_o <= tol["out"], f"{what}: out max-abs err {err_o:.3e} > {tol['out']}"
     assert err_l <= tol["lse"], f"{what}: lse max-abs err {err_l:.3e} > {tol['lse']}"
     return err_o, err_l
 
@@ -91,12 +106,17 @@ def oracle_rows(inp, w, b, g, t_rows, bounds=None, causal_offset=None):
     R = len(t_rows)
     o = np.zeros((n_split, R, G, w.dv))
     lse = np.full((n_split, R, G), -np.inf)
-    q_pos = np.repeat(causal + np.asarray(t_rows, dtype=np.int64), G)
+    if inp.get("q_pos_host") is not None:  # tokens stored out of sequence order
+        q_pos = np.repeat(np.asarray(inp["q_pos_host"][b], dtype=np.int64)[t_rows], G)
+        k_pos = np.asarray(inp["k_pos_host"][b], dtype=np.int64)
+    else:
+        q_pos = np.repeat(causal + np.asarray(t_rows, dtype=np.int64), G)
+        k_pos = np.arange(w.S)
     for j in range(n_split):
         lo, hi = max(bounds[b][j], 0), min(bounds[b][j + 1], seq, w.S)
         if hi <= lo:
             continue
-        oo, ll = oracle.attend(qb.reshape(R * G, w.dk), kf[lo:hi], vf[lo:hi], w.scale, q_pos, np.arange(lo, hi))
+        oo, ll = oracle.attend(qb.reshape(R * G, w.dk), kf[lo:hi], vf[lo:hi], w.scale, q_pos, k_pos[lo:hi])
         o[j] = oo.reshape(R, G, w.dv)
         lse[j] = ll.reshape(R, G)
     return o, lse
