@@ -49,7 +49,13 @@ constexpr int kStageBytes = 2 * kKTileBytes;     // K + V
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
 constexpr int kOffBar = kOffRing + kNStage * kStageBytes;
-constexpr int kSmem = 1024 + kOffBar + 256;
+// position mode: the item's tiles that some row can see, listed once per CTA
+constexpr int kMaxListTiles = 1024;  // items with more tiles keep every tile
+constexpr int kOffList = kOffBar + 256;                  // int32 tile index [kMaxListTiles]
+constexpr int kOffKmin = kOffList + 4 * kMaxListTiles;   // int32 min position of a tile's tokens
+constexpr int kOffKmax = kOffKmin + 4 * kMaxListTiles;   // int32 max position
+constexpr int kOffMisc = kOffKmax + 4 * kMaxListTiles;   // [0] the CTA's largest row position, [1] tiles kept
+constexpr int kSmem = 1024 + kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_k (and P_k over its first 64 columns) at kColS + 128 k
 constexpr uint32_t kColO = 256;  // O_k at kColO + 128 k
@@ -114,6 +120,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile_begin = r_lo / kTN;
   const int n_tiles = (r_hi > r_lo) ? ((r_hi + kTN - 1) / kTN - tile_begin) : 0;
 
+  // ---- position mode: list the tiles holding a token some row of this CTA can see.
+  // Every role walks the same list, so a tile that no row sees is never loaded, multiplied
+  // or masked; stages and barrier phases follow the position in the list.
+  int n_used = n_tiles;
+  bool listed = false;
+  const int* lidx = reinterpret_cast<const int*>(smem + kOffList);
+  const int* lkmin = reinterpret_cast<const int*>(smem + kOffKmin);
+  const int* lkmax = reinterpret_cast<const int*>(smem + kOffKmax);
+  if constexpr (POS) {
+    int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+    listed = n_tiles <= kMaxListTiles;
+    if (threadIdx.x == 0) misc[0] = INT_MIN;
+    __syncthreads();
+    int qm = INT_MIN;  // largest position of the CTA's query rows
+    for (int t = m0 / G + static_cast<int>(threadIdx.x); t <= m_last / G; t += kThreads)
+      qm = max(qm, __ldg(p.q_pos + b * p.Tq + t));
+    qm = __reduce_max_sync(0xffffffffu, qm);
+    if (lane == 0) atomicMax(&misc[0], qm);
+    if (listed) {
+      int* kmin_w = reinterpret_cast<int*>(smem + kOffKmin);
+      int* kmax_w = reinterpret_cast<int*>(smem + kOffKmax);
+      for (int i = warp; i < n_tiles; i += kThreads / 32) {
+        const int t = (tile_begin + i) * kTN + 4 * lane;
+        // S_max and t are multiples of 4: the four positions exist together or not at all
+        const int4 kp = (t < p.S_max) ? __ldg(reinterpret_cast<const int4*>(p.k_pos + static_cast<int64_t>(b) * p.S_max + t))
+                                      : make_int4(0, 0, 0, 0);
+        int mn = INT_MAX, mx = INT_MIN;
+        const int v4[4] = {kp.x, kp.y, kp.z, kp.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (t + u >= r_lo && t + u < r_hi) {  // only tokens of the item's range count
+            mn = min(mn, v4[u]);
+            mx = max(mx, v4[u]);
+          }
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+          kmin_w[i] = mn;
+          kmax_w[i] = mx;
+        }
+      }
+    }
+    __syncthreads();
+    if (listed && warp == 0) {
+      const int qmax_cta = misc[0];
+      int* lidx_w = reinterpret_cast<int*>(smem + kOffList);
+      int c = 0;
+      for (int base = 0; base < n_tiles; base += 32) {
+        const int i = base + lane;
+        const bool keep = i < n_tiles && lkmin[i] <= qmax_cta;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) lidx_w[c + __popc(bal & ((1u << lane) - 1u))] = i;
+        c += __popc(bal);
+      }
+      if (lane == 0) misc[1] = c;
+    }
+    __syncthreads();
+    if (listed) n_used = misc[1];
+  }
+  auto tile_of = [&](int c) -> int {
+    if constexpr (POS) return listed ? lidx[c] : c;
+    return c;
+  };
+
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kNStage; ++s) {
@@ -138,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_used > 0) {
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
@@ -150,12 +221,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              g * G, t_start, b);
       }
       int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+      for (int i = 0; i < n_used; ++i) {
         const int s = i % kNStage;
         if (i >= kNStage && !mbar_wait(&bars->kv_empty[s], ((i / kNStage) - 1) & 1, p.err, kDevErrEmptyWait)) break;
         mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
         uint8_t* st = smem + kOffRing + s * kStageBytes;
-        const int tok = (tile_begin + i) * kTN;
+        const int tok = (tile_begin + tile_of(i)) * kTN;
         for (int bx = 0; bx < 2; ++bx) {
           tma_load_4d_nohint(st + bx * kKVBoxBytes, &tmk, &bars->kv_full[s], bx * 64, tok, g, b);
           tma_load_4d_nohint(st + kKTileBytes + bx * kKVBoxBytes, &tmv, &bars->kv_full[s], bx * 64, tok, g, b);
@@ -169,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_used > 0) {
       const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
       const uint32_t idesc_pv = tc::idesc_f16(128, kD, true, false, true);
       const uint32_t q_base = smem_u32(smem + kOffQ);
@@ -207,13 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(smem_u32(&bars->s_full[0]));
         issue_s(1, 0);
         tc::mma_commit(smem_u32(&bars->s_full[1]));
-        for (int i = 0; i < n_tiles && ok; ++i) {
+        for (int i = 0; i < n_used && ok; ++i) {
           ok = mbar_wait(&bars->p_full[0], i & 1, p.err, kDevErrFullWait);
           if (!ok) break;
           tc::fence_after_sync();
           issue_pv(0, i);
           tc::mma_commit(smem_u32(&bars->pv_done[0]));
-          if (i + 1 < n_tiles) {
+          if (i + 1 < n_used) {
             ok = mbar_wait(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1, p.err, kDevErrFullWait);
             if (!ok) break;
             tc::fence_after_sync();
@@ -226,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(1, i);
           tc::mma_commit(smem_u32(&bars->pv_done[1]));
           tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
-          if (i + 1 < n_tiles) {
+          if (i + 1 < n_used) {
             issue_s(1, i + 1);
             tc::mma_commit(smem_u32(&bars->s_full[1]));
           }
@@ -247,17 +318,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tokens stored out of sequence order: column t is visible iff k_pos[t] <= q_pos[row]
     const int32_t* kpos_b = POS ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
     const int qp = (POS && valid) ? __ldg(p.q_pos + b * p.Tq + t_q) : 0;
+    // position range of this warp's rows: a listed tile entirely at or below it needs no
+    // mask, one entirely above it is invisible to the warp
+    int qmin_w = INT_MAX, qmax_w = INT_MIN;
+    if constexpr (POS) {
+      qmin_w = __reduce_min_sync(0xffffffffu, valid ? qp : INT_MAX);
+      qmax_w = __reduce_max_sync(0xffffffffu, valid ? qp : INT_MIN);
+    }
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
 
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int t0 = (tile_begin + i) * kTN;
+    for (int i = 0; i < n_used && ok; ++i) {
+      const int ti = tile_of(i);  // the tile; i is its place in the (listed) sequence
+      const int t0 = (tile_begin + ti) * kTN;
       ok = mbar_wait(&bars->s_full[k], i & 1, p.err, kDevErrFullWait);
       if (!ok) break;
       tc::fence_after_sync();
       const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
-      const bool need_mask = POS || !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+      bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+      bool none_visible = false;
+      if constexpr (POS) {
+        need_mask = !(listed && in_range && lkmax[ti] <= qmin_w);
+        none_visible = listed && lkmin[ti] > qmax_w;
+      }
       // visible columns of this row: [c_lo, c_lo + span)
       const int c_lo = min(max(r_lo - t0, 0), kTN);
       const int c_hi = static_cast<int>(
@@ -265,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
       // position mode: bit c of vis[c / 32] = column c visible (in range and k_pos <= q_pos);
       // the tile's positions are the same for every lane (L1 broadcast)
-      uint32_t vis[kTN / 32];
+      uint32_t vis[kTN / 32] = {0u, 0u, 0u, 0u};
       if constexpr (POS) {
+        if (need_mask && !none_visible) {
 #pragma unroll
         for (int w4 = 0; w4 < kTN / 32; ++w4) {
           uint32_t bits = 0u;
@@ -282,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bits |= static_cast<uint32_t>(kp.w <= qp && static_cast<unsigned>(col + 3 - c_lo) < span) << (4 * q4 + 3);
           }
           vis[w4] = bits;
+        }
         }
       }
       auto visible = [&](int col) -> bool {
@@ -410,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O / l and lse
-    if (n_tiles > 0 && ok) {
-      ok = mbar_wait(&bars->pv_done[k], (n_tiles - 1) & 1, p.err, kDevErrFullWait);
+    if (n_used > 0 && ok) {
+      ok = mbar_wait(&bars->pv_done[k], (n_used - 1) & 1, p.err, kDevErrFullWait);
       tc::fence_after_sync();
     }
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -423,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 2
       for (int c = 0; c < kD / 16; ++c) {
         uint32_t r[16];
-        if (n_tiles > 0) {
+        if (n_used > 0) {
           tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
           tc::tmem_wait_ld();
         } else {
@@ -452,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kD / 16; ++c) {
         uint32_t r[16];
-        if (n_tiles > 0) {
+        if (n_used > 0) {
           tc::tmem_ld16(t_lane + kColO + 128 * k + 16 * c, r);
           tc::tmem_wait_ld();
         } else {
