@@ -16,6 +16,11 @@ Input recipe (per workload, seed = 1000 + index):
     e4m3 0x7F) so that any read past the end of a sequence shows up in the output.
   * MLA workloads hold one latent buffer [B, 1, S, dk]; V is the view of its first
     ``dv`` columns (same storage, row stride dk).
+  * Paged workloads also scatter that same logical cache into pages
+    [num_blocks, Hkv, block_len, d]: logical block i of sequence b goes to physical block
+    perm[b * S / block_len + i] of a seeded permutation of all blocks (B spare blocks,
+    NaN-poisoned, are never referenced); the block table [B, S / block_len] records it.
+    fp8 scales move with their block: [num_blocks, Hkv, block_len / scale_block].
   * Zigzag / striped ring-prefill workloads store each of the n_split ranks' tokens in
     the rank's layout order (``layout_positions``); the KV cache is the ranks' shards
     one after another and the query chunk is rank ``cp_rank``'s tokens.  The original
@@ -55,6 +60,8 @@ class Workload:
     seed: int = 1000
     layout: str = "contiguous"  # "contiguous" | "zigzag" | "striped" (position-array workloads)
     cp_rank: int = 0            # the emulated rank whose query chunk is computed
+    paged: bool = False         # also store the cache as pages with a block table
+    block_len: int = 64         # tokens per page
 
     @property
     def scale(self) -> float:
@@ -159,6 +166,9 @@ def make_inputs(w: Workload, device="cpu", poison=True):
       split_bounds   list[list[int]]  ([B][n_split+1])
       q_pos, k_pos   int32 [B, Tq], [B, S] original positions (layout workloads), else None
       q_pos_host, k_pos_host  the same as lists, or None
+      paged workloads also: k_pages, v_pages [num_blocks, Hkv, block_len, d] (MLA: v_pages
+        a view of k_pages), k_scale_pages / v_scale_pages (fp8), block_table int32 [B, S /
+        block_len] and block_table_host
     """
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
@@ -208,6 +218,10 @@ def make_inputs(w: Workload, device="cpu", poison=True):
     else:
         raise ValueError(f"unknown kv dtype {w.kv_dtype}")
 
+    pages = {}
+    if w.paged:
+        pages = _make_pages(w, k, v, k_scale, v_scale, gen, dev)
+
     q_pos = k_pos = None
     q_pos_host = k_pos_host = None
     if w.layout != "contiguous":
@@ -233,4 +247,50 @@ def make_inputs(w: Workload, device="cpu", poison=True):
         "k_pos": k_pos,
         "q_pos_host": q_pos_host,
         "k_pos_host": k_pos_host,
+        **pages,
     }
+
+
+def _make_pages(w, k, v, k_scale, v_scale, gen, dev):
+    """Scatter the logical cache into pages (see the module docstring)."""
+    L = w.block_len
+    if w.S % L:
+        raise ValueError("S must be a multiple of block_len")
+    nb = w.S // L
+    n_blocks = w.B * nb + w.B  # B spare blocks nobody references
+    perm = torch.randperm(n_blocks, generator=gen, device=dev)
+    phys = perm[: w.B * nb]
+
+    def scatter(x):  # [B, H, S, d] -> [n_blocks, H, L, d]
+        B, H, S, d = x.shape
+        blocks = x.reshape(B, H, nb, L, d).permute(0, 2, 1, 3, 4).reshape(B * nb, H, L, d)
+        out = torch.empty((n_blocks, H, L, d), dtype=x.dtype, device=dev)
+        if x.dtype == torch.uint8:
+            out.fill_(0x7F)  # e4m3 NaN
+        else:
+            out.fill_(float("nan"))
+        out[phys] = blocks
+        return out
+
+    res = {"block_table": phys.reshape(w.B, nb).to(torch.int32).contiguous(),
+           "block_table_host": phys.reshape(w.B, nb).cpu().tolist()}
+    if w.mla:
+        lat = scatter(k)
+        res["k_pages"] = lat
+        res["v_pages"] = lat[..., : w.dv]
+    else:
+        res["k_pages"] = scatter(k)
+        res["v_pages"] = scatter(v)
+    if k_scale is not None:
+        per = L // w.scale_block
+
+        def scatter_s(sc):  # [B, H, S / sb] -> [n_blocks, H, L / sb]
+            B, H, _ = sc.shape
+            blocks = sc.reshape(B, H, nb, per).permute(0, 2, 1, 3).reshape(B * nb, H, per)
+            out = torch.ones((n_blocks, H, per), dtype=sc.dtype, device=dev)
+            out[phys] = blocks
+            return out
+
+        res["k_scale_pages"] = scatter_s(k_scale)
+        res["v_scale_pages"] = scatter_s(v_scale)
+    return res

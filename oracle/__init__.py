@@ -22,6 +22,7 @@ from .attention import (
     merge_lse,
     full_attention,
 )
+from .paged import gather_pages, gather_block_scales
 
 __all__ = [
     "bf16_bits_to_f64",
@@ -32,4 +33,6 @@ __all__ = [
     "split_attention",
     "merge_lse",
     "full_attention",
+    "gather_pages",
+    "gather_block_scales",
 ]

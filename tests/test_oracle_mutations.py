@@ -13,6 +13,8 @@ from oracle import attention as A
 from oracle import formats as F
 import tests.test_oracle_pins as P
 import tests.test_oracle_layouts as L
+import tests.test_oracle_paged as PG
+from oracle import paged as PGO
 
 _orig_attend = A.attend
 _orig_merge = A.merge_lse
@@ -60,6 +62,29 @@ def _split_ignores_seq_len(lo, hi, seq_len):
     return max(lo, 0), hi
 
 
+_orig_gather = PGO.gather_pages
+
+
+def _gather_row_and_block_swapped(pages, block_table, n_tokens):
+    # token t taken from block table[b][t % L], row t // L (the two indices swapped)
+    pages = np.asarray(pages)
+    nb, Hkv, Lb, d = pages.shape
+    table = np.asarray(block_table, dtype=np.int64)
+    out = np.empty((table.shape[0], Hkv, n_tokens, d), dtype=pages.dtype)
+    for b in range(table.shape[0]):
+        for t in range(n_tokens):
+            out[b, :, t] = pages[table[b, t % Lb] if t % Lb < table.shape[1] else 0, :, min(t // Lb, Lb - 1)]
+    return out
+
+
+def _gather_physical_order(pages, block_table, n_tokens):
+    # block table ignored: physical blocks read in storage order
+    pages = np.asarray(pages)
+    table = np.asarray(block_table, dtype=np.int64)
+    ident = np.arange(table.size).reshape(table.shape) % pages.shape[0]
+    return _orig_gather(pages, ident, n_tokens)
+
+
 def _visible_strict(q_pos, kv_pos):
     return np.asarray(kv_pos)[None, :] < np.asarray(q_pos)[:, None]  # t < p instead of t <= p
 
@@ -104,6 +129,12 @@ MUTANTS = [
      [L.test_layout_attention_equals_original_order_attention]),
     ("KV positions from the wrong rank", [(A, "split_attention", _split_swaps_positions)],
      [L.test_layout_attention_equals_original_order_attention]),
+    ("paged gather: row and block index swapped", [(PGO, "gather_pages", _gather_row_and_block_swapped),
+                                                   (oracle, "gather_pages", _gather_row_and_block_swapped)],
+     [PG.test_hand_worked_gather, PG.test_gather_inverts_the_generators_scatter_bf16]),
+    ("paged gather ignores the block table", [(PGO, "gather_pages", _gather_physical_order),
+                                              (oracle, "gather_pages", _gather_physical_order)],
+     [PG.test_hand_worked_gather, PG.test_gather_inverts_the_generators_scatter_bf16]),
 ]
 
 
