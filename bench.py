@@ -66,7 +66,8 @@ def config_of(w, ws=1):
                    % (alloc / 1e9)) if alloc > 4 * 129e6 else
                   ("KV (%.4f GB) fits in L2: a parity-size workload, not a bench line" % (alloc / 1e9)),
             "parallelism": f"replicas x{ws}",
-            **({"layout": w.layout, "query_rank": w.cp_rank} if w.layout != "contiguous" else {})}
+            **({"layout": w.layout, "query_rank": w.cp_rank} if w.layout != "contiguous" else {}),
+            **({"paged": True, "block_len": w.block_len} if w.paged else {})}
 
 
 def workload_by_name(name):
@@ -309,8 +310,18 @@ def ours_arm(args, w, ws, rank, local):
     out = torch.empty((w.B, w.Tq, w.Hq, w.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Tq, w.Hq), dtype=torch.float32, device=dev)
 
+    if w.paged:  # the pages are the cache; the logical copy is not needed here
+        for key in ("k", "v", "k_scale", "v_scale"):
+            inp[key] = None
+        torch.cuda.empty_cache()
+        kw = dict(k_scale=inp.get("k_scale_pages"), v_scale=inp.get("v_scale_pages"), softmax_scale=w.scale,
+                  scale_block=w.scale_block)
+
     def step():
-        if positional:
+        if w.paged:
+            skv.gqa_decode_attn_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["seq_lens"], bounds,
+                                      inp["block_table"], w.causal_offset, out=out, lse=lse, **kw)
+        elif positional:
             skv.gqa_decode_attn_pos(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, inp["q_pos"], inp["k_pos"],
                                     out=out, lse=lse, **kw)
         else:
@@ -356,17 +367,25 @@ def ours_arm(args, w, ws, rank, local):
     if not args.no_e2e:
         host = {}
         # the MLA value cache is a view of the latent (k): it is copied once, as k
-        keys = ("q", "k", "k_scale", "v_scale", "seq_lens") if w.mla else ("q", "k", "v", "k_scale", "v_scale",
-                                                                            "seq_lens", "q_pos", "k_pos")
+        if w.paged:
+            keys = ("q", "k_pages", "seq_lens", "block_table") + (() if w.mla else ("v_pages",)) + (
+                ("k_scale_pages", "v_scale_pages") if w.kv_dtype != "bf16" else ())
+        elif w.mla:
+            keys = ("q", "k", "k_scale", "v_scale", "seq_lens")
+        else:
+            keys = ("q", "k", "v", "k_scale", "v_scale", "seq_lens", "q_pos", "k_pos")
         for key in keys:
-            t = inp[key]
+            t = inp.get(key)
             host[key] = None if t is None else t.cpu().pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
         dev_bufs = {k2: (None if t is None else torch.empty_like(t, device=dev)) for k2, t in host.items()}
-        if w.mla:
+        if w.mla and w.paged:
+            dev_bufs["v_pages"] = dev_bufs["k_pages"][..., : w.dv]
+            dev_bufs["v_scale_pages"] = None
+        elif w.mla:
             dev_bufs["v"] = dev_bufs["k"][..., : w.dv]
         del inp
         torch.cuda.empty_cache()
@@ -375,9 +394,13 @@ def ours_arm(args, w, ws, rank, local):
             for k2, t in host.items():
                 if t is not None:
                     dev_bufs[k2].copy_(t, non_blocking=True)
-            e2e_kw = dict(k_scale=dev_bufs["k_scale"], v_scale=dev_bufs["v_scale"], softmax_scale=w.scale,
+            e2e_kw = dict(k_scale=dev_bufs.get("k_scale"), v_scale=dev_bufs.get("v_scale"), softmax_scale=w.scale,
                           scale_block=w.scale_block, out=out, lse=lse)
-            if positional:
+            if w.paged:
+                e2e_kw.update(k_scale=dev_bufs.get("k_scale_pages"), v_scale=dev_bufs.get("v_scale_pages"))
+                skv.gqa_decode_attn_paged(dev_bufs["q"], dev_bufs["k_pages"], dev_bufs["v_pages"], dev_bufs["seq_lens"],
+                                          bounds, dev_bufs["block_table"], w.causal_offset, **e2e_kw)
+            elif positional:
                 skv.gqa_decode_attn_pos(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
                                         dev_bufs["q_pos"], dev_bufs["k_pos"], **e2e_kw)
             else:

@@ -215,6 +215,45 @@ skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* 
                                const int32_t* k_pos, void* out, float* lse, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/*
+ * Paged block KV cache.  The attention-DP page ("KV Cache" section) keeps each rank's
+ * cache as [num_blocks, num_kv_heads, block_len, d_head]; a per-sequence block table maps
+ * logical block i of sequence b (its tokens [i * block_len, (i + 1) * block_len)) to the
+ * physical page that holds it, so token t of sequence b, KV head g is row t % block_len
+ * of page block_table[b * max_blocks + t / block_len], head g.  Pages may be shared.
+ */
+typedef struct {
+  int32_t block_len;           /* tokens per page: a positive multiple of 64 */
+  int32_t max_blocks;          /* block-table entries per sequence */
+  int64_t num_blocks;          /* pages in the caches (entries >= num_blocks read zeros) */
+  const int32_t* block_table;  /* DEVICE int32 [B][max_blocks], 4-byte aligned */
+} skv_paged;
+
+/*
+ * attn_partial_paged / gqa_decode_attn_paged -- attn_partial and gqa_decode_attn over a
+ * paged cache.  k_cache / v_cache are the pages [num_blocks][Hkv][block_len][d] with
+ * desc->k_strides / v_strides = (page, head, token) strides in elements (the MLA value
+ * cache is a view of the latent pages, as for the contiguous call); desc->S_max is the
+ * logical capacity of a sequence, at most max_blocks * block_len; fp8 block scales are
+ * per page: [num_blocks][Hkv][block_len / scale_block] (block_len a multiple of
+ * scale_block).  Split bounds, seq_lens and causal_offset are in logical tokens.  The
+ * workspace sizes are those of attn_partial_workspace_size / gqa_decode_attn_workspace_size
+ * for the same desc; outputs, ownership and errors as for the contiguous calls, plus
+ * SKV_EINVAL for a NULL or misaligned block table, block_len not a positive multiple of
+ * 64, or S_max above max_blocks * block_len.
+ */
+skv_status attn_partial_paged(const skv_desc* desc, const skv_paged* paged, const void* q, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
+                              int64_t causal_offset, float* out_partial, float* lse_partial, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
+                                 int64_t causal_offset, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

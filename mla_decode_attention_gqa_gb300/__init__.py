@@ -41,6 +41,8 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attn_noalloc",
     "attn_partial_pos",
     "gqa_decode_attn_pos",
+    "attn_partial_paged",
+    "gqa_decode_attn_paged",
 )
 
 # Every symbol declared in include/splitkv_attn_selftest.h (hardware self-tests).
@@ -102,6 +104,11 @@ def _load():
     lib.attn_partial_pos.restype = I32
     lib.gqa_decode_attn_pos.argtypes = common_pos + [P, P, P, SZ, P]
     lib.gqa_decode_attn_pos.restype = I32
+    common_paged = [D, ctypes.POINTER(SkvPaged), P, P, P, P, P, P, I32P, I32, I64]
+    lib.attn_partial_paged.argtypes = common_paged + [P, P, P, SZ, P]
+    lib.attn_partial_paged.restype = I32
+    lib.gqa_decode_attn_paged.argtypes = common_paged + [P, P, P, SZ, P]
+    lib.gqa_decode_attn_paged.restype = I32
     return lib
 
 
@@ -163,6 +170,15 @@ def _check(status):
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class SkvPaged(ctypes.Structure):
+    _fields_ = [
+        ("block_len", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p),
+    ]
 
 
 def _require_cuda(*ts):
@@ -245,6 +261,44 @@ def _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax
         if s is not None and (s.dtype != torch.float32 or not s.is_contiguous()):
             raise ValueError("scales must be contiguous float32 [B,Hkv,n_blocks]")
     return d, bounds, n_split
+
+
+def _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scale, v_scale, softmax_scale,
+                scale_block):
+    """Descriptor of a paged cache: pages [num_blocks, Hkv, block_len, d], block table
+    int32 [B, max_blocks]; S_max = max_blocks * block_len logical tokens per sequence."""
+    _require_cuda(q, k_pages, v_pages, seq_lens, k_scale, v_scale, block_table)
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    if block_table.dtype != torch.int32 or not block_table.is_contiguous() or block_table.dim() != 2:
+        raise ValueError("block_table must be contiguous int32 [B, max_blocks]")
+    if q.dim() != 4 or k_pages.dim() != 4 or v_pages.dim() != 4:
+        raise ValueError("q must be [B,Tq,Hq,dk] and pages [num_blocks,Hkv,block_len,d]")
+    for t in (q, k_pages, v_pages):
+        if t.stride(-1) != 1:
+            raise ValueError("the head dim must be unit-stride")
+    B, Tq, Hq, dk = q.shape
+    nb, Hkv, L, dk2 = k_pages.shape
+    if dk2 != dk or v_pages.shape[:3] != k_pages.shape[:3] or block_table.shape[0] != B:
+        raise ValueError("q / pages / block_table shapes disagree")
+    d = SkvDesc()
+    d.B, d.Tq, d.Hq, d.Hkv, d.dk, d.dv = B, Tq, Hq, Hkv, dk, v_pages.shape[3]
+    d.S_max = block_table.shape[1] * L
+    d.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(dk)
+    d.kv_dtype = _kv_dtype(k_pages)
+    d.scale_block = scale_block
+    for i in range(3):
+        d.q_strides[i] = q.stride(i)
+        d.k_strides[i] = k_pages.stride(i)
+        d.v_strides[i] = v_pages.stride(i)
+    pg = SkvPaged()
+    pg.block_len, pg.max_blocks, pg.num_blocks = L, block_table.shape[1], nb
+    pg.block_table = block_table.data_ptr()
+    bounds, n_split = _bounds_array(split_bounds, B)
+    for s_ in (k_scale, v_scale):
+        if s_ is not None and (s_.dtype != torch.float32 or not s_.is_contiguous()):
+            raise ValueError("scales must be contiguous float32 [num_blocks,Hkv,block_len/scale_block]")
+    return d, pg, bounds, n_split
 
 
 def attn_partial_workspace_size(desc, bounds, n_split):
@@ -359,8 +413,50 @@ def gqa_decode_attn_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_po
     return out, lse
 
 
+def attn_partial_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, causal_offset=NO_CAUSAL,
+                       k_scale=None, v_scale=None, softmax_scale=None, scale_block=64, out_partial=None,
+                       lse_partial=None):
+    """attn_partial over a paged cache (pages [num_blocks,Hkv,block_len,d], block table
+    int32 [B,max_blocks]; split bounds and seq_lens in logical tokens)."""
+    d, pg, bounds, n_split = _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scale, v_scale,
+                                         softmax_scale, scale_block)
+    dev = q.device
+    if out_partial is None:
+        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    ws = _workspace(nbytes, dev)
+    _check(_lib.attn_partial_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), bounds, n_split, int(causal_offset),
+                                   _ptr(out_partial), _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
+    return out_partial, lse_partial
+
+
+def gqa_decode_attn_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, causal_offset=NO_CAUSAL,
+                          k_scale=None, v_scale=None, softmax_scale=None, scale_block=64, out=None, lse=None,
+                          workspace=None):
+    """gqa_decode_attn over a paged cache (see attn_partial_paged)."""
+    d, pg, bounds, n_split = _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scale, v_scale,
+                                         softmax_scale, scale_block)
+    dev = q.device
+    if out is None:
+        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
+    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    _check(_lib.gqa_decode_attn_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), bounds, n_split,
+                                      int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
+                                      nbytes if workspace is None else workspace.numel(), _stream()))
+    return out, lse
+
+
 __all__ = [
     "attn_partial",
+    "attn_partial_paged",
+    "gqa_decode_attn_paged",
     "attn_partial_pos",
     "attn_merge_lse",
     "gqa_decode_attn",

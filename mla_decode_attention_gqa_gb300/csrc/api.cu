@@ -248,19 +248,22 @@ size_t ws_bytes_for(const skv_desc* d, int n_part) {
 }
 
 skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, const int64_t* strides, int dim,
-                         int box_rows) {
+                         int box_rows, const skv_paged* pg = nullptr) {
   cudaError_t e;
   auto encode = get_encode_fn(&e);
   if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
   const bool fp8 = d->kv_dtype == SKV_KV_FP8_E4M3;
   const int esz = fp8 ? 1 : 2;
-  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(d->S_max),
-                        static_cast<cuuint64_t>(d->Hkv), static_cast<cuuint64_t>(d->B)};
+  // contiguous: (dim, token, head, sequence); paged: (dim, row in page, head, page)
+  const int64_t rows = pg ? pg->block_len : d->S_max;
+  const int64_t outer = pg ? pg->num_blocks : d->B;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(d->Hkv), static_cast<cuuint64_t>(outer)};
   const int64_t tok_b = strides[2] * esz;
   int64_t head_b = strides[1] * esz, batch_b = strides[0] * esz;
   // a stride of a size-1 dimension is never stepped; give it any legal value
-  if (d->Hkv == 1 || head_b == 0) head_b = std::max<int64_t>(head_b, tok_b * d->S_max);
-  if (d->B == 1 || batch_b == 0) batch_b = std::max<int64_t>(batch_b, head_b * d->Hkv);
+  if (d->Hkv == 1 || head_b == 0) head_b = std::max<int64_t>(head_b, tok_b * rows);
+  if (outer == 1 || batch_b == 0) batch_b = std::max<int64_t>(batch_b, head_b * d->Hkv);
   cuuint64_t gstride[3] = {static_cast<cuuint64_t>(tok_b), static_cast<cuuint64_t>(head_b),
                            static_cast<cuuint64_t>(batch_b)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1, 1};
@@ -302,8 +305,8 @@ skv_status encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, ui
 // Fill the launch parameters common to every GQA partial launch.
 skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, const void* q, const float* ks,
                        const float* vs, const int32_t* seq_lens, const int32_t* bounds, int32_t n_split,
-                       int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos, float* out_o,
-                       float* out_lse, bool zero_empty) {
+                       int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos, const skv_paged* pg,
+                       float* out_o, float* out_lse, bool zero_empty) {
   std::memset(p, 0, sizeof(*p));
   cudaError_t e;
   p->err = device_error_word(&e);
@@ -323,6 +326,12 @@ skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, cons
   p->causal_offset = q_pos ? SKV_NO_CAUSAL : causal_offset;
   p->q_pos = q_pos;
   p->k_pos = k_pos;
+  if (pg) {
+    p->block_table = pg->block_table;
+    p->block_len = pg->block_len;
+    p->max_blocks = pg->max_blocks;
+    p->num_blocks = pg->num_blocks;
+  }
   p->scale_log2 = d->softmax_scale * 1.4426950408889634f;
   p->B = d->B;
   p->Tq = d->Tq;
@@ -370,7 +379,7 @@ skv_status encode_q_map(CUtensorMap* map, const void* q, const skv_desc* d) {
 // fp32 partial per split straight into out_o / out_lse.
 skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v, const int32_t* seq_lens,
                   const int32_t* bounds, int32_t n_split, int64_t causal_offset, const int32_t* q_pos,
-                  const int32_t* k_pos, bool fused, float* out_o,
+                  const int32_t* k_pos, const skv_paged* pg, bool fused, float* out_o,
                   float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream) {
   static thread_local PartialParams p;
   Plan pl;
@@ -379,7 +388,7 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   const int rows = tc_attn_rows_per_cta();
   pl.m_tiles = static_cast<int>((static_cast<int64_t>(d->Tq) * (d->Hq / d->Hkv) + rows - 1) / rows);
   skv_status st = fill_params(&p, d, pl, q, nullptr, nullptr, seq_lens, bounds, n_split, causal_offset, q_pos,
-                              k_pos, out_o, out_lse, true);
+                              k_pos, pg, out_o, out_lse, true);
   if (st != SKV_OK) return st;
   TcAttnExtra x;
   x.fused = fused ? 1 : 0;
@@ -387,8 +396,10 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   x.out_lse = lse_final;
   CUtensorMap tmq, tmk, tmv;
   if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, tc_attn_kv_tile())) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, tc_attn_kv_tile())) != SKV_OK) return st;
+  // a paged cache is read in 64-token halves of a tile (pages hold multiples of 64 tokens)
+  const int kv_box = pg ? tc_attn_kv_tile() / 2 : tc_attn_kv_tile();
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kv_box, pg)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kv_box, pg)) != SKV_OK) return st;
   const int64_t n_items = static_cast<int64_t>(d->B) * d->Hkv * (fused ? 1 : n_split) * pl.m_tiles;
   cudaError_t e = launch_tc_attn(p, x, tmq, tmk, tmv, n_items, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core attention launch");
@@ -398,10 +409,10 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
 skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const void* k, const void* v,
                        const float* ks, const float* vs, const int32_t* seq_lens, const int32_t* bounds,
                        int32_t n_split, int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos,
-                       float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream) {
+                       const skv_paged* pg, float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream) {
   static thread_local PartialParams p;  // ~8 KB: keep it off the stack
-  skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, q_pos, k_pos, out_o,
-                              out_lse, zero_empty);
+  skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, q_pos, k_pos, pg,
+                              out_o, out_lse, zero_empty);
   if (st != SKV_OK) return st;
   CUtensorMap tmk, tmv;
   cudaError_t e;
@@ -412,7 +423,7 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
       // loads its own slice of dims
       CUtensorMap tmq;
       if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
-      if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, mla_tc_kv_tile())) != SKV_OK) return st;
+      if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, mla_tc_kv_tile(), pg)) != SKV_OK) return st;
       TcAttnExtra x;
       x.fused = 0;
       x.out_bf16 = nullptr;
@@ -422,13 +433,13 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
       return SKV_OK;
     }
     // one latent map serves K (all 576 columns) and V (its first 512 columns)
-    if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kMlaTileN)) != SKV_OK) return st;
+    if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kMlaTileN, pg)) != SKV_OK) return st;
     e = launch_mla_partial(p, tmk, pl.n_items, stream);
     if (e != cudaSuccess) return cuda_fail(e, "MLA partial attention launch");
     return SKV_OK;
   }
-  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN)) != SKV_OK) return st;
-  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN, pg)) != SKV_OK) return st;
+  if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN, pg)) != SKV_OK) return st;
   e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
   return SKV_OK;
@@ -503,6 +514,21 @@ skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* spli
 
 namespace {
 
+// Paged-cache description of a *_paged call.
+skv_status validate_paged(const skv_desc* d, const skv_paged* pg) {
+  if (!pg) return fail(SKV_EINVAL, "paged is NULL");
+  if (!pg->block_table || !aligned(pg->block_table, 4)) return fail(SKV_EINVAL, "block_table NULL or misaligned");
+  if (pg->block_len <= 0 || pg->block_len % kTileN)
+    return fail(SKV_EINVAL, "block_len must be a positive multiple of 64");
+  if (pg->max_blocks <= 0 || pg->num_blocks <= 0) return fail(SKV_EINVAL, "max_blocks and num_blocks must be positive");
+  if (pg->num_blocks >= (int64_t(1) << 31)) return fail(SKV_EINVAL, "num_blocks must be below 2^31");
+  if (d->S_max > static_cast<int64_t>(pg->max_blocks) * pg->block_len)
+    return fail(SKV_EINVAL, "S_max must be at most max_blocks * block_len");
+  if (d->kv_dtype == SKV_KV_FP8_E4M3 && pg->block_len % d->scale_block)
+    return fail(SKV_EINVAL, "block_len must be a multiple of scale_block for fp8 pages");
+  return SKV_OK;
+}
+
 // Positions of a *_pos call: both arrays present, aligned for the kernels' vector loads.
 skv_status validate_positions(const skv_desc* d, const int32_t* q_pos, const int32_t* k_pos) {
   if (!q_pos || !k_pos) return fail(SKV_EINVAL, "q_pos and k_pos must be non-NULL");
@@ -515,8 +541,8 @@ skv_status validate_positions(const skv_desc* d, const int32_t* q_pos, const int
 skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                              const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                              const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
-                             const int32_t* q_pos, const int32_t* k_pos, float* out_partial, float* lse_partial,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+                             const int32_t* q_pos, const int32_t* k_pos, const skv_paged* pg, float* out_partial,
+                             float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
@@ -524,13 +550,13 @@ skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_
   if (!aligned(out_partial, 16) || !aligned(lse_partial, 4)) return fail(SKV_EINVAL, "outputs misaligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc(desc)) {
-    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, false,
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, pg, false,
                   out_partial, lse_partial, nullptr, nullptr, s);
   }
   const Plan pl = make_plan(desc, split_bounds, n_split);
   if (pl.n_chunk == 1) {
     return run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
-                       causal_offset, q_pos, k_pos, out_partial, lse_partial, true, s);
+                       causal_offset, q_pos, k_pos, pg, out_partial, lse_partial, true, s);
   }
   const size_t need = ws_bytes_for(desc, pl.n_part);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
@@ -540,7 +566,7 @@ skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
   st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   q_pos, k_pos, ws_o, ws_l, false, s);
+                   q_pos, k_pos, pg, ws_o, ws_l, false, s);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge(ws_o, ws_l, pl.n_chunk, n_split, static_cast<int64_t>(rows), desc->dv, out_partial,
                                false, lse_partial, s);
@@ -551,8 +577,8 @@ skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_
 skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                                 const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                                 const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
-                                const int32_t* q_pos, const int32_t* k_pos, void* out, float* lse, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+                                const int32_t* q_pos, const int32_t* k_pos, const skv_paged* pg, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   skv_status st = validate(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
@@ -561,7 +587,7 @@ skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc(desc)) {
     if (!aligned(out, 16)) return fail(SKV_EINVAL, "out must be 16-byte aligned for this shape");
-    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, true,
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, pg, true,
                   nullptr, nullptr, out, lse, s);
   }
   const Plan pl = make_plan(desc, split_bounds, n_split);
@@ -573,7 +599,7 @@ skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void*
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
   st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   q_pos, k_pos, ws_o, ws_l, false, s);
+                   q_pos, k_pos, pg, ws_o, ws_l, false, s);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
@@ -589,8 +615,8 @@ skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache
                         const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
                         float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
   return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
-                           causal_offset, nullptr, nullptr, out_partial, lse_partial, workspace, workspace_bytes,
-                           stream);
+                           causal_offset, nullptr, nullptr, nullptr, out_partial, lse_partial, workspace,
+                           workspace_bytes, stream);
 }
 
 skv_status attn_partial_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
@@ -602,7 +628,7 @@ skv_status attn_partial_pos(const skv_desc* desc, const void* q, const void* k_c
   if (st != SKV_OK) return st;
   if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
   return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
-                           k_pos, out_partial, lse_partial, workspace, workspace_bytes, stream);
+                           k_pos, nullptr, out_partial, lse_partial, workspace, workspace_bytes, stream);
 }
 
 skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, int32_t dv, const float* out_partials,
@@ -638,7 +664,32 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
                            float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
-                              causal_offset, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
+                              causal_offset, nullptr, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+skv_status attn_partial_paged(const skv_desc* desc, const skv_paged* paged, const void* q, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
+                              int64_t causal_offset, float* out_partial, float* lse_partial, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_paged(desc, paged)) != SKV_OK) return st;
+  return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                           causal_offset, nullptr, nullptr, paged, out_partial, lse_partial, workspace,
+                           workspace_bytes, stream);
+}
+
+skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
+                                 int64_t causal_offset, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  skv_status st = validate(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
+  if ((st = validate_paged(desc, paged)) != SKV_OK) return st;
+  return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                              causal_offset, nullptr, nullptr, paged, out, lse, workspace, workspace_bytes, stream);
 }
 
 skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
@@ -650,7 +701,7 @@ skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* 
   if (st != SKV_OK) return st;
   if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
-                              k_pos, out, lse, workspace, workspace_bytes, stream);
+                              k_pos, nullptr, out, lse, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
@@ -722,7 +773,7 @@ extern "C" skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* 
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
   st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   nullptr, nullptr, ws_o, ws_l, false, s);
+                   nullptr, nullptr, nullptr, ws_o, ws_l, false, s);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

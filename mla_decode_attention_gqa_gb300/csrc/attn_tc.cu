@@ -220,6 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d_nohint(smem + kOffQ + k * kQTileBytes + bx * (kQTileBytes / 2), &tmq, &bars->q_full, bx * 64,
                              g * G, t_start, b);
       }
+      // a paged cache is read in 64-token halves (a page holds a multiple of 64 tokens),
+      // each half's page read one tile ahead, behind the stage wait
+      const bool paged = p.block_table != nullptr;
+      // (a half that starts at or past S_max only holds masked tokens: it reuses the first
+      // half's page instead of reading past the sequence's block-table row)
+      auto pages_of = [&](int t, int& a, int& c) {
+        a = kv_page_of(p, b, t);
+        c = (t + kTN / 2 < p.S_max) ? kv_page_of(p, b, t + kTN / 2) : a;
+      };
+      int pg0 = 0, pg1 = 0;
+      if (paged) pages_of((tile_begin + tile_of(0)) * kTN, pg0, pg1);
       int issued = 0;
       for (int i = 0; i < n_used; ++i) {
         const int s = i % kNStage;
@@ -227,9 +238,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
         uint8_t* st = smem + kOffRing + s * kStageBytes;
         const int tok = (tile_begin + tile_of(i)) * kTN;
-        for (int bx = 0; bx < 2; ++bx) {
-          tma_load_4d_nohint(st + bx * kKVBoxBytes, &tmk, &bars->kv_full[s], bx * 64, tok, g, b);
-          tma_load_4d_nohint(st + kKTileBytes + bx * kKVBoxBytes, &tmv, &bars->kv_full[s], bx * 64, tok, g, b);
+        if (!paged) {
+          for (int bx = 0; bx < 2; ++bx) {
+            tma_load_4d_nohint(st + bx * kKVBoxBytes, &tmk, &bars->kv_full[s], bx * 64, tok, g, b);
+            tma_load_4d_nohint(st + kKTileBytes + bx * kKVBoxBytes, &tmv, &bars->kv_full[s], bx * 64, tok, g, b);
+          }
+        } else {
+          const int cur[2] = {pg0, pg1};
+          if (i + 1 < n_used) pages_of((tile_begin + tile_of(i + 1)) * kTN, pg0, pg1);
+          for (int hf = 0; hf < 2; ++hf) {
+            const int row = (tok + hf * (kTN / 2)) % p.block_len;
+            for (int bx = 0; bx < 2; ++bx) {
+              const int off = bx * kKVBoxBytes + hf * (kKVBoxBytes / 2);  // rows 64 hf.. of box bx
+              tma_load_4d_nohint(st + off, &tmk, &bars->kv_full[s], bx * 64, row, g, cur[hf]);
+              tma_load_4d_nohint(st + kKTileBytes + off, &tmv, &bars->kv_full[s], bx * 64, row, g, cur[hf]);
+            }
+          }
         }
         issued = i + 1;
       }

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       const uint64_t pol = l2_policy_evict_first();
+      const bool paged = p.block_table != nullptr;
+      // paged cache: the next tile's page is read one tile ahead, behind the stage wait
+      int page_next = paged ? kv_page_of(p, b, tile_begin * TN) : b;
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % NSTAGE;
@@ -173,10 +176,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         uint8_t* ks = smem + s * C::STAGE_BYTES;
         uint8_t* vs = ks + C::TILE_BYTES;
         const int tok = (tile_begin + i) * TN;
+        const int outer = page_next;  // page (paged) or sequence
+        const int row = paged ? tok % p.block_len : tok;
+        if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + TN);
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
-          tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, fb, bx * C::BOX_ELEMS, tok, g, b, pol);
-          tma_load_4d(vs + bx * C::BOX_BYTES, &tmv, fb, bx * C::BOX_ELEMS, tok, g, b, pol);
+          tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, fb, bx * C::BOX_ELEMS, row, g, outer, pol);
+          tma_load_4d(vs + bx * C::BOX_BYTES, &tmv, fb, bx * C::BOX_ELEMS, row, g, outer, pol);
         }
         issued = i + 1;
       }
@@ -261,8 +267,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int t0 = (tile_begin + i) * TN;
     float ksc = 1.f, vsc = 1.f;
     if constexpr (C::FP8) {
-      ksc = __ldg(kscale_row + t0 / p.scale_block);
-      vsc = __ldg(vscale_row + t0 / p.scale_block);
+      if (p.block_table == nullptr) {
+        ksc = __ldg(kscale_row + t0 / p.scale_block);
+        vsc = __ldg(vscale_row + t0 / p.scale_block);
+      } else {
+        // per-page scales [num_blocks][Hkv][block_len / scale_block]; a page outside the
+        // cache reads as zeros through TMA, so its scale is never fetched
+        const int page = kv_page_of(p, b, t0);
+        if (page >= 0 && page < p.num_blocks) {
+          const int per = p.block_len / p.scale_block;
+          const int64_t idx = (static_cast<int64_t>(page) * p.Hkv + g) * per + (t0 % p.block_len) / p.scale_block;
+          ksc = __ldg(p.k_scale + idx);
+          vsc = __ldg(p.v_scale + idx);
+        } else {
+          ksc = vsc = 0.f;
+        }
+      }
     }
     if (!mbar_wait(&full[full_slot<C>(i)], full_parity<C>(i), p.err, kDevErrFullWait)) break;
     const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);

@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&tmk);
       const uint64_t pol = l2_policy_evict_first();
+      const bool paged = p.block_table != nullptr;
+      int page_next = paged ? kv_page_of(p, b, tile_begin * kTN) : b;  // read one tile ahead
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % kNStage;
@@ -133,8 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[s], kTileBytes);
         uint8_t* ks = smem + s * kTileBytes;
         const int tok = (tile_begin + i) * kTN;
+        const int outer = page_next;
+        const int row = paged ? tok % p.block_len : tok;
+        if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
 #pragma unroll
-        for (int bx = 0; bx < kNBox; ++bx) tma_load_4d(ks + bx * kBoxBytes, &tmk, &full[s], bx * 64, tok, 0, b, pol);
+        for (int bx = 0; bx < kNBox; ++bx) tma_load_4d(ks + bx * kBoxBytes, &tmk, &full[s], bx * 64, row, 0, outer, pol);
         issued = i + 1;
       }
       for (int i = max(0, issued - kNStage); i < issued; ++i) {

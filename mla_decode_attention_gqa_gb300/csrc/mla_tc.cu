@@ -241,6 +241,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_4d_plain(smem + (bx < kQTmemBoxes ? bx * kQBoxBytes : kOffQRope), &tmq, &bars->q_full, bx * 64, 0,
                             t_start, b);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
+        const bool paged = p.block_table != nullptr;
+        int page_next = paged ? kv_page_of(p, b, tile_begin * kTN) : b;  // read one tile ahead
         int issued = 0;
         for (int i = 0; i < n_tiles && ok; ++i) {
           const int s = i % kNStage0;
@@ -249,8 +251,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->kv_full0[s], kStage0Bytes);
           uint8_t* st = smem + s * kStage0Bytes;
           const int tok = (tile_begin + i) * kTN;
+          const int outer = page_next;
+          const int row = paged ? tok % p.block_len : tok;
+          if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
           for (int bx = 0; bx < kKBoxes; ++bx)
-            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, tok, 0, b);
+            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, row, 0, outer);
           issued = i + 1;
         }
         for (int i = max(0, issued - kNStage0); i < issued; ++i) {
@@ -464,6 +469,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       if (lane == 0 && n_tiles > 0) {
         tma_prefetch_desc(&tml);
+        const bool paged = p.block_table != nullptr;
+        int page_next = paged ? kv_page_of(p, b, tile_begin * kTN) : b;  // read one tile ahead
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
           const int s = i % kNStage1;
@@ -472,8 +479,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->kv_full1[s], kStage1Bytes);
           uint8_t* st = smem + s * kStage1Bytes;
           const int tok = (tile_begin + i) * kTN;
+          const int outer = page_next;
+          const int row = paged ? tok % p.block_len : tok;
+          if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
           for (int bx = 0; bx < kVBoxes; ++bx)
-            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, tok, 0, b);
+            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row, 0, outer);
           issued = i + 1;
         }
         for (int i = max(0, issued - kNStage1); i < issued; ++i) {

@@ -37,6 +37,10 @@ struct PartialParams {
   int64_t causal_offset;
   const int32_t* q_pos;  // original positions [B][Tq] / [B][S_max] (NULL: rows at
   const int32_t* k_pos;  // causal_offset + i, tokens at their index)
+  const int32_t* block_table;  // paged cache: [B][max_blocks] page of each logical block
+  int32_t block_len;           //   (NULL: contiguous [B][Hkv][S_max][d]; the tensor maps'
+  int32_t max_blocks;          //   outer coordinate is then the page, the token one the
+  int64_t num_blocks;          //   row inside it)
   float scale_log2;  // softmax_scale * log2(e)
   int32_t B, Tq, Hq, Hkv, G;
   int32_t S_max;  // tokens at or past S_max do not exist
@@ -44,6 +48,14 @@ struct PartialParams {
   int32_t zero_empty;  // write o = 0 for items with no visible token
   int32_t bounds[kMaxBounds];  // [B][n_split + 1]
 };
+
+#ifdef __CUDACC__
+// Page holding logical token `tok` of sequence b in a paged cache (the tensor maps then
+// take (tok % block_len, page) where a contiguous cache takes (tok, b)).
+__device__ __forceinline__ int kv_page_of(const PartialParams& p, int b, int tok) {
+  return __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + tok / p.block_len);
+}
+#endif
 
 // Supported GQA kernel variants.
 enum class GqaVariant {

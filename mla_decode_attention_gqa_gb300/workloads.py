@@ -123,8 +123,15 @@ RING_PREFILL_ZIGZAG = Workload("ring_prefill_zigzag_8x4096", B=1, Tq=4096, Hq=12
 RING_PREFILL_STRIPED = Workload("ring_prefill_striped_8x4096", B=1, Tq=4096, Hq=128, Hkv=8, dk=128, dv=128,
                                 S=8 * 4096, n_split=8, layout="striped", cp_rank=0, seed=1006)
 
+# The Helix dense decode and the MLA decode with their caches in 64-token pages at a
+# seeded permutation of physical blocks.
+HELIX_DENSE_128K_PAGED = replace(HELIX_DENSE_128K, name="helix_dense_decode_s128k_paged64", paged=True,
+                                 block_len=64, seed=1007)
+MLA_ABSORBED_PAGED = replace(MLA_ABSORBED, name="mla_absorbed_decode_s32k_paged64", paged=True, block_len=64,
+                             seed=1008)
+
 WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL, RING_PREFILL_ZIGZAG,
-             RING_PREFILL_STRIPED]
+             RING_PREFILL_STRIPED, HELIX_DENSE_128K_PAGED, MLA_ABSORBED_PAGED]
 
 
 def scaled(w: Workload, **kw) -> Workload:

@@ -125,3 +125,50 @@ def test_missing_workspace_is_reported():
     b, n = _bounds(((0, 1024), (0, 1024)))
     st = lib.gqa_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, b, n, 0, FAKE, FAKE, None, 0, None)
     assert st == skv.SKV_EWORKSPACE
+
+
+def _paged(block_len=64, max_blocks=16, num_blocks=40, table=FAKE):
+    pg = skv.SkvPaged()
+    pg.block_len, pg.max_blocks, pg.num_blocks = block_len, max_blocks, num_blocks
+    pg.block_table = table.value if table is not None else None
+    return pg
+
+
+def _call_paged(d, pg, rows=((0, 1024), (0, 1024))):
+    lib = skv.load_library()
+    b, n = _bounds(rows)
+    return lib.attn_partial_paged(ctypes.byref(d), ctypes.byref(pg) if pg is not None else None, FAKE, FAKE, FAKE,
+                                  None, None, FAKE, b, n, 0, FAKE, FAKE, None, 0, None)
+
+
+def test_paged_arguments_are_checked_before_any_device_access():
+    d = _desc()  # S_max = 1024
+    assert _call_paged(d, None) == skv.SKV_EINVAL
+    assert _call_paged(d, _paged(block_len=96)) == skv.SKV_EINVAL  # not a multiple of 64
+    assert "block_len" in skv.last_error()
+    assert _call_paged(d, _paged(block_len=0)) == skv.SKV_EINVAL
+    assert _call_paged(d, _paged(table=None)) == skv.SKV_EINVAL
+    assert _call_paged(d, _paged(table=ctypes.c_void_p(0x10002))) == skv.SKV_EINVAL  # misaligned
+    assert _call_paged(d, _paged(max_blocks=8)) == skv.SKV_EINVAL  # 8 * 64 < S_max
+    assert "S_max" in skv.last_error()
+    assert _call_paged(d, _paged(num_blocks=0)) == skv.SKV_EINVAL
+    d8 = _desc(kv_dtype=1, scale_block=128)
+    assert _call_paged(d8, _paged(block_len=64)) == skv.SKV_EINVAL  # pages smaller than a scale block
+
+
+def test_position_arguments_are_checked_before_any_device_access():
+    lib = skv.load_library()
+    b, n = _bounds(((0, 1024), (0, 1024)))
+
+    def call(d, qp, kp):
+        return lib.attn_partial_pos(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, b, n, qp, kp, FAKE, FAKE,
+                                    None, 0, None)
+
+    d = _desc()
+    assert call(d, None, FAKE) == skv.SKV_EINVAL
+    assert call(d, FAKE, None) == skv.SKV_EINVAL
+    assert call(d, FAKE, ctypes.c_void_p(0x10004)) == skv.SKV_EINVAL  # k_pos not 16-byte aligned
+    assert call(_desc(S_max=1022), FAKE, FAKE) == skv.SKV_EINVAL  # S_max not a multiple of 4
+    mla = _desc(Hq=128, Hkv=1, dk=576, dv=512, q_strides=(128 * 576, 128 * 576, 576),
+                k_strides=(1024 * 576, 1024 * 576, 576), v_strides=(1024 * 576, 1024 * 576, 576))
+    assert call(mla, FAKE, FAKE) == skv.SKV_EUNSUPPORTED
