@@ -216,7 +216,7 @@ skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* 
                                void* stream);
 
 /*
- * Paged block KV cache.  The attention-DP page ("KV Cache" section) keeps each rank's
+ * Paged block KV cache.  "Attention DP", section "KV Cache", keeps each rank's
  * cache as [num_blocks, num_kv_heads, block_len, d_head]; a per-sequence block table maps
  * logical block i of sequence b (its tokens [i * block_len, (i + 1) * block_len)) to the
  * physical page that holds it, so token t of sequence b, KV head g is row t % block_len

@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE (see ``oracle/__init__.py``).
 
-Source: the attention-DP page's section "KV Cache" keeps each rank's cache as
+Source: "Attention DP", section "KV Cache": each rank keeps its cache as
 [num_blocks, num_kv_heads / TP, block_len, d_head].  Reading (where the page is silent,
 listed in the design doc): a per-sequence block table maps logical block i of sequence b to
 the physical block that holds its tokens [i * block_len, (i + 1) * block_len), so token t

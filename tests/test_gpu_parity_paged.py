@@ -1,5 +1,5 @@
 """GPU parity over a paged block KV cache (pages [num_blocks, Hkv, block_len, d] and a
-per-sequence block table; the attention-DP page's "KV Cache" layout) through
+per-sequence block table; the layout of "Attention DP", section "KV Cache") through
 attn_partial_paged / gqa_decode_attn_paged.  Each case is checked against the fp64
 oracle and, bit for bit, against the contiguous call on the same logical cache (the
 kernels read the same bytes in the same order)."""

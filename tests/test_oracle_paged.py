@@ -1,4 +1,4 @@
-"""Pins for the paged block KV cache gather (attention-DP page, section "KV Cache": a rank's
+"""Pins for the paged block KV cache gather ("Attention DP", section "KV Cache": a rank's
 cache is [num_blocks, num_kv_heads/TP, block_len, d_head]; a block table maps each
 sequence's logical blocks to physical ones).
 
