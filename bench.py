@@ -67,7 +67,8 @@ def config_of(w, ws=1):
                   ("KV (%.4f GB) fits in L2: a parity-size workload, not a bench line" % (alloc / 1e9)),
             "parallelism": f"replicas x{ws}",
             **({"layout": w.layout, "query_rank": w.cp_rank} if w.layout != "contiguous" else {}),
-            **({"paged": True, "block_len": w.block_len} if w.paged else {})}
+            **({"paged": True, "block_len": w.block_len} if w.paged else {}),
+            **({"ring_steps": w.n_split, "step_api": "attn_ring_step"} if w.ring_steps else {})}
 
 
 def workload_by_name(name):
@@ -222,6 +223,19 @@ def sum_over_ranks(x, ws):
 
 # --------------------------------------------------------------------------- CPU oracle leg
 
+def launches_per_step(w):
+    """This library's kernel launches in one timed step of a workload (its routing):
+    the tensor-core shapes (bf16, d = 128, the group dividing 128, >= 128 rows per KV
+    head) run one fused kernel; every other call is a partial kernel plus the merge."""
+    G = w.Hq // w.Hkv
+    tensor_core = (not w.mla and w.kv_dtype == "bf16" and w.dk == 128 and w.dv == 128 and 128 % G == 0
+                   and w.Tq * G >= 128)
+    if w.ring_steps:  # tensor core: one kernel per step, merging in its epilogue; otherwise the
+        # block's partial per step and a two-way merge after the first
+        return w.n_split if tensor_core else 2 * w.n_split - 1
+    return 1 if tensor_core else 2
+
+
 def oracle_sample(w, budget_s=12.0, max_groups=None):
     """Time the fp64 oracle on whole (batch, KV head) groups of the workload until the
     budget is spent; returns (KV bytes processed, seconds, groups, tokens)."""
@@ -317,8 +331,23 @@ def ours_arm(args, w, ws, rank, local):
         kw = dict(k_scale=inp.get("k_scale_pages"), v_scale=inp.get("v_scale_pages"), softmax_scale=w.scale,
                   scale_block=w.scale_block)
 
+    if w.ring_steps:  # pass-KV ring: every step's KV block in its own buffer
+        C = w.S // w.n_split
+        ring_blocks = [(inp["k"][:, :, j * C:(j + 1) * C].contiguous(), inp["v"][:, :, j * C:(j + 1) * C].contiguous(),
+                        torch.clamp(inp["seq_lens"] - j * C, 0, C).to(torch.int32)) for j in range(w.n_split)]
+        o_acc = torch.empty((w.B, w.Tq, w.Hq, w.dv), dtype=torch.float32, device=dev)
+        lse_acc = torch.empty((w.B, w.Tq, w.Hq), dtype=torch.float32, device=dev)
+
+    def ring_run(q, blocks):
+        C = w.S // w.n_split
+        for j, (kb, vb, sl) in enumerate(blocks):
+            skv.attn_ring_step(q, kb, vb, sl, o_acc, lse_acc, w.causal_offset - j * C, first=(j == 0),
+                               softmax_scale=w.scale)
+
     def step():
-        if w.paged:
+        if w.ring_steps:
+            ring_run(inp["q"], ring_blocks)
+        elif w.paged:
             skv.gqa_decode_attn_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["seq_lens"], bounds,
                                       inp["block_table"], w.causal_offset, out=out, lse=lse, **kw)
         elif positional:
@@ -367,7 +396,9 @@ def ours_arm(args, w, ws, rank, local):
     if not args.no_e2e:
         host = {}
         # the MLA value cache is a view of the latent (k): it is copied once, as k
-        if w.paged:
+        if w.ring_steps:
+            keys = ("q",)
+        elif w.paged:
             keys = ("q", "k_pages", "seq_lens", "block_table") + (() if w.mla else ("v_pages",)) + (
                 ("k_scale_pages", "v_scale_pages") if w.kv_dtype != "bf16" else ())
         elif w.mla:
@@ -377,6 +408,9 @@ def ours_arm(args, w, ws, rank, local):
         for key in keys:
             t = inp.get(key)
             host[key] = None if t is None else t.cpu().pin_memory()
+        if w.ring_steps:  # each step's block arrives from the host into its own buffer
+            for j, (kb, vb, sl) in enumerate(ring_blocks):
+                host[f"k{j}"], host[f"v{j}"], host[f"s{j}"] = kb.cpu().pin_memory(), vb.cpu().pin_memory(), sl.cpu().pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -396,7 +430,12 @@ def ours_arm(args, w, ws, rank, local):
                     dev_bufs[k2].copy_(t, non_blocking=True)
             e2e_kw = dict(k_scale=dev_bufs.get("k_scale"), v_scale=dev_bufs.get("v_scale"), softmax_scale=w.scale,
                           scale_block=w.scale_block, out=out, lse=lse)
-            if w.paged:
+            if w.ring_steps:
+                ring_run(dev_bufs["q"], [(dev_bufs[f"k{j}"], dev_bufs[f"v{j}"], dev_bufs[f"s{j}"])
+                                         for j in range(w.n_split)])
+                out.copy_(o_acc)  # the final output (bf16) read back like the other workloads'
+                lse.copy_(lse_acc)
+            elif w.paged:
                 e2e_kw.update(k_scale=dev_bufs.get("k_scale_pages"), v_scale=dev_bufs.get("v_scale_pages"))
                 skv.gqa_decode_attn_paged(dev_bufs["q"], dev_bufs["k_pages"], dev_bufs["v_pages"], dev_bufs["seq_lens"],
                                           bounds, dev_bufs["block_table"], w.causal_offset, **e2e_kw)
@@ -467,7 +506,7 @@ def ours_arm(args, w, ws, rank, local):
         "config": config_of(w, ws),
         "roofline": roof,
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),

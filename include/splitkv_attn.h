@@ -254,6 +254,33 @@ skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, c
                                  int64_t causal_offset, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/*
+ * attn_ring_step -- one pass-KV ring step ("Context Parallelism for Scalable Million-Token
+ * Inference", section "Pass-KV keeps queries local and circulates keys and values"): the
+ * local query chunk attends over the KV block received at this step, held in its own
+ * buffer, and the result is merged into a running output in place with the exact LSE
+ * merge, so no step's partial is kept.
+ *
+ *   desc     shapes; desc->S_max = tokens in this step's block
+ *   k_block, v_block  DEVICE [B][Hkv][S_max][d] with desc strides (fp8: scales as for
+ *            attn_partial, indexed by position in the block)
+ *   seq_lens DEVICE int32 [B]: tokens of the block that exist for each sequence
+ *   causal_offset  query row i sees block token t iff t <= causal_offset + i (the chunk's
+ *            offset minus the block's start; SKV_NO_CAUSAL for none)
+ *   first    nonzero: o_acc / lse_acc are written, not read (the first step)
+ *   o_acc    DEVICE fp32 [B][Tq][Hq][dv], lse_acc DEVICE fp32 [B][Tq][Hq]: the running
+ *            normalised output and natural-log LSE, updated in place; rows that have seen
+ *            no token yet hold o = 0, lse = -inf
+ *   workspace  DEVICE, at least attn_ring_step_workspace_size(desc) bytes, 256-aligned
+ * Errors as for attn_partial; the merge is the same one attn_merge_lse applies.
+ */
+skv_status attn_ring_step_workspace_size(const skv_desc* desc, size_t* bytes);
+
+skv_status attn_ring_step(const skv_desc* desc, const void* q, const void* k_block, const void* v_block,
+                          const float* k_scale, const float* v_scale, const int32_t* seq_lens, int64_t causal_offset,
+                          int32_t first, float* o_acc, float* lse_acc, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

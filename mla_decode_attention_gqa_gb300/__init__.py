@@ -43,6 +43,8 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attn_pos",
     "attn_partial_paged",
     "gqa_decode_attn_paged",
+    "attn_ring_step_workspace_size",
+    "attn_ring_step",
 )
 
 # Every symbol declared in include/splitkv_attn_selftest.h (hardware self-tests).
@@ -109,6 +111,10 @@ def _load():
     lib.attn_partial_paged.restype = I32
     lib.gqa_decode_attn_paged.argtypes = common_paged + [P, P, P, SZ, P]
     lib.gqa_decode_attn_paged.restype = I32
+    lib.attn_ring_step_workspace_size.argtypes = [D, ctypes.POINTER(SZ)]
+    lib.attn_ring_step_workspace_size.restype = I32
+    lib.attn_ring_step.argtypes = [D, P, P, P, P, P, P, I64, I32, P, P, P, SZ, P]
+    lib.attn_ring_step.restype = I32
     return lib
 
 
@@ -453,7 +459,28 @@ def gqa_decode_attn_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_tab
     return out, lse
 
 
+def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=NO_CAUSAL, first=False, k_scale=None,
+                   v_scale=None, softmax_scale=None, scale_block=64):
+    """One pass-KV ring step: attention of q over this step's KV block (its own buffer,
+    [B,Hkv,S_blk,d]) merged into the running o_acc fp32 [B,Tq,Hq,dv] / lse_acc fp32
+    [B,Tq,Hq] in place (written, not read, when first).  Returns (o_acc, lse_acc)."""
+    _require_cuda(o_acc, lse_acc)
+    d, _, _ = _prep(q, k_block, v_block, seq_lens, [[0, k_block.shape[2]]], k_scale, v_scale, softmax_scale,
+                    scale_block)
+    for t, shape, name in ((o_acc, (d.B, d.Tq, d.Hq, d.dv), "o_acc"), (lse_acc, (d.B, d.Tq, d.Hq), "lse_acc")):
+        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be contiguous float32 of shape {shape}")
+    n = ctypes.c_size_t(0)
+    _check(_lib.attn_ring_step_workspace_size(ctypes.byref(d), ctypes.byref(n)))
+    ws = _workspace(int(n.value), q.device)
+    _check(_lib.attn_ring_step(ctypes.byref(d), _ptr(q), _ptr(k_block), _ptr(v_block), _ptr(k_scale), _ptr(v_scale),
+                               _ptr(seq_lens), int(causal_offset), 1 if first else 0, _ptr(o_acc), _ptr(lse_acc),
+                               _ptr(ws), int(n.value), _stream()))
+    return o_acc, lse_acc
+
+
 __all__ = [
+    "attn_ring_step",
     "attn_partial",
     "attn_partial_paged",
     "gqa_decode_attn_paged",

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <vector>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -380,7 +381,7 @@ skv_status encode_q_map(CUtensorMap* map, const void* q, const skv_desc* d) {
 skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v, const int32_t* seq_lens,
                   const int32_t* bounds, int32_t n_split, int64_t causal_offset, const int32_t* q_pos,
                   const int32_t* k_pos, const skv_paged* pg, bool fused, float* out_o,
-                  float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream) {
+                  float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream, bool accumulate = false) {
   static thread_local PartialParams p;
   Plan pl;
   pl.n_chunk = 1;
@@ -394,6 +395,7 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   x.fused = fused ? 1 : 0;
   x.out_bf16 = out_bf16;
   x.out_lse = lse_final;
+  x.accumulate = accumulate ? 1 : 0;
   CUtensorMap tmq, tmk, tmv;
   if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
   // a paged cache is read in 64-token halves of a tile (pages hold multiples of 64 tokens)
@@ -690,6 +692,65 @@ skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, c
   if ((st = validate_paged(desc, paged)) != SKV_OK) return st;
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
                               causal_offset, nullptr, nullptr, paged, out, lse, workspace, workspace_bytes, stream);
+}
+
+skv_status attn_ring_step_workspace_size(const skv_desc* desc, size_t* bytes) {
+  if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
+  if (!desc) return fail(SKV_EINVAL, "desc is NULL");
+  if (desc->B <= 0 || 2 * static_cast<int64_t>(desc->B) > kMaxBounds) return fail(SKV_EINVAL, "B must be in [1, 1024]");
+  std::vector<int32_t> bounds(2 * desc->B);
+  for (int b = 0; b < desc->B; ++b) {
+    bounds[2 * b] = 0;
+    bounds[2 * b + 1] = static_cast<int32_t>(std::min<int64_t>(desc->S_max, INT32_MAX));
+  }
+  size_t part_ws = 0;
+  skv_status st = attn_partial_workspace_size(desc, bounds.data(), 1, &part_ws);
+  if (st != SKV_OK) return st;
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  *bytes = align_up(part_ws, 256) + align_up(rows * desc->dv * 4, 256) + align_up(rows * 4, 256);
+  return SKV_OK;
+}
+
+skv_status attn_ring_step(const skv_desc* desc, const void* q, const void* k_block, const void* v_block,
+                          const float* k_scale, const float* v_scale, const int32_t* seq_lens, int64_t causal_offset,
+                          int32_t first, float* o_acc, float* lse_acc, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  size_t need = 0;
+  skv_status st = attn_ring_step_workspace_size(desc, &need);
+  if (st != SKV_OK) return st;
+  if (!o_acc || !lse_acc) return fail(SKV_EINVAL, "o_acc and lse_acc must be non-NULL");
+  if (!aligned(o_acc, 16) || !aligned(lse_acc, 4)) return fail(SKV_EINVAL, "o_acc / lse_acc misaligned");
+  if (desc->dv % 4) return fail(SKV_EINVAL, "dv must be a multiple of 4");
+  std::vector<int32_t> bounds(2 * desc->B);  // one split: the whole block
+  for (int b = 0; b < desc->B; ++b) {
+    bounds[2 * b] = 0;
+    bounds[2 * b + 1] = static_cast<int32_t>(desc->S_max);
+  }
+  if (first) {  // the first block's partial is the running result
+    return attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, bounds.data(), 1, causal_offset,
+                             nullptr, nullptr, nullptr, o_acc, lse_acc, workspace, workspace_bytes, stream);
+  }
+  if (use_tc(desc)) {  // the tensor-core kernel merges into the running output in its epilogue
+    if ((st = validate(desc, bounds.data(), 1)) != SKV_OK) return st;
+    if ((st = validate_ptrs(desc, q, k_block, v_block, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
+    return run_tc(desc, q, k_block, v_block, seq_lens, bounds.data(), 1, causal_offset, nullptr, nullptr, nullptr,
+                  false, o_acc, lse_acc, nullptr, nullptr, static_cast<cudaStream_t>(stream), true);
+  }
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than attn_ring_step_workspace_size()");
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  size_t part_ws = 0;
+  if ((st = attn_partial_workspace_size(desc, bounds.data(), 1, &part_ws)) != SKV_OK) return st;
+  char* base = static_cast<char*>(workspace);
+  float* step_o = reinterpret_cast<float*>(base + align_up(part_ws, 256));
+  float* step_l = reinterpret_cast<float*>(base + align_up(part_ws, 256) + align_up(rows * desc->dv * 4, 256));
+  st = attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, bounds.data(), 1, causal_offset, nullptr,
+                         nullptr, nullptr, step_o, step_l, part_ws ? workspace : nullptr, part_ws, stream);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge_into(o_acc, lse_acc, step_o, step_l, static_cast<int64_t>(rows), desc->dv,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ring-step merge launch");
+  return SKV_OK;
 }
 
 skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,

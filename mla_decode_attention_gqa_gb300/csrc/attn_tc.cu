@@ -558,7 +558,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       const int64_t ro = ((static_cast<int64_t>(j) * p.B + b) * p.Tq + t_q) * p.Hq + h;
       float* orow = p.out_o + ro * kD;
-      const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
+      bool write_o = valid && (l_sum > 0.f || p.zero_empty);
+      // accumulate: o <- (w_acc o_acc + w o / l) / (w_acc + w) with w_x = e^{lse_x - max},
+      // the exact two-way merge; a row this item saw nothing of keeps its running value
+      float a_acc = 0.f, a_new = inv;
+      float lse_out = lse;
+      if (x.accumulate) {
+        const float lse_acc = valid ? p.out_lse[ro] : -INFINITY;
+        const float mx = fmaxf(lse_acc, lse);
+        write_o = valid && l_sum > 0.f;
+        if (write_o) {
+          const float wa = (lse_acc == -INFINITY) ? 0.f : __expf(lse_acc - mx);
+          const float wb = __expf(lse - mx);
+          const float den = 1.f / (wa + wb);
+          a_acc = wa * den;
+          a_new = wb * den * inv;
+          lse_out = mx + logf(wa + wb);
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < kD / 16; ++c) {
         uint32_t r[16];
@@ -571,13 +588,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (write_o) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(orow + 16 * c + e) =
-                make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                            __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+          for (int e = 0; e < 16; e += 4) {
+            float4 v = make_float4(__uint_as_float(r[e]) * a_new, __uint_as_float(r[e + 1]) * a_new,
+                                   __uint_as_float(r[e + 2]) * a_new, __uint_as_float(r[e + 3]) * a_new);
+            if (a_acc != 0.f) {
+              const float4 o0 = *reinterpret_cast<const float4*>(orow + 16 * c + e);
+              v.x += a_acc * o0.x;
+              v.y += a_acc * o0.y;
+              v.z += a_acc * o0.z;
+              v.w += a_acc * o0.w;
+            }
+            *reinterpret_cast<float4*>(orow + 16 * c + e) = v;
+          }
         }
       }
-      if (valid) p.out_lse[ro] = lse;
+      if (valid && (!x.accumulate || write_o)) p.out_lse[ro] = lse_out;
     }
   }
 

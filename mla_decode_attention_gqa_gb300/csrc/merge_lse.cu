@@ -90,7 +90,40 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ in
   if (lane == 0) out_lse[out_row] = (den > 0.f) ? m + logf(den) : -INFINITY;
 }
 
+// Two-way merge in place: (acc_o, acc_lse) <- merge((acc_o, acc_lse), (in_o, in_lse)), the
+// same formula as above for two fragments; one warp per row, 4 columns per lane per pass.
+__global__ void __launch_bounds__(256) merge_into_kernel(float* __restrict__ acc_o, float* __restrict__ acc_lse,
+                                                         const float* __restrict__ in_o,
+                                                         const float* __restrict__ in_lse, int64_t R, int32_t dv) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const float la = acc_lse[row], lb = in_lse[row];
+  const float m = fmaxf(la, lb);
+  if (m == -INFINITY) return;  // neither has seen a token: acc stays o = 0, lse = -inf
+  const float wa = (la == -INFINITY) ? 0.f : __expf(la - m);
+  const float wb = (lb == -INFINITY) ? 0.f : __expf(lb - m);
+  const float inv = 1.f / (wa + wb);
+  float* ao = acc_o + row * dv;
+  const float* bo = in_o + row * dv;
+  for (int d = lane * 4; d < dv; d += 128) {
+    const float4 x = (wa != 0.f) ? *reinterpret_cast<const float4*>(ao + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 y = (wb != 0.f) ? *reinterpret_cast<const float4*>(bo + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(ao + d) = make_float4((wa * x.x + wb * y.x) * inv, (wa * x.y + wb * y.y) * inv,
+                                                     (wa * x.z + wb * y.z) * inv, (wa * x.w + wb * y.w) * inv);
+  }
+  __syncwarp();
+  if (lane == 0) acc_lse[row] = m + logf(wa + wb);
+}
+
 }  // namespace
+
+cudaError_t launch_merge_into(float* acc_o, float* acc_lse, const float* in_o, const float* in_lse, int64_t R,
+                              int32_t dv, cudaStream_t stream) {
+  if (R <= 0) return cudaSuccess;
+  merge_into_kernel<<<static_cast<unsigned int>((R + 7) / 8), 256, 0, stream>>>(acc_o, acc_lse, in_o, in_lse, R, dv);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, int32_t g_out, int64_t R, int32_t dv,
                          void* out, bool out_bf16, float* out_lse, cudaStream_t stream) {

@@ -94,6 +94,9 @@ struct TcAttnExtra {
   int32_t fused;
   void* out_bf16;
   float* out_lse;
+  // partial mode with one split: merge the result into the running (out_o, out_lse) held
+  // there already instead of overwriting it (a pass-KV ring step)
+  int32_t accumulate = 0;
 };
 int tc_attn_rows_per_cta();
 int tc_attn_kv_tile();  // tokens per K/V tile = rows of the K/V tensor-map box
@@ -113,6 +116,9 @@ cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, f
 
 // Merge n_in partials per output group: in_o [G_out][n_in][R][dv], in_lse [G_out][n_in][R]
 // -> out [G_out][R][dv] (fp32 or bf16) and out_lse [G_out][R].
+// acc <- exact two-way LSE merge of acc and in (rows of dv fp32 values, lse per row).
+cudaError_t launch_merge_into(float* acc_o, float* acc_lse, const float* in_o, const float* in_lse, int64_t R,
+                              int32_t dv, cudaStream_t stream);
 cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, int32_t g_out, int64_t R,
                          int32_t dv, void* out, bool out_bf16, float* out_lse, cudaStream_t stream);
 

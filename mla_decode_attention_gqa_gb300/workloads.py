@@ -62,6 +62,7 @@ class Workload:
     cp_rank: int = 0            # the emulated rank whose query chunk is computed
     paged: bool = False         # also store the cache as pages with a block table
     block_len: int = 64         # tokens per page
+    ring_steps: bool = False    # run as n_split pass-KV ring steps, one KV block per call
 
     @property
     def scale(self) -> float:
@@ -130,8 +131,12 @@ HELIX_DENSE_128K_PAGED = replace(HELIX_DENSE_128K, name="helix_dense_decode_s128
 MLA_ABSORBED_PAGED = replace(MLA_ABSORBED, name="mla_absorbed_decode_s32k_paged64", paged=True, block_len=64,
                              seed=1008)
 
+# The ring prefill chunk as 8 pass-KV ring steps: each step's 4096-token KV block in its
+# own buffer, merged into a running output (attn_ring_step).
+RING_PREFILL_STEPS = replace(RING_PREFILL, name="ring_prefill_steps_8x4096", ring_steps=True, seed=1009)
+
 WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL, RING_PREFILL_ZIGZAG,
-             RING_PREFILL_STRIPED, HELIX_DENSE_128K_PAGED, MLA_ABSORBED_PAGED]
+             RING_PREFILL_STRIPED, HELIX_DENSE_128K_PAGED, MLA_ABSORBED_PAGED, RING_PREFILL_STEPS]
 
 
 def scaled(w: Workload, **kw) -> Workload:

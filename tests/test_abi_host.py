@@ -172,3 +172,15 @@ def test_position_arguments_are_checked_before_any_device_access():
     mla = _desc(Hq=128, Hkv=1, dk=576, dv=512, q_strides=(128 * 576, 128 * 576, 576),
                 k_strides=(1024 * 576, 1024 * 576, 576), v_strides=(1024 * 576, 1024 * 576, 576))
     assert call(mla, FAKE, FAKE) == skv.SKV_EUNSUPPORTED
+
+
+def test_ring_step_arguments_are_checked():
+    lib = skv.load_library()
+    d = _desc()
+    n = ctypes.c_size_t(0)
+    assert lib.attn_ring_step_workspace_size(ctypes.byref(d), ctypes.byref(n)) == skv.SKV_OK and n.value > 0
+    st = lib.attn_ring_step(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, 0, 0, None, FAKE, FAKE, n.value, None)
+    assert st == skv.SKV_EINVAL  # no o_acc
+    st = lib.attn_ring_step(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, 0, 0, FAKE, FAKE, None, 0, None)
+    assert st == skv.SKV_EWORKSPACE  # a later step needs its workspace
+    assert lib.attn_ring_step_workspace_size(ctypes.byref(_desc(B=0)), ctypes.byref(n)) == skv.SKV_EINVAL
