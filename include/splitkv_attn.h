@@ -105,6 +105,19 @@ skv_status splitkv_device_error(uint32_t* code);
 skv_status splitkv_device_error_detail(uint32_t* record);
 
 /*
+ * Kernel timing.  splitkv_kernel_timing(1) clears the record and makes every later call of
+ * this library, from this host thread, record a pair of CUDA events (owned by the library)
+ * on the call's stream immediately before and after its attention kernel -- the split-KV
+ * partial / tensor-core kernel, not the merge -- so that the kernel's own device time can
+ * be read while a caller times whole calls; splitkv_kernel_timing(0) stops recording.
+ * splitkv_kernel_timing_read waits for the recorded events and returns the summed kernel
+ * time in milliseconds and the number of kernel launches recorded since the last enable
+ * (at most 4096 per enable; later launches are not recorded).  SKV_ECUDA on event errors.
+ */
+skv_status splitkv_kernel_timing(int32_t enable);
+skv_status splitkv_kernel_timing_read(float* total_ms, int32_t* launches);
+
+/*
  * attn_partial -- one partial attention output per split.
  *
  *   q            bf16, logical [B][Tq][Hq][dk] with desc->q_strides

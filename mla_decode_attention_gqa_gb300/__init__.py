@@ -33,6 +33,8 @@ EXPORTED_SYMBOLS = (
     "splitkv_last_error",
     "splitkv_device_error",
     "splitkv_device_error_detail",
+    "splitkv_kernel_timing",
+    "splitkv_kernel_timing_read",
     "attn_partial_workspace_size",
     "attn_partial",
     "attn_merge_lse",
@@ -90,6 +92,10 @@ def _load():
     lib.splitkv_device_error.restype = I32
     lib.splitkv_device_error_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.splitkv_device_error_detail.restype = I32
+    lib.splitkv_kernel_timing.argtypes = [I32]
+    lib.splitkv_kernel_timing.restype = I32
+    lib.splitkv_kernel_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I32P]
+    lib.splitkv_kernel_timing_read.restype = I32
     for name in ("attn_partial_workspace_size", "gqa_decode_attn_workspace_size"):
         f = getattr(lib, name)
         f.argtypes = [D, I32P, I32, ctypes.POINTER(SZ)]
@@ -479,7 +485,22 @@ def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=
     return o_acc, lse_acc
 
 
+def kernel_timing(enable):
+    """Start (True: clears the record) or stop recording the attention kernels' own device time."""
+    _check(_lib.splitkv_kernel_timing(1 if enable else 0))
+
+
+def kernel_timing_read():
+    """(total milliseconds, launches) of the attention kernels recorded since timing was enabled."""
+    ms = ctypes.c_float(0.0)
+    n = ctypes.c_int32(0)
+    _check(_lib.splitkv_kernel_timing_read(ctypes.byref(ms), ctypes.byref(n)))
+    return float(ms.value), int(n.value)
+
+
 __all__ = [
+    "kernel_timing",
+    "kernel_timing_read",
     "attn_ring_step",
     "attn_partial",
     "attn_partial_paged",

@@ -89,6 +89,31 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn(cudaError_t* err) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ------------------------------------------------------------------ kernel timing
+
+// Events around the attention kernel of each call while timing is on (host-thread state;
+// the events are created on first use, on the device current at that time).
+struct KernelTiming {
+  static constexpr int kMax = 4096;
+  bool on = false;
+  int n = 0;
+  cudaEvent_t ev[2 * kMax] = {};
+};
+thread_local KernelTiming t_timing;
+
+cudaError_t timing_mark(bool after, cudaStream_t stream) {
+  KernelTiming& t = t_timing;
+  if (!t.on || t.n >= KernelTiming::kMax) return cudaSuccess;
+  cudaEvent_t& e = t.ev[2 * t.n + (after ? 1 : 0)];
+  if (!e) {
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return r;
+  }
+  cudaError_t r = cudaEventRecord(e, stream);
+  if (after) ++t.n;
+  return r;
+}
+
 // ------------------------------------------------------------------ plan of a call
 
 struct Plan {
@@ -403,7 +428,9 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
   if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kv_box, pg)) != SKV_OK) return st;
   if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kv_box, pg)) != SKV_OK) return st;
   const int64_t n_items = static_cast<int64_t>(d->B) * d->Hkv * (fused ? 1 : n_split) * pl.m_tiles;
-  cudaError_t e = launch_tc_attn(p, x, tmq, tmk, tmv, n_items, stream);
+  cudaError_t e = timing_mark(false, stream);
+  if (e == cudaSuccess) e = launch_tc_attn(p, x, tmq, tmk, tmv, n_items, stream);
+  if (e == cudaSuccess) e = timing_mark(true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core attention launch");
   return SKV_OK;
 }
@@ -430,19 +457,25 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
       x.fused = 0;
       x.out_bf16 = nullptr;
       x.out_lse = nullptr;
-      e = launch_mla_tc(p, x, tmq, tmk, pl.n_items, stream);
+      e = timing_mark(false, stream);
+      if (e == cudaSuccess) e = launch_mla_tc(p, x, tmq, tmk, pl.n_items, stream);
+      if (e == cudaSuccess) e = timing_mark(true, stream);
       if (e != cudaSuccess) return cuda_fail(e, "MLA tensor-core attention launch");
       return SKV_OK;
     }
     // one latent map serves K (all 576 columns) and V (its first 512 columns)
     if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kMlaTileN, pg)) != SKV_OK) return st;
-    e = launch_mla_partial(p, tmk, pl.n_items, stream);
+    e = timing_mark(false, stream);
+    if (e == cudaSuccess) e = launch_mla_partial(p, tmk, pl.n_items, stream);
+    if (e == cudaSuccess) e = timing_mark(true, stream);
     if (e != cudaSuccess) return cuda_fail(e, "MLA partial attention launch");
     return SKV_OK;
   }
   if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, kTileN, pg)) != SKV_OK) return st;
   if ((st = encode_kv_map(&tmv, v, d, d->v_strides, d->dv, kTileN, pg)) != SKV_OK) return st;
-  e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
+  e = timing_mark(false, stream);
+  if (e == cudaSuccess) e = launch_gqa_partial(pl.variant, p, tmk, tmv, pl.n_items, stream);
+  if (e == cudaSuccess) e = timing_mark(true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
   return SKV_OK;
 }
@@ -452,6 +485,28 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
 extern "C" {
 
 int32_t splitkv_version(void) { return (1 << 16) | 0; }
+
+skv_status splitkv_kernel_timing(int32_t enable) {
+  t_timing.on = enable != 0;
+  if (t_timing.on) t_timing.n = 0;
+  return SKV_OK;
+}
+
+skv_status splitkv_kernel_timing_read(float* total_ms, int32_t* launches) {
+  if (!total_ms || !launches) return fail(SKV_EINVAL, "total_ms and launches must be non-NULL");
+  float sum = 0.f;
+  for (int i = 0; i < t_timing.n; ++i) {
+    cudaError_t e = cudaEventSynchronize(t_timing.ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel timing event");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, t_timing.ev[2 * i], t_timing.ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel timing elapsed");
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = t_timing.n;
+  return SKV_OK;
+}
 
 const char* splitkv_last_error(void) { return t_last_error.c_str(); }
 
