@@ -83,7 +83,8 @@ __device__ __forceinline__ void tma_load_4d_nohint(void* dst, const CUtensorMap*
 
 
 // POS: the causal rule comes from position arrays (tokens stored out of sequence order)
-template <bool POS>
+// PAGED: K/V live in pages with a block table (read in 64-token halves)
+template <bool POS, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attn_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
                    const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -222,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // a paged cache is read in 64-token halves (a page holds a multiple of 64 tokens),
       // each half's page read one tile ahead, behind the stage wait
-      const bool paged = p.block_table != nullptr;
       // (a half that starts at or past S_max only holds masked tokens: it reuses the first
       // half's page instead of reading past the sequence's block-table row)
       auto pages_of = [&](int t, int& a, int& c) {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         c = (t + kTN / 2 < p.S_max) ? kv_page_of(p, b, t + kTN / 2) : a;
       };
       int pg0 = 0, pg1 = 0;
-      if (paged) pages_of((tile_begin + tile_of(0)) * kTN, pg0, pg1);
+      if constexpr (PAGED) pages_of((tile_begin + tile_of(0)) * kTN, pg0, pg1);
       int issued = 0;
       for (int i = 0; i < n_used; ++i) {
         const int s = i % kNStage;
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->kv_full[s], kStageBytes);
         uint8_t* st = smem + kOffRing + s * kStageBytes;
         const int tok = (tile_begin + tile_of(i)) * kTN;
-        if (!paged) {
+        if constexpr (!PAGED) {
           for (int bx = 0; bx < 2; ++bx) {
             tma_load_4d_nohint(st + bx * kKVBoxBytes, &tmk, &bars->kv_full[s], bx * 64, tok, g, b);
             tma_load_4d_nohint(st + kKTileBytes + bx * kKVBoxBytes, &tmv, &bars->kv_full[s], bx * 64, tok, g, b);
@@ -620,17 +620,26 @@ cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const C
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_attn_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_attn_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_attn_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   if (n_items <= 0) return cudaSuccess;
-  if (p.k_pos)
-    tc_attn_kernel<true><<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  const unsigned int grid = static_cast<unsigned int>(n_items);
+  if (p.k_pos && p.block_table)
+    tc_attn_kernel<true, true><<<grid, kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  else if (p.k_pos)
+    tc_attn_kernel<true, false><<<grid, kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+  else if (p.block_table)
+    tc_attn_kernel<false, true><<<grid, kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
   else
-    tc_attn_kernel<false><<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
+    tc_attn_kernel<false, false><<<grid, kThreads, kSmem, stream>>>(p, x, tmq, tmk, tmv);
   return cudaGetLastError();
 }
 

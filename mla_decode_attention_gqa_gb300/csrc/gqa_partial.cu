@@ -107,7 +107,10 @@ __device__ __forceinline__ uint32_t half_mask(bool lo, bool hi) {
   return (lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u);
 }
 
-template <class C>
+// PAGED: K/V live in pages with a block table; POS: the causal rule comes from position
+// arrays.  Separate instantiations, so the plain kernels carry none of that code (a
+// runtime test of either cost the fp8 decode 4 %).
+template <class C, bool PAGED, bool POS>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     gqa_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
@@ -164,9 +167,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       const uint64_t pol = l2_policy_evict_first();
-      const bool paged = p.block_table != nullptr;
       // paged cache: the next tile's page is read one tile ahead, behind the stage wait
-      int page_next = paged ? kv_page_of(p, b, tile_begin * TN) : b;
+      int page_next = b;
+      if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * TN);
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % NSTAGE;
@@ -177,8 +180,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         uint8_t* vs = ks + C::TILE_BYTES;
         const int tok = (tile_begin + i) * TN;
         const int outer = page_next;  // page (paged) or sequence
-        const int row = paged ? tok % p.block_len : tok;
-        if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + TN);
+        int row = tok;
+        if constexpr (PAGED) {
+          row = tok % p.block_len;
+          if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + TN);
+        }
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
           tma_load_4d(ks + bx * C::BOX_BYTES, &tmk, fb, bx * C::BOX_ELEMS, row, g, outer, pol);
@@ -205,9 +211,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int64_t hz0 = p.causal_offset + tq0, hz1 = p.causal_offset + tq1;
   const int64_t hz_min = p.causal_offset + (m0 + wm * 16) / p.G;
   // tokens stored out of sequence order: visible iff k_pos[t] <= q_pos[row]
-  const int32_t* kpos_b = p.k_pos ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
-  const int qp0 = p.q_pos ? __ldg(p.q_pos + b * p.Tq + tq0) : 0;
-  const int qp1 = p.q_pos ? __ldg(p.q_pos + b * p.Tq + tq1) : 0;
+  const int32_t* kpos_b = POS ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
+  const int qp0 = POS ? __ldg(p.q_pos + b * p.Tq + tq0) : 0;
+  const int qp1 = POS ? __ldg(p.q_pos + b * p.Tq + tq1) : 0;
 
   // ---- Q fragments (A operand, 16 rows x D): registers for bf16, shared memory for fp8
   uint32_t qa[C::FP8 ? 1 : D / 16][4];
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int t0 = (tile_begin + i) * TN;
     float ksc = 1.f, vsc = 1.f;
     if constexpr (C::FP8) {
-      if (p.block_table == nullptr) {
+      if constexpr (!PAGED) {
         ksc = __ldg(kscale_row + t0 / p.scale_block);
         vsc = __ldg(vscale_row + t0 / p.scale_block);
       } else {
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     // ---- scale, mask, online softmax
     const float sl = p.scale_log2 * ksc;
     const bool in_range = (t0s >= r_lo) && (t0s + NS <= r_hi);
-    const bool need_mask = kpos_b != nullptr || !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
+    const bool need_mask = POS || !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NS / 8; ++nt) {
@@ -350,8 +356,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         if (need_mask) {
           const int tok = t0s + 8 * nt + 2 * tq + (e & 1);
           const int64_t hz = (e < 2) ? hz0 : hz1;
-          const bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz &&
-                          (kpos_b == nullptr || __ldg(kpos_b + tok) <= ((e < 2) ? qp0 : qp1));
+          bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
+          if constexpr (POS) ok = ok && __ldg(kpos_b + tok) <= ((e < 2) ? qp0 : qp1);
           x = ok ? x : -INFINITY;
         }
         sc[nt][e] = x;
@@ -616,12 +622,26 @@ cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUt
                        cudaStream_t stream) {
   static bool attr_done = false;  // per variant; set once per process
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_partial_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
+    const void* fns[4] = {reinterpret_cast<const void*>(gqa_partial_kernel<C, false, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, false, true>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, true>)};
+    for (const void* f : fns) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      if (e != cudaSuccess) return e;
+    }
     attr_done = true;
   }
   if (n_items <= 0) return cudaSuccess;
-  gqa_partial_kernel<C><<<static_cast<unsigned int>(n_items), C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  const unsigned int grid = static_cast<unsigned int>(n_items);
+  if (p.block_table && p.k_pos)
+    gqa_partial_kernel<C, true, true><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  else if (p.block_table)
+    gqa_partial_kernel<C, true, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  else if (p.k_pos)
+    gqa_partial_kernel<C, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  else
+    gqa_partial_kernel<C, false, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
   return cudaGetLastError();
 }
 

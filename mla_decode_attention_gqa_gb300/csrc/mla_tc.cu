@@ -153,6 +153,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
   return __all_sync(0xffffffffu, ok);
 }
 
+// PAGED: the latent lives in pages with a block table (kept out of the contiguous
+// instantiation: the extra producer code alone slowed it by a tenth)
+template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
                   const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tml) {
@@ -241,8 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_4d_plain(smem + (bx < kQTmemBoxes ? bx * kQBoxBytes : kOffQRope), &tmq, &bars->q_full, bx * 64, 0,
                             t_start, b);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
-        const bool paged = p.block_table != nullptr;
-        int page_next = paged ? kv_page_of(p, b, tile_begin * kTN) : b;  // read one tile ahead
+        int page_next = b;  // paged: the next tile's page, read one tile ahead
+        if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * kTN);
         int issued = 0;
         for (int i = 0; i < n_tiles && ok; ++i) {
           const int s = i % kNStage0;
@@ -252,8 +255,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * kStage0Bytes;
           const int tok = (tile_begin + i) * kTN;
           const int outer = page_next;
-          const int row = paged ? tok % p.block_len : tok;
-          if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
+          int row = tok;
+          if constexpr (PAGED) {
+            row = tok % p.block_len;
+            if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
+          }
           for (int bx = 0; bx < kKBoxes; ++bx)
             tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, row, 0, outer);
           issued = i + 1;
@@ -469,8 +475,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       if (lane == 0 && n_tiles > 0) {
         tma_prefetch_desc(&tml);
-        const bool paged = p.block_table != nullptr;
-        int page_next = paged ? kv_page_of(p, b, tile_begin * kTN) : b;  // read one tile ahead
+        int page_next = b;  // paged: the next tile's page, read one tile ahead
+        if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * kTN);
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
           const int s = i % kNStage1;
@@ -480,8 +486,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * kStage1Bytes;
           const int tok = (tile_begin + i) * kTN;
           const int outer = page_next;
-          const int row = paged ? tok % p.block_len : tok;
-          if (paged && i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
+          int row = tok;
+          if constexpr (PAGED) {
+            row = tok % p.block_len;
+            if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
+          }
           for (int bx = 0; bx < kVBoxes; ++bx)
             tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row, 0, outer);
           issued = i + 1;
@@ -658,12 +667,17 @@ cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CU
                           const CUtensorMap& tml, int64_t n_items, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   if (n_items <= 0) return cudaSuccess;
-  mla_tc_kernel<<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);
+  if (p.block_table)
+    mla_tc_kernel<true><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);
+  else
+    mla_tc_kernel<false><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);
   return cudaGetLastError();
 }
 
