@@ -68,7 +68,9 @@ def config_of(w, ws=1):
             "parallelism": f"replicas x{ws}",
             **({"layout": w.layout, "query_rank": w.cp_rank} if w.layout != "contiguous" else {}),
             **({"paged": True, "block_len": w.block_len} if w.paged else {}),
-            **({"ring_steps": w.n_split, "step_api": "attn_ring_step"} if w.ring_steps else {})}
+            **({"ring_steps": w.n_split, "step_api": "attn_ring_step"} if w.ring_steps else {}),
+            **({"passq_ranks": w.passq_ranks, "decode_tokens": w.passq_decode_tokens,
+                "step_api": "gqa_decode_attn_passq"} if w.passq_ranks else {})}
 
 
 def workload_by_name(name):
@@ -250,6 +252,8 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
         pos = {"q_positions": [W.layout_positions(w.layout, w.S, w.n_split, w.cp_rank)],
                "k_positions": [[p for r in range(w.n_split) for p in W.layout_positions(w.layout, w.S, w.n_split, r)]]}
     done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
+    if w.passq_ranks:
+        return _oracle_sample_passq(w, gen, budget_s, max_groups)
     while elapsed < budget_s and (max_groups is None or groups < max_groups):
         S = w.S
         q = torch.randn((1, w.Tq, G, w.dk), generator=gen).to(torch.bfloat16)
@@ -276,6 +280,36 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
     return done_bytes, elapsed, groups, tokens
 
 
+def _oracle_sample_passq(w, gen, budget_s, max_groups):
+    """Pass-Q: one (request, KV head) group of S tokens spread over the N ranks as the
+    workload spreads them, its query block padded with N - 1 empty requests (the padding
+    of a batch of one to the group size), run through the oracle's ring, return and merge;
+    returns like oracle_sample."""
+    import numpy as np
+    import oracle
+
+    N, G = w.passq_ranks, w.Hq // w.Hkv
+    lens = W.passq_shard_lens(W.scaled(w, B=N), [w.S] + [0] * (N - 1))
+    S_loc = max(lens[r][0] for r in range(N))
+    done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
+    while elapsed < budget_s and (max_groups is None or groups < max_groups):
+        q = torch.randn((N, 1, G, w.dk), generator=gen).to(torch.bfloat16)
+        k = torch.randn((N, 1, S_loc, w.dk), generator=gen).to(torch.bfloat16)  # request 0 on each rank
+        v = torch.randn((N, 1, S_loc, w.dv), generator=gen).to(torch.bfloat16)
+        t0 = time.perf_counter()
+        qf = oracle.bf16_bits_to_f64(q.view(torch.int16).numpy())
+        kf = np.zeros((N, N, 1, S_loc, w.dk))  # the empty requests' rows are never touched
+        vf = np.zeros((N, N, 1, S_loc, w.dv))
+        kf[:, 0] = oracle.bf16_bits_to_f64(k.view(torch.int16).numpy())
+        vf[:, 0] = oracle.bf16_bits_to_f64(v.view(torch.int16).numpy())
+        oracle.passq_decode(qf, kf, vf, lens, w.scale)
+        elapsed += time.perf_counter() - t0
+        done_bytes += RL.kv_bytes(1, w.dk, w.dv, "bf16", [w.S], [[0, w.S]])
+        groups += 1
+        tokens += w.S
+    return done_bytes, elapsed, groups, tokens
+
+
 def reference_arm(args, w, ws, rank):
     if rank != 0:
         return
@@ -288,7 +322,8 @@ def reference_arm(args, w, ws, rank):
             steps.append(s)
             bytes_total += b
             secs_total += s
-            sample = f"1 (batch, KV head) group of {t} tokens x {w.Tq} rows x {w.Hq // w.Hkv} heads per step"
+            sample = (f"{g} (batch, KV head) group(s) of {t // max(g, 1)} tokens x {w.Tq} rows x {w.Hq // w.Hkv} "
+                      f"heads per step" + (f", through the {w.passq_ranks}-rank pass-Q ring" if w.passq_ranks else ""))
     gbs = bytes_total / secs_total / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
@@ -316,7 +351,13 @@ def ours_arm(args, w, ws, rank, local):
     kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, inp["seq_lens_host"], bounds, mla=w.mla,
                            scale_block=w.scale_block)
     positional = inp["q_pos"] is not None  # zigzag / striped storage: the *_pos entry point
-    if positional:
+    if w.passq_ranks:  # pass-Q: every rank's resident shard of every request, once
+        flat = [n for r in inp["shard_lens_host"] for n in r]
+        S_loc = inp["k_shards"].shape[2]
+        kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, flat, [[0, S_loc]] * len(flat),
+                               scale_block=w.scale_block)
+        flops = RL.attn_flops(1, w.Hq, w.dk, w.dv, flat, [[0, S_loc]] * len(flat))
+    elif positional:
         flops = RL.attn_flops_positions(w.Hq, w.dk, w.dv, inp["seq_lens_host"], bounds, inp["q_pos_host"],
                                         inp["k_pos_host"])
     else:
@@ -345,7 +386,11 @@ def ours_arm(args, w, ws, rank, local):
                                softmax_scale=w.scale)
 
     def step():
-        if w.ring_steps:
+        if w.passq_ranks:
+            skv.gqa_decode_attn_passq(inp["q"], inp["k_shards"], inp["v_shards"], inp["shard_lens"],
+                                      k_scale=inp["k_shard_scale"], v_scale=inp["v_shard_scale"],
+                                      softmax_scale=w.scale, scale_block=w.scale_block, out=out, lse=lse)
+        elif w.ring_steps:
             ring_run(inp["q"], ring_blocks)
         elif w.paged:
             skv.gqa_decode_attn_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["seq_lens"], bounds,
@@ -401,6 +446,8 @@ def ours_arm(args, w, ws, rank, local):
         # the MLA value cache is a view of the latent (k): it is copied once, as k
         if w.ring_steps:
             keys = ("q",)
+        elif w.passq_ranks:
+            keys = ("q", "k_shards", "v_shards", "k_shard_scale", "v_shard_scale", "shard_lens")
         elif w.paged:
             keys = ("q", "k_pages", "seq_lens", "block_table") + (() if w.mla else ("v_pages",)) + (
                 ("k_scale_pages", "v_scale_pages") if w.kv_dtype != "bf16" else ())
@@ -433,7 +480,12 @@ def ours_arm(args, w, ws, rank, local):
                     dev_bufs[k2].copy_(t, non_blocking=True)
             e2e_kw = dict(k_scale=dev_bufs.get("k_scale"), v_scale=dev_bufs.get("v_scale"), softmax_scale=w.scale,
                           scale_block=w.scale_block, out=out, lse=lse)
-            if w.ring_steps:
+            if w.passq_ranks:
+                skv.gqa_decode_attn_passq(dev_bufs["q"], dev_bufs["k_shards"], dev_bufs["v_shards"],
+                                          dev_bufs["shard_lens"], k_scale=dev_bufs["k_shard_scale"],
+                                          v_scale=dev_bufs["v_shard_scale"], softmax_scale=w.scale,
+                                          scale_block=w.scale_block, out=out, lse=lse)
+            elif w.ring_steps:
                 ring_run(dev_bufs["q"], [(dev_bufs[f"k{j}"], dev_bufs[f"v{j}"], dev_bufs[f"s{j}"])
                                          for j in range(w.n_split)])
                 out.copy_(o_acc)  # the final output (bf16) read back like the other workloads'

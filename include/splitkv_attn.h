@@ -294,6 +294,48 @@ skv_status attn_ring_step(const skv_desc* desc, const void* q, const void* k_blo
                           int32_t first, float* o_acc, float* lse_acc, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/*
+ * gqa_decode_attn_passq -- pass-Q decode over a context-parallel group of n_ranks ranks,
+ * every rank emulated on this GPU ("Context Parallelism for Scalable Million-Token
+ * Inference", sections "Pass-Q keeps KV stationary for cache-heavy turns" and "Pass-Q
+ * decode protects capacity but can hurt TTIT").  Each rank keeps its own resident shard of
+ * every request's KV cache; the one-token queries travel the ring with their batch ids and
+ * attend over the shard of whichever rank they reach; the partials are permuted back to the
+ * queries' owners (the All-to-All) and merged exactly by their LSE.  The result is the
+ * attention of each request's query over the union of its shards.
+ *
+ *   desc        desc->B = requests, a multiple of n_ranks (rank r owns the queries of
+ *               requests [r * B / n_ranks, (r + 1) * B / n_ranks): pad the batch to a
+ *               multiple of the group size); desc->Tq = 1; desc->S_max = capacity of one
+ *               rank's shard of one request; GQA shapes only (bf16 d = 64 / 128, fp8
+ *               d = 128); desc strides as for attn_partial, k/v strides of one shard row
+ *   n_ranks     ranks in the group, >= 1
+ *   q           DEVICE bf16 [B][1][Hq][dk] with desc->q_strides
+ *   k_shards, v_shards  DEVICE [n_ranks * B][Hkv][S_max][d] with desc->k/v_strides: row
+ *               r * B + b is rank r's resident shard of request b.  The order of the tokens
+ *               inside a shard is free (the new token follows every cached one, so it sees
+ *               all of them); tokens past the shard's length are never read
+ *   k_scale, v_scale  fp8 only: DEVICE fp32 [n_ranks * B][Hkv][S_max / scale_block]
+ *   shard_lens  DEVICE int32 [n_ranks][B]: resident tokens of request b on rank r, 0 allowed
+ *   out, lse    DEVICE bf16 [B][1][Hq][dv] and fp32 [B][1][Hq] (contiguous); a request
+ *               with no resident token anywhere gets out = 0, lse = -inf
+ *   workspace   DEVICE, gqa_decode_attn_passq_workspace_size() bytes, 256-byte aligned:
+ *               the exchange buffer of fp32 partials [owner][source rank][part][B /
+ *               n_ranks][Hq][dv] and their LSEs
+ * Schedule: rank k at ring step s (s = 0 .. n_ranks - 1) holds the query block that started
+ * on rank (k - s) mod n_ranks and writes its partial to that owner's slot from rank k.  One
+ * partial launch covers every rank and step; one merge launch covers the exchange and the
+ * merge.  Caller owns every buffer; the library allocates nothing.
+ * Errors: as gqa_decode_attn, plus SKV_EINVAL for n_ranks < 1, B not a multiple of n_ranks or
+ * n_ranks * B above 1024; SKV_EUNSUPPORTED for Tq != 1 or the MLA latent shape.
+ */
+skv_status gqa_decode_attn_passq_workspace_size(const skv_desc* desc, int32_t n_ranks, size_t* bytes);
+
+skv_status gqa_decode_attn_passq(const skv_desc* desc, int32_t n_ranks, const void* q, const void* k_shards,
+                                 const void* v_shards, const float* k_scale, const float* v_scale,
+                                 const int32_t* shard_lens, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

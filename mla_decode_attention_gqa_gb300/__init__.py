@@ -10,6 +10,8 @@ Entry points (same names as the C ABI):
   attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out_partial, lse_partial)
   attn_merge_lse(out_partials, lse_partials) -> (out, lse)
   gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out, lse)
+  gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, ...) -> (out, lse)
+plus the position-masked (_pos), paged (_paged) and pass-KV ring-step variants.
 """
 
 import ctypes
@@ -47,6 +49,8 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attn_paged",
     "attn_ring_step_workspace_size",
     "attn_ring_step",
+    "gqa_decode_attn_passq_workspace_size",
+    "gqa_decode_attn_passq",
 )
 
 # Every symbol declared in include/splitkv_attn_selftest.h (hardware self-tests).
@@ -121,6 +125,10 @@ def _load():
     lib.attn_ring_step_workspace_size.restype = I32
     lib.attn_ring_step.argtypes = [D, P, P, P, P, P, P, I64, I32, P, P, P, SZ, P]
     lib.attn_ring_step.restype = I32
+    lib.gqa_decode_attn_passq_workspace_size.argtypes = [D, I32, ctypes.POINTER(SZ)]
+    lib.gqa_decode_attn_passq_workspace_size.restype = I32
+    lib.gqa_decode_attn_passq.argtypes = [D, I32, P, P, P, P, P, P, P, P, P, SZ, P]
+    lib.gqa_decode_attn_passq.restype = I32
     return lib
 
 
@@ -485,6 +493,41 @@ def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=
     return o_acc, lse_acc
 
 
+def gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, k_scale=None, v_scale=None, softmax_scale=None,
+                          scale_block=64, out=None, lse=None, workspace=None):
+    """Pass-Q decode over the N = shard_lens.shape[0] ranks of a context-parallel group,
+    emulated on this GPU: q bf16 [B,1,Hq,dk] (rank r owns requests [r*B/N, (r+1)*B/N));
+    k_shards / v_shards [N*B,Hkv,S_loc,d] (row r*B+b: rank r's resident shard of request
+    b); shard_lens int32 [N,B]; fp8 scales [N*B,Hkv,S_loc/scale_block].  Returns (out bf16
+    [B,1,Hq,dv], lse fp32 [B,1,Hq])."""
+    _require_cuda(q, k_shards, v_shards, shard_lens, k_scale, v_scale)
+    if shard_lens.dtype != torch.int32 or not shard_lens.is_contiguous() or shard_lens.dim() != 2:
+        raise ValueError("shard_lens must be contiguous int32 [n_ranks, B]")
+    n_ranks, B = shard_lens.shape
+    if k_shards.dim() != 4 or k_shards.shape[0] != n_ranks * B or v_shards.shape[0] != n_ranks * B:
+        raise ValueError("k_shards / v_shards must be [n_ranks * B, Hkv, S_loc, d]")
+    if q.dim() != 4 or q.shape[0] != B:
+        raise ValueError("q must be [B, 1, Hq, dk] with B = shard_lens.shape[1]")
+    # one shard row's description: the library steps through all n_ranks * B rows
+    d = make_desc(q, k_shards[:B], v_shards[:B], softmax_scale, scale_block)
+    for s_ in (k_scale, v_scale):
+        if s_ is not None and (s_.dtype != torch.float32 or not s_.is_contiguous()):
+            raise ValueError("scales must be contiguous float32 [n_ranks * B, Hkv, n_blocks]")
+    dev = q.device
+    if out is None:
+        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    n = ctypes.c_size_t(0)
+    _check(_lib.gqa_decode_attn_passq_workspace_size(ctypes.byref(d), n_ranks, ctypes.byref(n)))
+    nbytes = int(n.value)
+    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    _check(_lib.gqa_decode_attn_passq(ctypes.byref(d), n_ranks, _ptr(q), _ptr(k_shards), _ptr(v_shards),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(shard_lens), _ptr(out), _ptr(lse), _ptr(ws),
+                                      nbytes if workspace is None else workspace.numel(), _stream()))
+    return out, lse
+
+
 def kernel_timing(enable):
     """Start (True: clears the record) or stop recording the attention kernels' own device time."""
     _check(_lib.splitkv_kernel_timing(1 if enable else 0))
@@ -502,6 +545,7 @@ __all__ = [
     "kernel_timing",
     "kernel_timing_read",
     "attn_ring_step",
+    "gqa_decode_attn_passq",
     "attn_partial",
     "attn_partial_paged",
     "gqa_decode_attn_paged",

@@ -438,11 +438,16 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
 skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const void* k, const void* v,
                        const float* ks, const float* vs, const int32_t* seq_lens, const int32_t* bounds,
                        int32_t n_split, int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos,
-                       const skv_paged* pg, float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream) {
+                       const skv_paged* pg, float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream,
+                       int32_t ring_n = 0) {
   static thread_local PartialParams p;  // ~8 KB: keep it off the stack
   skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, q_pos, k_pos, pg,
                               out_o, out_lse, zero_empty);
   if (st != SKV_OK) return st;
+  if (ring_n > 0) {  // pass-Q: d->B counts (rank, ring step, slot) work rows
+    p.ring_n = ring_n;
+    p.ring_bq = d->B / (ring_n * ring_n);
+  }
   CUtensorMap tmk, tmv;
   cudaError_t e;
   if (pl.mla) {
@@ -895,3 +900,74 @@ extern "C" skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* 
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return SKV_OK;
 }
+
+// ------------------------------------------------------------------ pass-Q decode
+
+namespace {
+
+// A pass-Q call as one batched partial launch: the n_ranks * B work rows (rank, ring step,
+// slot) and the n_ranks * B cache rows (rank, request) share one count, every cache row is
+// one split [0, S_max) clipped to its shard length on the device.
+skv_status passq_setup(const skv_desc* d, int32_t n_ranks, skv_desc* vd, std::vector<int32_t>* bounds) {
+  if (!d) return fail(SKV_EINVAL, "desc is NULL");
+  if (n_ranks < 1) return fail(SKV_EINVAL, "n_ranks must be >= 1");
+  if (d->B <= 0 || d->B % n_ranks) return fail(SKV_EINVAL, "B must be a positive multiple of n_ranks");
+  if (static_cast<int64_t>(n_ranks) * d->B > kMaxBounds / 2) return fail(SKV_EINVAL, "n_ranks * B must be <= 1024");
+  if (is_mla_shape(d)) return fail(SKV_EUNSUPPORTED, "pass-Q decode is not supported for the MLA latent shape");
+  if (d->Tq != 1) return fail(SKV_EUNSUPPORTED, "pass-Q decode takes one query token per request (Tq = 1)");
+  *vd = *d;
+  vd->B = n_ranks * d->B;
+  const int32_t hi = static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(d->S_max, 0), INT32_MAX));
+  bounds->assign(2 * static_cast<size_t>(vd->B), 0);
+  for (int r = 0; r < vd->B; ++r) (*bounds)[2 * r + 1] = hi;
+  return validate(vd, bounds->data(), 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+skv_status gqa_decode_attn_passq_workspace_size(const skv_desc* desc, int32_t n_ranks, size_t* bytes) {
+  if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
+  skv_desc vd;
+  std::vector<int32_t> bounds;
+  skv_status st = passq_setup(desc, n_ranks, &vd, &bounds);
+  if (st != SKV_OK) return st;
+  const Plan pl = make_plan(&vd, bounds.data(), 1);
+  *bytes = ws_bytes_for(&vd, pl.n_part);
+  return SKV_OK;
+}
+
+skv_status gqa_decode_attn_passq(const skv_desc* desc, int32_t n_ranks, const void* q, const void* k_shards,
+                                 const void* v_shards, const float* k_scale, const float* v_scale,
+                                 const int32_t* shard_lens, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  skv_desc vd;
+  static thread_local std::vector<int32_t> bounds;
+  skv_status st = passq_setup(desc, n_ranks, &vd, &bounds);
+  if (st != SKV_OK) return st;
+  if ((st = validate_ptrs(&vd, q, k_shards, v_shards, k_scale, v_scale, shard_lens)) != SKV_OK) return st;
+  if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
+  if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
+  const Plan pl = make_plan(&vd, bounds.data(), 1);
+  const size_t need = ws_bytes_for(&vd, pl.n_part);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_passq_workspace_size()");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(vd.B) * vd.Tq * vd.Hq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * vd.dv * 4, 256));
+  // every rank, every ring step: partials land in the owners' exchange slots
+  st = run_partial(&vd, pl, q, k_shards, v_shards, k_scale, v_scale, shard_lens, bounds.data(), 1, SKV_NO_CAUSAL,
+                   nullptr, nullptr, nullptr, ws_o, ws_l, false, s, n_ranks);
+  if (st != SKV_OK) return st;
+  // the exchange delivered [owner][source rank][part] slabs: each owner merges its
+  // n_ranks * n_part partials per query row
+  const int64_t owner_rows = static_cast<int64_t>(desc->B / n_ranks) * desc->Tq * desc->Hq;
+  cudaError_t e = launch_merge(ws_o, ws_l, n_ranks * pl.n_part, n_ranks, owner_rows, desc->dv, out, true, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pass-Q merge launch");
+  return SKV_OK;
+}
+
+}  // extern "C"

@@ -12,6 +12,14 @@
 // (head h reads KV head h / G).  A token t is visible to query row i when it lies in
 // the range, t < seq_len[b] and t <= causal_offset + i.
 //
+// Pass-Q decode ("Context Parallelism for Scalable Million-Token Inference", sections
+// "Pass-Q keeps KV stationary for cache-heavy turns" and "Pass-Q decode protects capacity
+// but can hurt TTIT") runs through the same kernel: with ring_n ranks, each holding its
+// own resident shard of every request, one launch covers every rank's every ring step; a
+// work item decodes which query block has arrived at which rank and writes its partial
+// straight into the exchange slot of the query's owner, so the exchange and the merge
+// that follow are one merge launch.
+//
 // GB300 design:
 //   * one producer warp streams K and V tiles (64 tokens) with TMA tiled bulk-tensor
 //     copies into a multi-stage shared-memory ring (128-byte swizzle, conflict-free
@@ -107,10 +115,42 @@ __device__ __forceinline__ uint32_t half_mask(bool lo, bool hi) {
   return (lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u);
 }
 
+// Pass-Q ring (RING instantiation, ring_n > 0): work row b = (k * ring_n + s) * ring_bq + jj is rank k at ring
+// step s, holding the query block that started on rank src = (k - s) mod ring_n; its slot
+// jj carries request src * ring_bq + jj (the batch id that travels with the query), whose
+// shard on rank k is cache row k * (ring_n * ring_bq) + request.
+__device__ __forceinline__ void ring_rows(const PartialParams& p, int b, int* bq, int* bkv) {
+  const int jj = b % p.ring_bq;
+  const int ks = b / p.ring_bq;
+  const int s = ks % p.ring_n, k = ks / p.ring_n;
+  const int src = (k - s + p.ring_n) % p.ring_n;
+  *bq = src * p.ring_bq + jj;
+  *bkv = k * (p.ring_n * p.ring_bq) + *bq;
+}
+
+// Output slot of a pass-Q ring's work item: the exchange slot [owner src][from rank k]
+// [part][jj] of the query's owner (the permutation before the All-to-All, done at the
+// store); recomputed from the block index so that it holds no register through the loop.
+__device__ __forceinline__ int64_t ring_out_slot(const PartialParams& p) {
+  int64_t item = blockIdx.x / p.m_tiles;
+  const int c = static_cast<int>(item % p.n_chunk);
+  item /= p.n_chunk;
+  const int j = static_cast<int>(item % p.n_split);
+  item /= p.n_split;
+  const int b = static_cast<int>(item / p.Hkv);
+  const int part = j * p.n_chunk + c;
+  const int jj = b % p.ring_bq;
+  const int ks = b / p.ring_bq;
+  const int s = ks % p.ring_n, k = ks / p.ring_n;
+  const int src = (k - s + p.ring_n) % p.ring_n;
+  return ((static_cast<int64_t>(src) * p.ring_n + k) * (p.n_split * p.n_chunk) + part) * p.ring_bq + jj;
+}
+
 // PAGED: K/V live in pages with a block table; POS: the causal rule comes from position
-// arrays.  Separate instantiations, so the plain kernels carry none of that code (a
-// runtime test of either cost the fp8 decode 4 %).
-template <class C, bool PAGED, bool POS>
+// arrays; RING: a pass-Q ring's work rows (never with PAGED or POS).  Separate
+// instantiations, so the plain kernels carry none of that code (a runtime test of the
+// first two cost the fp8 decode 4 %, of the third 1.3 %).
+template <class C, bool PAGED, bool POS, bool RING>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     gqa_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
@@ -135,8 +175,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int g = static_cast<int>(item % p.Hkv);
   const int b = static_cast<int>(item / p.Hkv);
 
-  const int seq_len = p.seq_lens[b];
-  const int* bnd = p.bounds + b * (p.n_split + 1);
+  // bq: query row; bkv: KV row (sequence) of the cache
+  int bq = b, bkv = b;
+  if constexpr (RING) ring_rows(p, b, &bq, &bkv);
+
+  const int seq_len = p.seq_lens[bkv];
+  const int* bnd = p.bounds + bkv * (p.n_split + 1);
   int lo = max(bnd[j], 0);
   int hi = min(min(bnd[j + 1], seq_len), p.S_max);
   const int win_lo = (lo / TN) * TN + c * p.chunk_tiles * TN;
@@ -168,8 +212,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       tma_prefetch_desc(&tmv);
       const uint64_t pol = l2_policy_evict_first();
       // paged cache: the next tile's page is read one tile ahead, behind the stage wait
-      int page_next = b;
-      if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * TN);
+      int page_next = bkv;
+      if constexpr (PAGED) page_next = kv_page_of(p, bkv, tile_begin * TN);
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % NSTAGE;
@@ -183,7 +227,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         int row = tok;
         if constexpr (PAGED) {
           row = tok % p.block_len;
-          if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + TN);
+          if (i + 1 < n_tiles) page_next = kv_page_of(p, bkv, tok + TN);
         }
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
@@ -211,16 +255,16 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const int64_t hz0 = p.causal_offset + tq0, hz1 = p.causal_offset + tq1;
   const int64_t hz_min = p.causal_offset + (m0 + wm * 16) / p.G;
   // tokens stored out of sequence order: visible iff k_pos[t] <= q_pos[row]
-  const int32_t* kpos_b = POS ? p.k_pos + static_cast<int64_t>(b) * p.S_max : nullptr;
-  const int qp0 = POS ? __ldg(p.q_pos + b * p.Tq + tq0) : 0;
-  const int qp1 = POS ? __ldg(p.q_pos + b * p.Tq + tq1) : 0;
+  const int32_t* kpos_b = POS ? p.k_pos + static_cast<int64_t>(bkv) * p.S_max : nullptr;
+  const int qp0 = POS ? __ldg(p.q_pos + bq * p.Tq + tq0) : 0;
+  const int qp1 = POS ? __ldg(p.q_pos + bq * p.Tq + tq1) : 0;
 
   // ---- Q fragments (A operand, 16 rows x D): registers for bf16, shared memory for fp8
   uint32_t qa[C::FP8 ? 1 : D / 16][4];
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* q0 = q + b * p.q_sb + tq0 * p.q_st + h0 * p.q_sh;
-    const __nv_bfloat16* q1 = q + b * p.q_sb + tq1 * p.q_st + h1 * p.q_sh;
+    const __nv_bfloat16* q0 = q + bq * p.q_sb + tq0 * p.q_st + h0 * p.q_sh;
+    const __nv_bfloat16* q1 = q + bq * p.q_sb + tq1 * p.q_st + h1 * p.q_sh;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       if constexpr (!C::FP8) {
@@ -264,8 +308,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   const float* kscale_row = nullptr;
   const float* vscale_row = nullptr;
   if constexpr (C::FP8) {
-    kscale_row = p.k_scale + (static_cast<int64_t>(b) * p.Hkv + g) * p.n_scale_blk;
-    vscale_row = p.v_scale + (static_cast<int64_t>(b) * p.Hkv + g) * p.n_scale_blk;
+    kscale_row = p.k_scale + (static_cast<int64_t>(bkv) * p.Hkv + g) * p.n_scale_blk;
+    vscale_row = p.v_scale + (static_cast<int64_t>(bkv) * p.Hkv + g) * p.n_scale_blk;
   }
 
   for (int i = wn; i < n_tiles; i += WN) {
@@ -279,7 +323,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       } else {
         // per-page scales [num_blocks][Hkv][block_len / scale_block]; a page outside the
         // cache reads as zeros through TMA, so its scale is never fetched
-        const int page = kv_page_of(p, b, t0);
+        const int page = kv_page_of(p, bkv, t0);
         if (page >= 0 && page < p.num_blocks) {
           const int per = p.block_len / p.scale_block;
           const int64_t idx = (static_cast<int64_t>(page) * p.Hkv + g) * per + (t0 % p.block_len) / p.scale_block;
@@ -478,10 +522,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 2);
   }
   constexpr float kLn2 = 0.6931471805599453f;
-  const int part = j * p.n_chunk + c;
-  auto row_out = [&](int t_q, int h) -> int64_t {
-    return ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
-  };
+  int64_t oslot;
+  if constexpr (RING)
+    oslot = ring_out_slot(p);
+  else
+    oslot = static_cast<int64_t>(j * p.n_chunk + c) * p.B + b;
+  auto row_out = [&](int t_q, int h) -> int64_t { return (oslot * p.Tq + t_q) * p.Hq + h; };
 
   if constexpr (WN == 1) {
     const float inv0 = lrun[0] > 0.f ? 1.f / lrun[0] : 0.f;
@@ -622,10 +668,11 @@ cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUt
                        cudaStream_t stream) {
   static bool attr_done = false;  // per variant; set once per process
   if (!attr_done) {
-    const void* fns[4] = {reinterpret_cast<const void*>(gqa_partial_kernel<C, false, false>),
-                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, false>),
-                          reinterpret_cast<const void*>(gqa_partial_kernel<C, false, true>),
-                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, true>)};
+    const void* fns[5] = {reinterpret_cast<const void*>(gqa_partial_kernel<C, false, false, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, false, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, false, true, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, true, true, false>),
+                          reinterpret_cast<const void*>(gqa_partial_kernel<C, false, false, true>)};
     for (const void* f : fns) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
       if (e != cudaSuccess) return e;
@@ -634,14 +681,18 @@ cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUt
   }
   if (n_items <= 0) return cudaSuccess;
   const unsigned int grid = static_cast<unsigned int>(n_items);
-  if (p.block_table && p.k_pos)
-    gqa_partial_kernel<C, true, true><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
-  else if (p.block_table)
-    gqa_partial_kernel<C, true, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
-  else if (p.k_pos)
-    gqa_partial_kernel<C, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
-  else
-    gqa_partial_kernel<C, false, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  if (p.ring_n > 0) {
+    if (p.block_table || p.k_pos) return cudaErrorInvalidValue;  // no such instantiation
+    gqa_partial_kernel<C, false, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  } else if (p.block_table && p.k_pos) {
+    gqa_partial_kernel<C, true, true, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  } else if (p.block_table) {
+    gqa_partial_kernel<C, true, false, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  } else if (p.k_pos) {
+    gqa_partial_kernel<C, false, true, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  } else {
+    gqa_partial_kernel<C, false, false, false><<<grid, C::THREADS, C::SMEM, stream>>>(p, tmk, tmv);
+  }
   return cudaGetLastError();
 }
 

@@ -46,6 +46,8 @@ struct PartialParams {
   int32_t S_max;  // tokens at or past S_max do not exist
   int32_t n_split, n_chunk, chunk_tiles, m_tiles;
   int32_t zero_empty;  // write o = 0 for items with no visible token
+  int32_t ring_n;      // pass-Q ring: ranks (0: off) and query rows each rank owns; B then
+  int32_t ring_bq;     //   counts ring_n * ring_n * ring_bq work rows (rank, step, slot)
   int32_t bounds[kMaxBounds];  // [B][n_split + 1]
 };
 

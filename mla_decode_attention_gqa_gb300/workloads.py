@@ -25,6 +25,13 @@ Input recipe (per workload, seed = 1000 + index):
     the rank's layout order (``layout_positions``); the KV cache is the ranks' shards
     one after another and the query chunk is rank ``cp_rank``'s tokens.  The original
     positions go with them as int32 arrays q_pos [B, Tq] and k_pos [B, S].
+  * Pass-Q decode workloads spread each request's seq_len_b tokens over ``passq_ranks``
+    ranks (``passq_shard_lens``) and draw every rank's resident shard directly:
+    k_shards / v_shards [N * B, Hkv, S_loc, d] (row r * B + b: rank r's shard of request
+    b; S_loc = the longest shard rounded up to 64), N(0, 1) like the other caches, NaN
+    past each shard's length; fp8 shards are quantised per shard block of scale_block
+    tokens.  No logical cache is drawn: attention without a causal cut does not depend on
+    the order of the tokens, only on which tokens exist.
 
 Shapes follow the pages' workloads: Llama-405B-like GQA heads (Hq=128, Hkv=8,
 d=128) from the Helix and context-parallel pages, a DeepSeek-style absorbed MLA
@@ -63,6 +70,8 @@ class Workload:
     paged: bool = False         # also store the cache as pages with a block table
     block_len: int = 64         # tokens per page
     ring_steps: bool = False    # run as n_split pass-KV ring steps, one KV block per call
+    passq_ranks: int = 0        # pass-Q decode over this many emulated CP ranks (0: off)
+    passq_decode_tokens: int = 0  # tokens each request has decoded since its prompt
 
     @property
     def scale(self) -> float:
@@ -135,8 +144,41 @@ MLA_ABSORBED_PAGED = replace(MLA_ABSORBED, name="mla_absorbed_decode_s32k_paged6
 # own buffer, merged into a running output (attn_ring_step).
 RING_PREFILL_STEPS = replace(RING_PREFILL, name="ring_prefill_steps_8x4096", ring_steps=True, seed=1009)
 
+# Pass-Q decode on a CP4 group: 8 one-token queries (2 owned by each rank) of requests with
+# 64K..128K tokens of context, each request's cache spread over the 4 ranks (load-balanced
+# prompt chunks plus 1024 decoded tokens on a rotating owner); Llama-405B-like GQA heads.
+PASSQ_DECODE_CP4 = Workload("passq_decode_cp4_s128k", B=8, Tq=1, Hq=128, Hkv=8, dk=128, dv=128, S=131072,
+                            ragged=True, passq_ranks=4, passq_decode_tokens=1024, seed=1010)
+
 WORKLOADS = [TINY_GQA, HELIX_DENSE_128K, HELIX_KVP8_FP8_1M, MLA_ABSORBED, RING_PREFILL, RING_PREFILL_ZIGZAG,
-             RING_PREFILL_STRIPED, HELIX_DENSE_128K_PAGED, MLA_ABSORBED_PAGED, RING_PREFILL_STEPS]
+             RING_PREFILL_STRIPED, HELIX_DENSE_128K_PAGED, MLA_ABSORBED_PAGED, RING_PREFILL_STEPS, PASSQ_DECODE_CP4]
+
+
+def passq_shard_lens(w, seq_lens):
+    """[N][B] tokens of each request resident on each of the w.passq_ranks ranks.
+
+    A request of L tokens is a prompt of P = L - D tokens followed by D = min(L,
+    passq_decode_tokens) decoded ones.  The prompt is cut into 2N chunks of ceil(P / 2N)
+    tokens (the last ones shorter or empty) and rank r keeps chunks r and 2N - 1 - r, the
+    load-balanced pairing of "Context Parallelism for Scalable Million-Token Inference",
+    section "Load-balanced sharding makes causal work and memory land evenly"; decoded
+    token t of request b was stored on rank (b + t) mod N, the owner moving on every
+    decode iteration (same page, section "Pass-Q decode protects capacity but can hurt
+    TTIT").
+    """
+    N = w.passq_ranks
+    lens = [[0] * len(seq_lens) for _ in range(N)]
+    for b, L in enumerate(seq_lens):
+        D = min(w.passq_decode_tokens, L)
+        P = L - D
+        c = -(-P // (2 * N))
+        for r in range(N):
+            for ch in (r, 2 * N - 1 - r):
+                lens[r][b] += max(0, min(P, (ch + 1) * c) - ch * c)
+            # decoded tokens t with (b + t) mod N == r: t = (r - b) mod N, then every N-th
+            first = (r - b) % N
+            lens[r][b] += 0 if first >= D else (D - 1 - first) // N + 1
+    return lens
 
 
 def scaled(w: Workload, **kw) -> Workload:
@@ -230,6 +272,9 @@ def make_inputs(w: Workload, device="cpu", poison=True):
     else:
         raise ValueError(f"unknown kv dtype {w.kv_dtype}")
 
+    if w.passq_ranks:
+        return _make_passq(w, q, seq, seq_host, gen, dev, poison)
+
     pages = {}
     if w.paged:
         pages = _make_pages(w, k, v, k_scale, v_scale, gen, dev)
@@ -306,3 +351,47 @@ def _make_pages(w, k, v, k_scale, v_scale, gen, dev):
         res["k_scale_pages"] = scatter_s(k_scale)
         res["v_scale_pages"] = scatter_s(v_scale)
     return res
+
+
+def _make_passq(w, q, seq, seq_host, gen, dev, poison):
+    """Inputs of a pass-Q decode workload (see the module docstring)."""
+    N, B, Hkv = w.passq_ranks, w.B, w.Hkv
+    if B % N or w.Tq != 1:
+        raise ValueError("pass-Q decode: one query token per request, B a multiple of passq_ranks")
+    lens = passq_shard_lens(w, seq_host)
+    S_loc = max(64, -(-max(max(r) for r in lens) // 64) * 64)
+    fp8 = w.kv_dtype == "fp8_e4m3"
+    if not fp8 and w.kv_dtype != "bf16":
+        raise ValueError(f"unknown kv dtype {w.kv_dtype}")
+    dt = torch.uint8 if fp8 else torch.bfloat16
+    k = torch.empty((N * B, Hkv, S_loc, w.dk), dtype=dt, device=dev)
+    v = torch.empty((N * B, Hkv, S_loc, w.dv), dtype=dt, device=dev)
+    ks = vs = None
+    if fp8:
+        nb = S_loc // w.scale_block if S_loc % w.scale_block == 0 else S_loc // w.scale_block + 1
+        ks = torch.empty((N * B, Hkv, nb), dtype=torch.float32, device=dev)
+        vs = torch.empty((N * B, Hkv, nb), dtype=torch.float32, device=dev)
+    for r in range(N):
+        for b in range(B):
+            row, n = r * B + b, lens[r][b]
+            for g in range(Hkv):
+                if fp8:
+                    k[row, g], ks[row, g] = _quantize_e4m3_blocks(_randn((S_loc, w.dk), gen, dev), w.scale_block)
+                    v[row, g], vs[row, g] = _quantize_e4m3_blocks(_randn((S_loc, w.dv), gen, dev), w.scale_block)
+                else:
+                    k[row, g] = _randn((S_loc, w.dk), gen, dev).to(torch.bfloat16)
+                    v[row, g] = _randn((S_loc, w.dv), gen, dev).to(torch.bfloat16)
+            if poison and n < S_loc:
+                if fp8:
+                    k[row, :, n:] = 0x7F
+                    v[row, :, n:] = 0x7F
+                else:
+                    k[row, :, n:] = float("nan")
+                    v[row, :, n:] = float("nan")
+    return {
+        "q": q, "k": None, "v": None, "k_scale": None, "v_scale": None,
+        "seq_lens": seq.to(torch.int32), "seq_lens_host": seq_host, "split_bounds": [[0, w.S]] * B,
+        "q_pos": None, "k_pos": None, "q_pos_host": None, "k_pos_host": None,
+        "k_shards": k, "v_shards": v, "k_shard_scale": ks, "v_shard_scale": vs,
+        "shard_lens": torch.tensor(lens, dtype=torch.int32, device=dev), "shard_lens_host": lens,
+    }

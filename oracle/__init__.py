@@ -23,6 +23,7 @@ from .attention import (
     full_attention,
 )
 from .paged import gather_pages, gather_block_scales
+from .passq import passq_decode, gather_shards
 
 __all__ = [
     "bf16_bits_to_f64",
@@ -35,4 +36,6 @@ __all__ = [
     "full_attention",
     "gather_pages",
     "gather_block_scales",
+    "passq_decode",
+    "gather_shards",
 ]

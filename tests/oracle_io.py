@@ -120,3 +120,28 @@ def oracle_rows(inp, w, b, g, t_rows, bounds=None, causal_offset=None):
         o[j] = oo.reshape(R, G, w.dv)
         lse[j] = ll.reshape(R, G)
     return o, lse
+
+
+def oracle_passq(inp, w, b, g):
+    """Oracle of one (request b, KV head g) of a pass-Q workload: attention of the request's
+    query heads over the union of its shards on every rank.  Returns (o [1, G, dv], lse [1, G])."""
+    G = w.Hq // w.Hkv
+    N = w.passq_ranks
+    lens = inp["shard_lens_host"]
+    ks, vs = [], []
+    for r in range(N):
+        row = r * w.B + b
+        for which, acc in (("k", ks), ("v", vs)):
+            t = inp[f"{which}_shards"][row, g]
+            if w.kv_dtype == "bf16":
+                f = oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).cpu().numpy())
+            else:
+                sc = inp[f"{which}_shard_scale"][row, g].cpu().numpy()
+                f = oracle.dequant_e4m3_blocks(t.contiguous().cpu().numpy(), sc, w.scale_block)
+            acc.append(f[None, None, None])  # [1 rank, 1 request, 1 head, S_loc, d]
+    sl = [[lens[r][b]] for r in range(N)]
+    ku, tot = oracle.gather_shards(np.concatenate(ks), sl)
+    vu, _ = oracle.gather_shards(np.concatenate(vs), sl)
+    qb = q_f64(inp["q"][b : b + 1, :, g * G : (g + 1) * G])
+    o, lse = oracle.full_attention(qb, ku, vu, tot, w.causal_offset, w.scale)
+    return o[0], lse[0]

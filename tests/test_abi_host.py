@@ -184,3 +184,32 @@ def test_ring_step_arguments_are_checked():
     st = lib.attn_ring_step(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, 0, 0, FAKE, FAKE, None, 0, None)
     assert st == skv.SKV_EWORKSPACE  # a later step needs its workspace
     assert lib.attn_ring_step_workspace_size(ctypes.byref(_desc(B=0)), ctypes.byref(n)) == skv.SKV_EINVAL
+
+
+def test_passq_arguments_are_checked():
+    lib = skv.load_library()
+    n = ctypes.c_size_t(0)
+
+    def ws(d, n_ranks):
+        return lib.gqa_decode_attn_passq_workspace_size(ctypes.byref(d), n_ranks, ctypes.byref(n))
+
+    assert ws(_desc(B=4), 2) == skv.SKV_OK and n.value > 0
+    assert ws(_desc(B=3), 2) == skv.SKV_EINVAL  # B not a multiple of the group
+    assert ws(_desc(B=4), 0) == skv.SKV_EINVAL
+    assert ws(_desc(B=512), 4) == skv.SKV_EINVAL  # n_ranks * B above 1024
+    assert ws(_desc(B=4, Tq=2), 2) == skv.SKV_EUNSUPPORTED  # decode only
+    mla = _desc(B=4, Hq=128, Hkv=1, dk=576, dv=512, q_strides=(128 * 576, 128 * 576, 576),
+                k_strides=(1024 * 576, 1024 * 576, 576), v_strides=(1024 * 576, 1024 * 576, 576))
+    assert ws(mla, 2) == skv.SKV_EUNSUPPORTED
+    d = _desc(B=4)
+    assert ws(d, 2) == skv.SKV_OK
+    need = n.value
+    st = lib.gqa_decode_attn_passq(ctypes.byref(d), 2, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE, FAKE, need,
+                                   None)
+    assert st == skv.SKV_EINVAL  # no out
+    st = lib.gqa_decode_attn_passq(ctypes.byref(d), 2, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE,
+                                   need - 1, None)
+    assert st == skv.SKV_EWORKSPACE
+    st = lib.gqa_decode_attn_passq(ctypes.byref(d), 2, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, need,
+                                   None)
+    assert st == skv.SKV_EINVAL  # no shard_lens

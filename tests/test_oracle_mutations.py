@@ -15,6 +15,8 @@ import tests.test_oracle_pins as P
 import tests.test_oracle_layouts as L
 import tests.test_oracle_paged as PG
 from oracle import paged as PGO
+from oracle import passq as PQO
+import tests.test_oracle_passq as PQ
 
 _orig_attend = A.attend
 _orig_merge = A.merge_lse
@@ -104,6 +106,31 @@ def _split_swaps_positions(q, k, v, seq_lens, split_bounds, causal_offset, scale
     return _orig_split(q, k, v, seq_lens, split_bounds, causal_offset, scale, q_positions, k_positions)
 
 
+_orig_rank_partial = PQO.rank_partial
+_orig_gather_shards = PQO.gather_shards
+
+
+def _rank_partial_without_batch_ids(q_block, batch_ids, k_local, v_local, lens_local, scale):
+    # the block arrives without its batch ids: slot j reads the rank's entry of request j
+    return _orig_rank_partial(q_block, list(range(len(batch_ids))), k_local, v_local, lens_local, scale)
+
+
+def _return_to_computing_rank(arrived):
+    # partials filed under the rank that computed them instead of the queries' owner
+    N = len(arrived)
+    received = [[None] * N for _ in range(N)]
+    for k in range(N):
+        for s in range(N):
+            received[k][PQO.ring_source(k, s, N)] = arrived[k][s]
+    return received
+
+
+def _gather_shards_drops_last_rank(shards, shard_lens):
+    lens = [list(r) for r in shard_lens]
+    lens[-1] = [0] * len(lens[-1])
+    return _orig_gather_shards(shards, lens)
+
+
 MUTANTS = [
     ("attend without softmax scale", [(A, "attend", _attend_no_scale), (oracle, "attend", _attend_no_scale)],
      [P.test_golden_closed_forms]),
@@ -135,6 +162,15 @@ MUTANTS = [
     ("paged gather ignores the block table", [(PGO, "gather_pages", _gather_physical_order),
                                               (oracle, "gather_pages", _gather_physical_order)],
      [PG.test_hand_worked_gather, PG.test_gather_inverts_the_generators_scatter_bf16]),
+    ("pass-Q block travels without its batch ids", [(PQO, "rank_partial", _rank_partial_without_batch_ids)],
+     [PQ.test_zero_query_is_the_mean_value_over_every_rank_and_log_count,
+      PQ.test_one_token_per_request_returns_its_value_row]),
+    ("pass-Q partials kept by the computing rank", [(PQO, "return_to_owners", _return_to_computing_rank)],
+     [PQ.test_zero_query_is_the_mean_value_over_every_rank_and_log_count,
+      PQ.test_one_token_per_request_returns_its_value_row]),
+    ("shard gather drops the last rank", [(PQO, "gather_shards", _gather_shards_drops_last_rank),
+                                          (oracle, "gather_shards", _gather_shards_drops_last_rank)],
+     [PQ.test_hand_worked_gather]),
 ]
 
 
