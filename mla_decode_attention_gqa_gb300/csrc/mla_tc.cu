@@ -77,6 +77,14 @@ constexpr int kKStepsA = kKSteps / 2;    // warp 1: k-steps 0..17; warp 6: 18..3
 constexpr uint32_t kColO = 0;    // CTA 1: O, 512 columns
 constexpr uint32_t kPMsgBytes = 4 * (32 * 128 + 32 * 4);  // P rows + factors, four warps
 constexpr float kRescaleThreshold = 8.0f;
+// CTA 0's two 72 KB stages keep too few bytes in flight to cover the HBM latency (a tile
+// took ~2.1k cycles from issue to arrival, so the ring ran at (latency + MMA) / 2 per
+// tile); its producer also prefetches the tile this far ahead into L2, so that the ring's
+// own loads (and CTA 1's reads) hit L2.  Measured: 3, 4 and 5 ahead all take the step from
+// 0.181 to ~0.165 ms; 6 and 8 gain less.  Over a paged cache the same prefetch (its page
+// looked up one tile ahead) cost 4 % (0.191 -> 0.199 ms, same box), so the paged
+// instantiation does not prefetch.
+constexpr int kL2Ahead = 4;
 
 // One barrier block at the same offset in both CTAs (remote arrivals address a peer's
 // barrier by this CTA's own offset).
@@ -145,6 +153,14 @@ __device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* 
       "%5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Prefetch one tensor-map box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 // A warp's wait: every lane polls, and the warp leaves together.
@@ -243,6 +259,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int bx = 0; bx < kKBoxes; ++bx)
           tma_load_4d_plain(smem + (bx < kQTmemBoxes ? bx * kQBoxBytes : kOffQRope), &tmq, &bars->q_full, bx * 64, 0,
                             t_start, b);
+        // L2 prefetch of tile i (contiguous cache only)
+        auto prefetch = [&](int i) {
+          for (int bx = 0; bx < kKBoxes; ++bx) tma_prefetch_l2_4d(&tml, bx * 64, (tile_begin + i) * kTN, 0, b);
+        };
+        if constexpr (!PAGED)
+          for (int i = kNStage0; i < min(kL2Ahead, n_tiles); ++i) prefetch(i);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
         int page_next = b;  // paged: the next tile's page, read one tile ahead
         if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * kTN);
@@ -262,6 +284,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           for (int bx = 0; bx < kKBoxes; ++bx)
             tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, row, 0, outer);
+          if constexpr (!PAGED)
+            if (i + kL2Ahead < n_tiles) prefetch(i + kL2Ahead);
           issued = i + 1;
         }
         for (int i = max(0, issued - kNStage0); i < issued; ++i) {
