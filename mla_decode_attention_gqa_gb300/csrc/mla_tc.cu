@@ -163,6 +163,17 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c
                : "memory");
 }
 
+// Bulk copy of `bytes` contiguous shared-memory bytes to global memory (this thread's bulk
+// group), and the waits for this thread's groups: sources read / copies complete.
+__device__ __forceinline__ void bulk_store_global(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\tcp.async.bulk.commit_group;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // A warp's wait: every lane polls, and the warp leaves together.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
   const bool ok = mbar_wait(bar, parity, err, kDevErrFullWait);
@@ -650,28 +661,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // fp32 partial rows (2 KB each): staged through the ring's bytes (free once the last PV
+        // has completed and every load has landed) and written by one bulk copy per half row,
+        // so global memory sees whole contiguous rows rather than 16-byte pieces of 32 rows
+        // per store instruction.  Row pitch 1040 B keeps the staging stores conflict-free.
         const int part = j * p.n_chunk + c;
         const int64_t ro = ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
         float* orow = p.out_o + ro * kDv;
         const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
+        constexpr int kHalf = kDv / 2;              // 256 floats, 1 KB
+        constexpr uint32_t kPitch = kHalf * 4 + 16;  // staging row pitch
+        static_assert(kRows * kPitch <= kNStage1 * kStage1Bytes, "staging fits in the ring bytes");
+        float* stage = reinterpret_cast<float*>(smem + row * kPitch);
 #pragma unroll 1
-        for (int cc = 0; cc < kDv / 16; ++cc) {
-          uint32_t r[16];
-          if (have_o) {
-            tc::tmem_ld16(t_lane + kColO + 16 * cc, r);
-            tc::tmem_wait_ld();
-          } else {
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1 && write_o) bulk_wait_read();  // the first half's copy has read the row
+#pragma unroll 1
+          for (int c4 = 0; c4 < kHalf / 64; ++c4) {  // four 16-column loads per TMEM wait
+            uint32_t r[4][16];
+            if (have_o) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = 0u;
+              for (int u = 0; u < 4; ++u) tc::tmem_ld16(t_lane + kColO + half * kHalf + 64 * c4 + 16 * u, r[u]);
+              tc::tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[u][e] = 0u;
+            }
+            if (write_o) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                  *reinterpret_cast<float4*>(stage + 64 * c4 + 16 * u + e) =
+                      make_float4(__uint_as_float(r[u][e]) * inv, __uint_as_float(r[u][e + 1]) * inv,
+                                  __uint_as_float(r[u][e + 2]) * inv, __uint_as_float(r[u][e + 3]) * inv);
+            }
           }
           if (write_o) {
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              *reinterpret_cast<float4*>(orow + 16 * cc + e) =
-                  make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                              __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+            fence_proxy_async_smem();  // the staging writes before the bulk copy reads them
+            bulk_store_global(orow + half * kHalf, smem_u32(stage), kHalf * 4);
           }
         }
+        if (write_o) bulk_wait_all();
       }
     }
   }
