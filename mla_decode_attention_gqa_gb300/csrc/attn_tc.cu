@@ -350,7 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       qmax_w = __reduce_max_sync(0xffffffffu, valid ? qp : INT_MIN);
     }
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lgrp * 32) << 16);
-    float m_used = -INFINITY, l_sum = 0.f;
+    // l_sum: the fp32 row sum (for the lse); l_pv: the sum of the bf16-rounded p that PV
+    // uses (for normalising O: the output is then an exact convex combination of V rows with
+    // those weights; with the optimistic max no p is exact, and normalising by the fp32 sum
+    // left up to ~2^-8 max|v| of error in a split of a few tokens)
+    float m_used = -INFINITY, l_sum = 0.f, l_pv = 0.f;
     bool ok = true;
 
     for (int i = 0; i < n_used && ok; ++i) {
@@ -404,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Optimistic pass: p = 2^(scale*s - m_used) with the running max, the tile max
       // tracked alongside; P stays packed in registers until the max is known to be fine.
       uint32_t pk[kTN / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
+      uint64_t lr[2] = {0ull, 0ull};  // the same of the bf16-rounded p
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       const float base0 = (m_used == -INFINITY) ? 0.f : m_used;
 #pragma unroll
@@ -426,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], v1);
           const float p0 = fast_exp2(fmaf(v0, sl, -base0));
           const float p1 = fast_exp2(fmaf(v1, sl, -base0));
-          ls[(2 * e) & 3] += p0;
-          ls[(2 * e + 1) & 3] += p1;
+          ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
           pk[16 * cc + e] = pack_bf16(p0, p1);
         }
       }
@@ -456,12 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tmem_wait_st();
           l_sum *= alpha;
+          l_pv *= alpha;
         } else {
           l_sum = 0.f;
+          l_pv = 0.f;
         }
         m_used = m_new;
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+        ls[0] = ls[1] = 0ull;
 #pragma unroll 1
         for (int cc = 0; cc < kTN / 32; ++cc) {
           uint32_t r[2][16];
@@ -480,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float p0 = fast_exp2(fmaf(v0, sl, -base));
             const float p1 = fast_exp2(fmaf(v1, sl, -base));
-            ls[(2 * e) & 3] += p0;
-            ls[(2 * e + 1) & 3] += p1;
+            ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
             w[e] = pack_bf16(p0, p1);
+            lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(w[e]), bf16_hi(w[e]));
           }
           tc::tmem_st16(s_col + 16 * cc, w);  // S columns 32cc.. were read before P 16cc.. is written
         }
@@ -492,12 +498,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kTN / 32; ++cc) {
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pk[16 * cc + e];
+          for (int e = 0; e < 16; ++e) {
+            w[e] = pk[16 * cc + e];
+            lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(w[e]), bf16_hi(w[e]));
+          }
           tc::tmem_st16(s_col + 16 * cc, w);
         }
       }
       tc::tmem_wait_st();
-      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l_sum += sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
+      l_pv += sum_f32x2(lr[0]) + sum_f32x2(lr[1]);
       if (k == 0 && !in_range) {
         // tokens outside [r_lo, r_hi) may hold anything (NaN past the end of a sequence):
         // zero their V rows so that p = 0 really contributes nothing
@@ -524,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(&bars->pv_done[k], (n_used - 1) & 1, p.err, kDevErrFullWait);
       tc::fence_after_sync();
     }
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    const float inv = l_pv > 0.f ? 1.f / l_pv : 0.f;
     constexpr float kLn2 = 0.6931471805599453f;
     const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
     if (x.fused) {

@@ -358,7 +358,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t peer_p_full1 = map_to_rank(smem_u32(&bars->p_full[1]), 1);
       const uint32_t peer_precv = map_to_rank(smem_u32(smem + kOffPRecv), 1);
       const uint32_t peer_arecv = map_to_rank(smem_u32(smem + kOffARecv), 1);
-      float m_used = -INFINITY, l_sum = 0.f;
+      // l_sum: the fp32 row sum (for the lse); l_pv: the sum of the bf16-rounded p that PV
+      // uses, sent to CTA 1 to normalise O (an exact convex combination of V rows then; with
+      // the optimistic max no p is exact)
+      float m_used = -INFINITY, l_sum = 0.f, l_pv = 0.f;
       bool ok = true;
 
       if (n_tiles > 0) {
@@ -445,6 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float m_new = fmaxf(m_used, tmax);
           alpha = (i > 0) ? fast_exp2(m_used - m_new) : 1.f;
           l_sum *= alpha;
+          l_pv *= alpha;
           m_used = m_new;
         }
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
@@ -456,7 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         uint8_t* pst = smem + kOffPStage + (i & 1) * kPBytes;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
 #pragma unroll
         for (int ch = 0; ch < kTN / 8; ++ch) {
           uint32_t w[4];
@@ -464,13 +468,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             const float p0 = fast_exp2(fmaf(sv[8 * ch + 2 * e], sl, -base));
             const float p1 = fast_exp2(fmaf(sv[8 * ch + 2 * e + 1], sl, -base));
-            ls[(2 * e) & 3] += p0;
-            ls[(2 * e + 1) & 3] += p1;
+            ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
             w[e] = pack_bf16(p0, p1);
           }
           *reinterpret_cast<uint4*>(pst + swz128(row, ch * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l_sum += sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
         float* ast = reinterpret_cast<float*>(smem + kOffAStage + (i & 1) * kRows * 4);
         ast[row] = alpha;
         fence_proxy_async_smem();  // generic writes before the bulk copy reads them
@@ -482,11 +485,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t aoff = static_cast<uint32_t>((i & 1) * kRows * 4 + lgrp * 32 * 4);
           bulk_copy_to_peer(peer_arecv + aoff, smem_u32(smem + kOffAStage + aoff), 32 * 4, bar);
         }
+        // the sum of the rounded weights, off the path to the copy: re-read the staged row
+        // (the copy only reads it too; the slot is rewritten only after PV(i) is done)
+        uint64_t lr[2] = {0ull, 0ull};
+#pragma unroll
+        for (int ch = 0; ch < kTN / 8; ++ch) {
+          const uint4 q = *reinterpret_cast<const uint4*>(pst + swz128(row, ch * 16));
+          lr[0] = add_f32x2(lr[0], bf16_lo(q.x), bf16_hi(q.x));
+          lr[1] = add_f32x2(lr[1], bf16_lo(q.y), bf16_hi(q.y));
+          lr[0] = add_f32x2(lr[0], bf16_lo(q.z), bf16_hi(q.z));
+          lr[1] = add_f32x2(lr[1], bf16_lo(q.w), bf16_hi(q.w));
+        }
+        l_pv += sum_f32x2(lr[0]) + sum_f32x2(lr[1]);
       }
 
       // ---- final row sums to CTA 1 (it normalises O); lse from here
       float* lst = reinterpret_cast<float*>(smem + kOffLStage);
-      lst[row] = l_sum;
+      lst[row] = l_pv;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -629,8 +644,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
       }
       const bool got_l = warp_wait(&bars->l_full, 0, p.err);
-      const float l_sum = got_l ? reinterpret_cast<const float*>(smem + kOffLRecv)[row] : 0.f;
-      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      // the sum of the bf16 weights PV used (CTA 0's l_pv)
+      const float l_pv = got_l ? reinterpret_cast<const float*>(smem + kOffLRecv)[row] : 0.f;
+      const float inv = l_pv > 0.f ? 1.f / l_pv : 0.f;
       const bool have_o = ok && n_tiles > 0;
       constexpr int kDv = 512;
       if (x.fused) {
@@ -668,7 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int part = j * p.n_chunk + c;
         const int64_t ro = ((static_cast<int64_t>(part) * p.B + b) * p.Tq + t_q) * p.Hq + h;
         float* orow = p.out_o + ro * kDv;
-        const bool write_o = valid && (l_sum > 0.f || p.zero_empty);
+        const bool write_o = valid && (l_pv > 0.f || p.zero_empty);
         constexpr int kHalf = kDv / 2;              // 256 floats, 1 KB
         constexpr uint32_t kPitch = kHalf * 4 + 16;  // staging row pitch
         static_assert(kRows * kPitch <= kNStage1 * kStage1Bytes, "staging fits in the ring bytes");

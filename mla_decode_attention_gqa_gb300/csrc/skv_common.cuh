@@ -204,6 +204,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The two bf16 values of a packed pair (pack_bf16), widened back to float exactly.  A
+// softmax whose P goes through bf16 normalises O by the sum of these (the output is then an
+// exact convex combination of V rows with the rounded weights) and keeps the fp32 sum of p
+// for its lse.  With an optimistic running max (p up to 2^8, none exact) normalising by the
+// fp32 sum instead leaves the rounding errors in the output: up to ~2^-8 max|v| for a split
+// of a few tokens, about twice the error of the consistent normalisation.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two running fp32 sums in one 64-bit register, advanced by one packed add (two IEEE
+// round-to-nearest adds in one instruction): the softmax row sums take one instruction per
+// pair of columns.
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t acc, float x, float y) {
+  uint64_t v, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x), "f"(y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(acc), "l"(v));
+  return r;
+}
+__device__ __forceinline__ float sum_f32x2(uint64_t acc) {
+  float x, y;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc));
+  return x + y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
