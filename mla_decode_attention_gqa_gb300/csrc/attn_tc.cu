@@ -427,12 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             v0 = visible(col) ? v0 : -INFINITY;
             v1 = visible(col + 1) ? v1 : -INFINITY;
           }
-          mx[(2 * e) & 3] = fmaxf(mx[(2 * e) & 3], v0);
-          mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], v1);
-          const float p0 = fast_exp2(fmaf(v0, sl, -base0));
-          const float p1 = fast_exp2(fmaf(v1, sl, -base0));
+          // pairwise: one three-input max, one packed FMA, packed adds per column pair
+          mx[e & 3] = fmax3(mx[e & 3], v0, v1);
+          float a0, a1;
+          fma_pair(v0, v1, sl, -base0, a0, a1);
+          const float p0 = fast_exp2(a0);
+          const float p1 = fast_exp2(a1);
           ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
           pk[16 * cc + e] = pack_bf16(p0, p1);
+          lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(pk[16 * cc + e]), bf16_hi(pk[16 * cc + e]));
         }
       }
       // scores are scaled after the max (the scale is positive)
@@ -468,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
         ls[0] = ls[1] = 0ull;
+        lr[0] = lr[1] = 0ull;
 #pragma unroll 1
         for (int cc = 0; cc < kTN / 32; ++cc) {
           uint32_t r[2][16];
@@ -498,10 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kTN / 32; ++cc) {
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            w[e] = pk[16 * cc + e];
-            lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(w[e]), bf16_hi(w[e]));
-          }
+          for (int e = 0; e < 16; ++e) w[e] = pk[16 * cc + e];
           tc::tmem_st16(s_col + 16 * cc, w);
         }
       }

@@ -222,6 +222,21 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t acc, float x, float y) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(acc), "l"(v));
   return r;
 }
+// max(a, b, c) in one instruction (NaN operands ignored, as fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+// (x0, x1) * s + c for a pair in one packed instruction (two round-to-nearest FMAs).
+__device__ __forceinline__ void fma_pair(float x0, float x1, float s, float c, float& r0, float& r1) {
+  uint64_t x, sv, cv, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(sv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
 __device__ __forceinline__ float sum_f32x2(uint64_t acc) {
   float x, y;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc));
