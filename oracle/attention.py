@@ -14,7 +14,7 @@ Sources (web pages; cited by title and section):
   same merge as a closed-form equation over the N ring steps, and section "A
   runtime heuristic chooses the ring direction": shape(Q) = [T, N_H, D_H],
   shape(K) = shape(V) = [T+P, N_KV, D_H].
-* [Survey] "现代大模型推理并行策略总览", section "Transformer 的工程实践": rank r of a
+* [Overview] "现代大模型推理并行策略总览", section "Transformer 的工程实践": rank r of a
   head-aligned split holds query heads [r*h_q_local, (r+1)*h_q_local) and KV heads
   [r*h_kv_local, ...), i.e. query heads map to KV heads in contiguous groups;
   section "Decode CP：固定 KV Cache 分片，归并局部结果": each shard keeps one LSE per
@@ -22,13 +22,13 @@ Sources (web pages; cited by title and section):
   denominator; section "序列布局": a causal mask is decided by a token's original
   position.
 
-Readings where the pages are silent (all listed in the design doc): the LSE is the
+Readings where the pages are silent: the LSE is the
 natural log of the softmax denominator over *scaled* scores; a partial output is
 normalised by its own denominator; the merged LSE is m + ln(den); a split with no
 visible token has o = 0 and lse = -inf and weight 0 in the merge; query row i of a
 chunk sits at global position causal_offset + i and sees KV position t iff
 t <= causal_offset + i.  When the tokens are stored out of sequence order (the
-zigzag and striped layouts of [Survey] section "序列布局：Contiguous、Zigzag 与
+zigzag and striped layouts of [Overview] section "序列布局：Contiguous、Zigzag 与
 Striped"), every stored query row and KV token carries its original position and the
 same rule applies to those positions: a token is visible iff its position is at most
 the row's.
@@ -38,7 +38,7 @@ import numpy as np
 
 
 def kv_head_of(h, Hq, Hkv):
-    """KV head read by query head h: contiguous groups of Hq/Hkv heads ([Survey])."""
+    """KV head read by query head h: contiguous groups of Hq/Hkv heads ([Overview])."""
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     return h // (Hq // Hkv)
@@ -46,7 +46,7 @@ def kv_head_of(h, Hq, Hkv):
 
 def visible_mask(q_pos, kv_pos):
     """[R, n] bool: KV token t is visible to query row i iff kv_pos[t] <= q_pos[i]
-    (causal mask by original position, [Survey] section "序列布局")."""
+    (causal mask by original position, [Overview] section "序列布局")."""
     return np.asarray(kv_pos)[None, :] <= np.asarray(q_pos)[:, None]
 
 
@@ -59,7 +59,7 @@ def attend(q, k, v, scale, q_pos=None, kv_pos=None):
     scale : softmax scale applied to q.k
     q_pos, kv_pos : optional global positions ([R], [n]); when both are given a
         token is visible to a row only if kv_pos <= q_pos (causal mask by original
-        position, [Survey] "序列布局").
+        position, [Overview] "序列布局").
 
     Returns (o [R, dv], lse [R]):  o = sum_t e^{s_t - M} v_t / sum_t e^{s_t - M},
     lse = M + ln sum_t e^{s_t - M}, s_t = scale * q.k_t over the visible t, M their

@@ -13,8 +13,8 @@ The KV-cache quantisation that uses E4M3 (one fp32 scale per block of 64 tokens 
 per KV head, dequantised value = code value x scale) is the long-context KVP
 workload's cache format; the Helix page ("Helix Parallelism: Why Tensor
 Parallelism Hits a Wall at Million-Token Context", section "The ceiling, in
-algebra") only names low-precision (FP4) KV, so the block-scale reading is stated
-in DESIGN.md.
+algebra") only names low-precision (FP4) KV, so the block-scale format (one fp32
+scale per block of 64 tokens and KV head, value = code x scale) is this project's reading.
 """
 
 import numpy as np

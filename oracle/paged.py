@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE (see ``oracle/__init__.py``).
 
 Source: "Attention DP", section "KV Cache": each rank keeps its cache as
-[num_blocks, num_kv_heads / TP, block_len, d_head].  Reading (where the page is silent,
-listed in the design doc): a per-sequence block table maps logical block i of sequence b to
+[num_blocks, num_kv_heads / TP, block_len, d_head].  Reading (where the page is silent):
+a per-sequence block table maps logical block i of sequence b to
 the physical block that holds its tokens [i * block_len, (i + 1) * block_len), so token t
 of sequence b, KV head g is row t mod block_len of block table[b][t // block_len], head g.
 Per-block fp8 scales follow the block: scales[phys, g, (t mod block_len) // scale_block].

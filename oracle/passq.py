@@ -13,7 +13,7 @@ returned to the ranks the queries came from by an All-to-All, and merged there e
 by their log-sum-exp (the merge of section "Pass-KV keeps queries local and circulates
 keys and values").  The decode batch is padded to a multiple of the group size.
 
-Readings where the pages are silent (all listed in the design doc): rank r owns the queries of
+Readings where the pages are silent: rank r owns the queries of
 requests [r * B/N, (r + 1) * B/N); at ring step s rank k holds the block that started on
 rank (k - s) mod N (each rank passes its block to rank k + 1); a decode token follows
 every token of its request's cache, so it sees every resident token on every rank, in
