@@ -24,8 +24,10 @@
 //   * MMA order per KV tile: PV0(i), S0(i+1), PV1(i), S1(i+1), so each softmax group works
 //     while the tensor core serves the other group.  MMAs from one thread run in order, so
 //     when S_k(i) has landed, PV_k(i-1) is complete: O_k may be rescaled and P_k rewritten;
-//   * O is rescaled (TMEM load / scale / store) only when a row's running max rises by
-//     more than 2^8; otherwise p = 2^(s - m_used) <= 256 stays exact enough in bf16.
+//   * optimistic softmax: p = 2^(s - m_used) against the running max; O is rescaled (TMEM
+//     load / scale / store) and the tile redone only on a row's first visible tile or when
+//     the tile's p sum exceeds 2^16 (a score rose far above m_used), so no max is taken on
+//     the common path and every p stays <= 2^16, fine for bf16 P and the fp32 sums.
 #include <climits>
 #include <cuda_runtime.h>
 
@@ -59,7 +61,9 @@ constexpr int kSmem = 1024 + kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_k (and P_k over its first 64 columns) at kColS + 128 k
 constexpr uint32_t kColO = 256;  // O_k at kColO + 128 k
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// The optimistic softmax redoes a tile (new running max, O and l rescaled) only when the
+// tile's p sum exceeds this: then every p <= 2^16, fine for bf16 P and the fp32 sums.
+constexpr float kTileSumLimit = 65536.0f;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 struct Bars {
@@ -405,12 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_col = t_lane + kColS + 128 * k;
       const float sl = p.scale_log2;
 
-      // Optimistic pass: p = 2^(scale*s - m_used) with the running max, the tile max
-      // tracked alongside; P stays packed in registers until the max is known to be fine.
+      // Optimistic pass: p = 2^(scale*s - m_used) with the running max; P stays packed in
+      // registers until the tile's sum shows it is fine (no max is taken here: the redo
+      // below finds it when needed).
       uint32_t pk[kTN / 2];
       uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
       uint64_t lr[2] = {0ull, 0ull};  // the same of the bf16-rounded p
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       const float base0 = (m_used == -INFINITY) ? 0.f : m_used;
 #pragma unroll
       for (int cc = 0; cc < kTN / 32; ++cc) {
@@ -427,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v0 = visible(col) ? v0 : -INFINITY;
             v1 = visible(col + 1) ? v1 : -INFINITY;
           }
-          // pairwise: one three-input max, one packed FMA, packed adds per column pair
-          mx[e & 3] = fmax3(mx[e & 3], v0, v1);
+          // pairwise: one packed FMA and packed adds per column pair
           float a0, a1;
           fma_pair(v0, v1, sl, -base0, a0, a1);
           const float p0 = fast_exp2(a0);
@@ -438,12 +441,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(pk[16 * cc + e]), bf16_hi(pk[16 * cc + e]));
         }
       }
-      // scores are scaled after the max (the scale is positive)
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
-      const bool need = (tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold);
+      // Redo when this is the row's first visible tile, or when its p grew past the limit
+      // (then some score rose far above m_used; every p <= the tile sum <= 2^16 otherwise).
+      const float tile_sum = sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
+      bool row_vis = true;  // the row sees some column of this tile
+      if (need_mask) {
+        if constexpr (POS)
+          row_vis = (vis[0] | vis[1] | vis[2] | vis[3]) != 0u;
+        else
+          row_vis = span > 0u;
+      }
+      const bool need = row_vis && (m_used == -INFINITY || !(tile_sum <= kTileSumLimit));
       if (__any_sync(0xffffffffu, need)) {
-        // rare: a row's max rose by more than 2^8 (always on a row's first visible tile):
-        // rescale O and l to the new max and redo this tile's P from S (still in TMEM)
+        // rare: rescale O and l to the tile's true max and redo this tile's P from S (still
+        // in TMEM); the max comes from one pass over S (every lane of the warp takes part)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int cc = 0; cc < kTN / 32; ++cc) {
+          uint32_t r[2][16];
+          tc::tmem_ld16(s_col + 32 * cc, r[0]);
+          tc::tmem_ld16(s_col + 32 * cc + 16, r[1]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = 32 * cc + 2 * e;
+            float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
+            float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
+            if (need_mask) {
+              v0 = visible(col) ? v0 : -INFINITY;
+              v1 = visible(col + 1) ? v1 : -INFINITY;
+            }
+            mx[e & 3] = fmax3(mx[e & 3], v0, v1);
+          }
+        }
+        // scores are scaled after the max (the scale is positive)
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
         const float m_new = need ? fmaxf(m_used, tmax) : m_used;
         if (i > 0) {
           // PV_k(i-1) ran before S_k(i) on the in-order tensor pipe, so O_k is final here
