@@ -86,3 +86,28 @@ def test_fp8_decode_ring():
     o, l = _ring(w, inp, 4, [1, 3, 0, 2], 0)
     ro, rl = _oracle(inp, w, W.NO_CAUSAL)
     io.assert_close(o, l, ro, rl, io.TOL_FP8, "ring fp8")
+
+
+@pytest.mark.slow
+def test_full_size_ring_steps_sampled_rows():
+    """The ring-step workload bench.py times, at full size (8 steps of 4096-token blocks for
+    the last 4096-query chunk): equal to the single fused call over the same cache within
+    the bar, and sampled rows (edges of the diagonal block included) against the oracle."""
+    w = W.RING_PREFILL_STEPS
+    inp = W.make_inputs(w, DEV)
+    o_acc, lse_acc = _ring(w, inp, w.n_split, list(range(w.n_split)), w.n_split - 1)
+    out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"],
+                                   w.causal_offset, softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert skv.device_error() == 0
+    # the fused call's output is bf16: half an ulp of storage on top of the bar
+    ref = out.float()
+    assert torch.all((o_acc - ref).abs() <= io.TOL_BF16["out"] + io.BF16_STORE_REL * ref.abs())
+    assert (lse_acc - lse).abs().max().item() <= io.TOL_BF16["lse"]
+    G = w.Hq // w.Hkv
+    rows = [0, 1, 127, 128, 2047, 4094, 4095]
+    for g in (0, 7):
+        ro_p, rl_p = io.oracle_rows(inp, w, 0, g, rows)
+        ro, rl = oracle.merge_lse(ro_p, rl_p)
+        io.assert_close(o_acc[0, rows, g * G:(g + 1) * G], lse_acc[0, rows, g * G:(g + 1) * G], ro, rl, io.TOL_BF16,
+                        f"g={g}")
