@@ -99,9 +99,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: (b, g, [split j,] 256-row tile mt)
+  // Row tiles are handed out last-first across all (b, g, split): a causal chunk's later
+  // rows see more keys, so the heaviest CTAs start first and the last wave is light.
   int64_t item = blockIdx.x;
-  const int mt = static_cast<int>(item % p.m_tiles);
-  item /= p.m_tiles;
+  const int64_t per_tile = static_cast<int64_t>(p.B) * p.Hkv * (x.fused ? 1 : p.n_split);
+  const int mt = p.m_tiles - 1 - static_cast<int>(item / per_tile);
+  item %= per_tile;
   int j = 0;
   if (!x.fused) {
     j = static_cast<int>(item % p.n_split);
