@@ -26,6 +26,9 @@ template <bool OUT_BF16>
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ in_o, const float* __restrict__ in_lse,
                                                     int32_t n_in, int32_t g_out, int64_t R, int32_t dv,
                                                     void* __restrict__ out, float* __restrict__ out_lse) {
+  // launched as a programmatic dependent of the partial kernel: wait until that grid has
+  // completed and its partials are visible (a no-op for an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row_id = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row_id >= static_cast<int64_t>(g_out) * R) return;
@@ -130,14 +133,21 @@ cudaError_t launch_merge(const float* in_o, const float* in_lse, int32_t n_in, i
   const int64_t rows = static_cast<int64_t>(g_out) * R;
   if (rows <= 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
-  if (out_bf16) {
-    merge_kernel<true><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(in_o, in_lse, n_in, g_out, R, dv, out,
-                                                                              out_lse);
-  } else {
-    merge_kernel<false><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(in_o, in_lse, n_in, g_out, R, dv, out,
-                                                                               out_lse);
-  }
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid is set up while the partial kernel
+  // before it on the stream drains; griddepcontrol.wait in the kernel keeps the order
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (out_bf16)
+    return cudaLaunchKernelEx(&cfg, merge_kernel<true>, in_o, in_lse, n_in, g_out, R, dv, out, out_lse);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<false>, in_o, in_lse, n_in, g_out, R, dv, out, out_lse);
 }
 
 }  // namespace skv
