@@ -2,6 +2,7 @@
 value = its first 512 dims, 128 query heads) against the fp64 oracle.
 Bars: bf16 out max-abs <= 1e-2, lse <= 1e-3."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -84,4 +85,36 @@ def test_mla_two_query_rows_causal():
 def test_mla_single_split_chunked_long():
     """One long split that the planner cuts into chunks to fill the GPU."""
     w = W.scaled(W.MLA_ABSORBED, B=1, S=9000, n_split=1)
+    _all_paths(w, W.make_inputs(w, DEV))
+
+
+def _shard_bounds(B, S, seed):
+    """[B][3] bounds: a random range per sequence (every 7th empty, every 11th one token),
+    cut at a random point."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(B):
+        a = int(rng.integers(0, S + 1))
+        c = int(rng.integers(a, S + 1))
+        if b % 7 == 0:
+            c = a
+        if b % 11 == 0:
+            c = min(a + 1, S)
+        rows.append([a, int(rng.integers(a, c + 1)), c])
+    return rows
+
+
+def test_mla_many_ragged_sequences():
+    """160 short sequences whose ranges are empty, one token long or start off a tile
+    boundary, with lengths that stop short of the bounds."""
+    w = W.Workload("mla_many", B=160, Tq=1, Hq=128, Hkv=1, dk=576, dv=512, S=640, n_split=2, mla=True,
+                   softmax_scale=W.MLA_ABSORBED.softmax_scale, ragged=True, seed=1014)
+    inp = W.make_inputs(w, DEV)
+    _all_paths(w, inp, bounds=_shard_bounds(w.B, w.S, 1014))
+
+
+def test_mla_six_hundred_sequences():
+    """600 two-tile sequences: 600 cluster pairs, eight waves of them."""
+    w = W.Workload("mla_b600", B=600, Tq=1, Hq=128, Hkv=1, dk=576, dv=512, S=128, n_split=1, mla=True,
+                   softmax_scale=W.MLA_ABSORBED.softmax_scale, ragged=True, seed=1015)
     _all_paths(w, W.make_inputs(w, DEV))
