@@ -90,6 +90,23 @@ def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
     return err_o, err_l
 
 
+# Bar on the largest output error relative to the RMS of the reference outputs, for the
+# full-size cases: there the outputs are averages over up to 2^20 value rows (magnitude
+# ~1/sqrt(tokens)), so an absolute bar of 1e-2 (4e-2 for fp8) says little.  The expected
+# error is dominated by the bf16 rounding of the stored output, at most 2^-9 of an element
+# that is a few times the RMS (~1 % of the RMS); P's rounding averages out over the tokens.
+# The bar, 2^-5 of the RMS, leaves a factor of ~3.
+REL_RMS_BAR = 2.0 ** -5
+
+
+def rel_rms_err(got_o, ref_o):
+    """max |o - o_ref| / RMS(o_ref) over a set of output rows."""
+    go = got_o.detach().float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref_o, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(np.max(np.abs(go - ref))) / rms if rms > 0 else 0.0
+
+
 def oracle_rows(inp, w, b, g, t_rows, bounds=None, causal_offset=None):
     """Oracle partials of selected query rows of one (batch, KV head):
     o [n_split, len(t_rows), G, dv], lse [n_split, len(t_rows), G].  Used at full size,

@@ -1,7 +1,8 @@
 """GPU parity at the workloads' full sizes, on sampled outputs the oracle computes one
 group at a time (every query head of a sampled KV head, at sampled query rows), in the
 launch configuration bench.py times (the fused gqa_decode_attn call) and through
-attn_partial + attn_merge_lse.  Bars as in test_gpu_parity_gqa.py."""
+attn_partial + attn_merge_lse.  Bars as in test_gpu_parity_gqa.py, plus one on the largest
+merged-output error relative to the outputs' RMS (oracle_io.REL_RMS_BAR)."""
 
 import numpy as np
 import pytest
@@ -26,6 +27,9 @@ def _check_groups(w, inp, out, lse, groups, t_rows, parts=None):
         got_o = out[b, t_rows, g * G : (g + 1) * G]
         got_l = lse[b, t_rows, g * G : (g + 1) * G]
         io.assert_close(got_o, got_l, ro, rl, tol, f"merged b={b} g={g}")
+        rel = io.rel_rms_err(got_o, ro)
+        print(f"{w.name} b={b} g={g}: max-abs err / RMS(out) = {rel:.3e}")
+        assert rel <= io.REL_RMS_BAR, f"merged b={b} g={g}: err / RMS {rel:.3e} > {io.REL_RMS_BAR}"
         if parts is not None:
             po, pl = parts
             io.assert_close(po[:, b, t_rows, g * G : (g + 1) * G], pl[:, b, t_rows, g * G : (g + 1) * G], ro_p, rl_p,

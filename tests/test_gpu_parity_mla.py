@@ -67,6 +67,9 @@ def test_mla_absorbed_full_size_sampled():
         ro_p, rl_p = io.oracle_rows(inp, w, b, 0, [0])
         ro, rl = oracle.merge_lse(ro_p, rl_p)
         io.assert_close(out[b, [0]], lse[b, [0]], ro, rl, io.TOL_BF16, f"b={b}")
+        rel = io.rel_rms_err(out[b, [0]], ro)
+        print(f"{w.name} b={b}: max-abs err / RMS(out) = {rel:.3e}")
+        assert rel <= io.REL_RMS_BAR, f"b={b}: err / RMS {rel:.3e} > {io.REL_RMS_BAR}"
 
 
 def test_mla_64_heads_half_row_tile():

@@ -113,5 +113,12 @@ def test_full_size_cp4_sampled():
     out, lse = _call(w, inp)
     seq = inp["seq_lens_host"]
     bs = sorted(range(w.B), key=lambda b: seq[b])
-    _check(w, inp, out, lse, [(bs[0], 0), (bs[0], 7), (bs[-1], 3), (bs[-1], 4)])
+    pairs = [(bs[0], 0), (bs[0], 7), (bs[-1], 3), (bs[-1], 4)]
+    _check(w, inp, out, lse, pairs)
+    G = w.Hq // w.Hkv
+    for b, g in pairs:
+        ro, _ = io.oracle_passq(inp, w, b, g)
+        rel = io.rel_rms_err(out[b, :, g * G:(g + 1) * G], ro)
+        print(f"{w.name} b={b} g={g}: max-abs err / RMS(out) = {rel:.3e}")
+        assert rel <= io.REL_RMS_BAR, f"b={b} g={g}: err / RMS {rel:.3e} > {io.REL_RMS_BAR}"
     assert torch.isfinite(out.float()).all()
