@@ -3,10 +3,10 @@ real two-rank groups on the CPU (gloo, world_size 2, 127.0.0.1), with the fp64 o
 each rank's attention.
 
 KVP decode ("Helix Parallelism: Why Tensor Parallelism Hits a Wall at Million-Token
-Context", section "Sharding the sequence instead"): every rank
-holds one contiguous shard of every sequence's KV, computes the partial of all query heads
-over it, and one All-to-All over the query-head axis gives each rank every shard's partial
-for its own slab of heads, which it merges exactly by the lse.  The test also checks that
+Context", section "Sharding the sequence instead"): every rank holds one contiguous shard
+of every sequence's KV, computes the partial of all query heads over it, and one
+All-to-All over the query-head axis gives each rank every shard's partial for its own
+slab of heads, which it merges exactly by the lse.  The test also checks that
 a rank's send buffer is its split's slab of the single-GPU partial layout
 [split][B][Tq][Hq][dv], the layout attn_partial writes.
 
