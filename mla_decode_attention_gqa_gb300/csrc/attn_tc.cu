@@ -664,8 +664,8 @@ int tc_attn_kv_tile() { return kTN; }
 
 cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e0 = once_per_device(attr_done, [] {
     cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_attn_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -673,9 +673,9 @@ cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const C
       e = cudaFuncSetAttribute(tc_attn_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_attn_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   if (n_items <= 0) return cudaSuccess;
   const unsigned int grid = static_cast<unsigned int>(n_items);
   if (p.k_pos && p.block_table)

@@ -666,8 +666,8 @@ GqaLaunchInfo info_of() {
 template <class C>
 cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int64_t n_items,
                        cudaStream_t stream) {
-  static bool attr_done = false;  // per variant; set once per process
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};  // per variant, per device
+  cudaError_t e0 = once_per_device(attr_done, [] {
     const void* fns[5] = {reinterpret_cast<const void*>(gqa_partial_kernel<C, false, false, false>),
                           reinterpret_cast<const void*>(gqa_partial_kernel<C, true, false, false>),
                           reinterpret_cast<const void*>(gqa_partial_kernel<C, false, true, false>),
@@ -677,8 +677,9 @@ cudaError_t launch_cfg(const PartialParams& p, const CUtensorMap& tmk, const CUt
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
       if (e != cudaSuccess) return e;
     }
-    attr_done = true;
-  }
+    return cudaSuccess;
+  });
+  if (e0 != cudaSuccess) return e0;
   if (n_items <= 0) return cudaSuccess;
   const unsigned int grid = static_cast<unsigned int>(n_items);
   if (p.ring_n > 0) {

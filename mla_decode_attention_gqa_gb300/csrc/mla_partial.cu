@@ -313,12 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 GqaLaunchInfo mla_launch_info() { return GqaLaunchInfo{kRows, kThreads, kSmem, 1}; }
 
 cudaError_t launch_mla_partial(const PartialParams& p, const CUtensorMap& tmk, int64_t n_items, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e0 = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e0 != cudaSuccess) return e0;
   if (n_items <= 0) return cudaSuccess;
   mla_partial_kernel<<<static_cast<unsigned int>(n_items), kThreads, kSmem, stream>>>(p, tmk);
   return cudaGetLastError();

@@ -738,14 +738,14 @@ int mla_tc_kv_tile() { return kTN; }
 
 cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
                           const CUtensorMap& tml, int64_t n_items, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e0 = once_per_device(attr_done, [] {
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   if (n_items <= 0) return cudaSuccess;
   if (p.block_table)
     mla_tc_kernel<true><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);

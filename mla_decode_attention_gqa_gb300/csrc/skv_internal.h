@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace skv {
 
 // Largest B * (n_split + 1) whose split bounds travel inside the kernel parameters.
@@ -23,6 +25,21 @@ constexpr int kTileN = 64;
 //
 // The item writes its partial (normalised o, natural-log lse) to part
 // p = j * n_chunk + c of out_o [n_part][B][Tq][Hq][dv] and out_lse [n_part][B][Tq][Hq].
+// Kernel attributes set with cudaFuncSetAttribute belong to the current device's context,
+// so a launcher applies them the first time it launches on each device: `done` keeps one
+// bit per device (devices past 63 set them on every launch).
+template <class F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 struct PartialParams {
   const void* q;  // bf16 [B][Tq][Hq][dk] with strides below (elements)
   int64_t q_sb, q_st, q_sh;
