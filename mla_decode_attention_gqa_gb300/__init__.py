@@ -15,6 +15,8 @@ plus the position-masked (_pos), paged (_paged) and pass-KV ring-step variants.
 """
 
 import ctypes
+import functools
+import inspect
 import math
 import os
 
@@ -207,6 +209,60 @@ def _require_cuda(*ts):
             raise ValueError("split-KV attention runs on CUDA tensors only (no CPU path)")
 
 
+def _on_tensor_device(fn):
+    """Run a call with its first tensor's device current: the library launches on the
+    current device and stream, so every tensor of the call must live on that device."""
+
+    first = next(iter(inspect.signature(fn).parameters))
+
+    @functools.wraps(fn)
+    def wrapped(*args, **kw):
+        t = args[0] if args else kw.get(first)
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("split-KV attention runs on CUDA tensors only (no CPU path)")
+        with torch.cuda.device(t.device):
+            return fn(*args, **kw)
+
+    return wrapped
+
+
+def _same_device(dev, **tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device} but q on {dev}: every tensor of a call must be on one device")
+
+
+def _out(t, shape, dtype, dev, name):
+    """The caller's output buffer, checked (exact shape and dtype, contiguous, on dev), or a new one."""
+    shape = tuple(int(x) for x in shape)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=dev)
+    if t.device != dev or t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape} on {dev}")
+    return t
+
+
+def _ws_arg(workspace, nbytes, dev):
+    """(buffer, bytes) of the caller's workspace, or of the library's cached scratch."""
+    if workspace is None:
+        return _workspace(nbytes, dev), nbytes
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {dev}")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def _check_lens(t, n, name):
+    if t.dtype != torch.int32 or not t.is_contiguous() or tuple(t.shape) != (n,):
+        raise ValueError(f"{name} must be contiguous int32 of shape ({n},)")
+
+
+def _check_scales(scales, shape, layout):
+    shape = tuple(int(x) for x in shape)
+    for s in scales:
+        if s is not None and (s.dtype != torch.float32 or not s.is_contiguous() or tuple(s.shape) != shape):
+            raise ValueError(f"scales must be contiguous float32 {layout} = {shape}")
+
+
 def _kv_dtype(k):
     if k.dtype == torch.bfloat16:
         return SKV_KV_BF16
@@ -256,10 +312,12 @@ _ws_cache = {}
 
 
 def _workspace(nbytes, device):
-    """A reusable device scratch buffer of at least nbytes (torch allocation)."""
+    """A reusable device scratch buffer of at least nbytes (torch allocation), one per
+    (device, current stream): calls on different streams never share one."""
     if nbytes == 0:
         return None
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           torch.cuda.current_stream(device).cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -273,13 +331,12 @@ def _stream():
 
 def _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale, scale_block):
     _require_cuda(q, k_cache, v_cache, seq_lens, k_scale, v_scale)
-    if seq_lens.dtype != torch.int32:
-        raise ValueError("seq_lens must be int32")
+    _same_device(q.device, k_cache=k_cache, v_cache=v_cache, seq_lens=seq_lens, k_scale=k_scale, v_scale=v_scale)
     d = make_desc(q, k_cache, v_cache, softmax_scale, scale_block)
+    _check_lens(seq_lens, d.B, "seq_lens")
     bounds, n_split = _bounds_array(split_bounds, d.B)
-    for s in (k_scale, v_scale):
-        if s is not None and (s.dtype != torch.float32 or not s.is_contiguous()):
-            raise ValueError("scales must be contiguous float32 [B,Hkv,n_blocks]")
+    if d.kv_dtype == SKV_KV_FP8_E4M3 and scale_block > 0:
+        _check_scales((k_scale, v_scale), (d.B, d.Hkv, -(-d.S_max // scale_block)), "[B, Hkv, ceil(S / scale_block)]")
     return d, bounds, n_split
 
 
@@ -288,8 +345,8 @@ def _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scal
     """Descriptor of a paged cache: pages [num_blocks, Hkv, block_len, d], block table
     int32 [B, max_blocks]; S_max = max_blocks * block_len logical tokens per sequence."""
     _require_cuda(q, k_pages, v_pages, seq_lens, k_scale, v_scale, block_table)
-    if seq_lens.dtype != torch.int32:
-        raise ValueError("seq_lens must be int32")
+    _same_device(q.device, k_pages=k_pages, v_pages=v_pages, seq_lens=seq_lens, k_scale=k_scale, v_scale=v_scale,
+                 block_table=block_table)
     if block_table.dtype != torch.int32 or not block_table.is_contiguous() or block_table.dim() != 2:
         raise ValueError("block_table must be contiguous int32 [B, max_blocks]")
     if q.dim() != 4 or k_pages.dim() != 4 or v_pages.dim() != 4:
@@ -301,6 +358,7 @@ def _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scal
     nb, Hkv, L, dk2 = k_pages.shape
     if dk2 != dk or v_pages.shape[:3] != k_pages.shape[:3] or block_table.shape[0] != B:
         raise ValueError("q / pages / block_table shapes disagree")
+    _check_lens(seq_lens, B, "seq_lens")
     d = SkvDesc()
     d.B, d.Tq, d.Hq, d.Hkv, d.dk, d.dv = B, Tq, Hq, Hkv, dk, v_pages.shape[3]
     d.S_max = block_table.shape[1] * L
@@ -315,9 +373,8 @@ def _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scal
     pg.block_len, pg.max_blocks, pg.num_blocks = L, block_table.shape[1], nb
     pg.block_table = block_table.data_ptr()
     bounds, n_split = _bounds_array(split_bounds, B)
-    for s_ in (k_scale, v_scale):
-        if s_ is not None and (s_.dtype != torch.float32 or not s_.is_contiguous()):
-            raise ValueError("scales must be contiguous float32 [num_blocks,Hkv,block_len/scale_block]")
+    if d.kv_dtype == SKV_KV_FP8_E4M3 and scale_block > 0:
+        _check_scales((k_scale, v_scale), (nb, Hkv, L // scale_block), "[num_blocks, Hkv, block_len / scale_block]")
     return d, pg, bounds, n_split
 
 
@@ -333,16 +390,15 @@ def gqa_decode_attn_workspace_size(desc, bounds, n_split):
     return int(n.value)
 
 
+@_on_tensor_device
 def attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_CAUSAL, k_scale=None,
                  v_scale=None, softmax_scale=None, scale_block=64, out_partial=None, lse_partial=None):
     """Per-split partial attention: returns (out_partial fp32 [n_split,B,Tq,Hq,dv], lse fp32 [n_split,B,Tq,Hq])."""
     d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
                                scale_block)
     dev = q.device
-    if out_partial is None:
-        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
-    if lse_partial is None:
-        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
+    lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
     nbytes = attn_partial_workspace_size(d, bounds, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -351,6 +407,7 @@ def attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_C
     return out_partial, lse_partial
 
 
+@_on_tensor_device
 def attn_merge_lse(out_partials, lse_partials, out=None, lse=None):
     """Exact LSE merge over the first axis: returns (out bf16 [B,Tq,Hq,dv], lse fp32 [B,Tq,Hq])."""
     _require_cuda(out_partials, lse_partials)
@@ -358,53 +415,53 @@ def attn_merge_lse(out_partials, lse_partials, out=None, lse=None):
         raise ValueError("partials must be float32")
     if not (out_partials.is_contiguous() and lse_partials.is_contiguous()):
         raise ValueError("partials must be contiguous")
+    if out_partials.dim() != 5 or tuple(lse_partials.shape) != tuple(out_partials.shape[:4]):
+        raise ValueError("partials must be out [n_split,B,Tq,Hq,dv] and lse [n_split,B,Tq,Hq]")
+    dev = out_partials.device
+    _same_device(dev, lse_partials=lse_partials)
     n_split, B, Tq, Hq, dv = out_partials.shape
-    if out is None:
-        out = torch.empty((B, Tq, Hq, dv), dtype=torch.bfloat16, device=out_partials.device)
-    if lse is None:
-        lse = torch.empty((B, Tq, Hq), dtype=torch.float32, device=out_partials.device)
+    out = _out(out, (B, Tq, Hq, dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (B, Tq, Hq), torch.float32, dev, "lse")
     _check(_lib.attn_merge_lse(n_split, B, Tq, Hq, dv, _ptr(out_partials), _ptr(lse_partials), _ptr(out), _ptr(lse),
                                _stream()))
     return out, lse
 
 
+@_on_tensor_device
 def gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_CAUSAL, k_scale=None,
                     v_scale=None, softmax_scale=None, scale_block=64, out=None, lse=None, workspace=None):
     """Split-KV attention plus merge in one call: returns (out bf16 [B,Tq,Hq,dv], lse fp32 [B,Tq,Hq])."""
     d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
                                scale_block)
     dev = q.device
-    if out is None:
-        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
-    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
-    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
     _check(_lib.gqa_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                 _ptr(seq_lens), bounds, n_split, int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
-                                nbytes if workspace is None else workspace.numel(), _stream()))
+                                ws_bytes, _stream()))
     return out, lse
 
 
-def _positions(q_pos, k_pos, d):
+def _positions(q_pos, k_pos, d, dev):
     _require_cuda(q_pos, k_pos)
+    _same_device(dev, q_pos=q_pos, k_pos=k_pos)
     for t, shape, name in ((q_pos, (d.B, d.Tq), "q_pos"), (k_pos, (d.B, d.S_max), "k_pos")):
         if t.dtype != torch.int32 or not t.is_contiguous() or tuple(t.shape) != shape:
             raise ValueError(f"{name} must be contiguous int32 of shape {shape}")
 
 
+@_on_tensor_device
 def attn_partial_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, k_scale=None, v_scale=None,
                      softmax_scale=None, scale_block=64, out_partial=None, lse_partial=None):
     """attn_partial with the causal rule taken from original positions: token t is visible to
     row i iff k_pos[b, t] <= q_pos[b, i] (q_pos int32 [B,Tq], k_pos int32 [B,S], on the GPU)."""
     d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
                                scale_block)
-    _positions(q_pos, k_pos, d)
+    _positions(q_pos, k_pos, d, q.device)
     dev = q.device
-    if out_partial is None:
-        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
-    if lse_partial is None:
-        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
+    lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
     nbytes = attn_partial_workspace_size(d, bounds, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
@@ -413,26 +470,24 @@ def attn_partial_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, 
     return out_partial, lse_partial
 
 
+@_on_tensor_device
 def gqa_decode_attn_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, k_scale=None, v_scale=None,
                         softmax_scale=None, scale_block=64, out=None, lse=None, workspace=None):
     """gqa_decode_attn with the causal rule taken from original positions (see attn_partial_pos)."""
     d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
                                scale_block)
-    _positions(q_pos, k_pos, d)
+    _positions(q_pos, k_pos, d, q.device)
     dev = q.device
-    if out is None:
-        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
-    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
-    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
     _check(_lib.gqa_decode_attn_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                     _ptr(v_scale), _ptr(seq_lens), bounds, n_split, _ptr(q_pos), _ptr(k_pos),
-                                    _ptr(out), _ptr(lse), _ptr(ws), nbytes if workspace is None else workspace.numel(),
-                                    _stream()))
+                                    _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream()))
     return out, lse
 
 
+@_on_tensor_device
 def attn_partial_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, causal_offset=NO_CAUSAL,
                        k_scale=None, v_scale=None, softmax_scale=None, scale_block=64, out_partial=None,
                        lse_partial=None):
@@ -441,10 +496,8 @@ def attn_partial_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table,
     d, pg, bounds, n_split = _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scale, v_scale,
                                          softmax_scale, scale_block)
     dev = q.device
-    if out_partial is None:
-        out_partial = torch.empty((n_split, d.B, d.Tq, d.Hq, d.dv), dtype=torch.float32, device=dev)
-    if lse_partial is None:
-        lse_partial = torch.empty((n_split, d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
+    lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
     nbytes = attn_partial_workspace_size(d, bounds, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
@@ -453,6 +506,7 @@ def attn_partial_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table,
     return out_partial, lse_partial
 
 
+@_on_tensor_device
 def gqa_decode_attn_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, causal_offset=NO_CAUSAL,
                           k_scale=None, v_scale=None, softmax_scale=None, scale_block=64, out=None, lse=None,
                           workspace=None):
@@ -460,25 +514,23 @@ def gqa_decode_attn_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_tab
     d, pg, bounds, n_split = _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scale, v_scale,
                                          softmax_scale, scale_block)
     dev = q.device
-    if out is None:
-        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
-    nbytes = gqa_decode_attn_workspace_size(d, bounds, n_split)
-    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
     _check(_lib.gqa_decode_attn_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                       _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), bounds, n_split,
-                                      int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
-                                      nbytes if workspace is None else workspace.numel(), _stream()))
+                                      int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream()))
     return out, lse
 
 
+@_on_tensor_device
 def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=NO_CAUSAL, first=False, k_scale=None,
                    v_scale=None, softmax_scale=None, scale_block=64):
     """One pass-KV ring step: attention of q over this step's KV block (its own buffer,
     [B,Hkv,S_blk,d]) merged into the running o_acc fp32 [B,Tq,Hq,dv] / lse_acc fp32
     [B,Tq,Hq] in place (written, not read, when first).  Returns (o_acc, lse_acc)."""
     _require_cuda(o_acc, lse_acc)
+    _same_device(q.device, o_acc=o_acc, lse_acc=lse_acc)
     d, _, _ = _prep(q, k_block, v_block, seq_lens, [[0, k_block.shape[2]]], k_scale, v_scale, softmax_scale,
                     scale_block)
     for t, shape, name in ((o_acc, (d.B, d.Tq, d.Hq, d.dv), "o_acc"), (lse_acc, (d.B, d.Tq, d.Hq), "lse_acc")):
@@ -493,6 +545,7 @@ def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=
     return o_acc, lse_acc
 
 
+@_on_tensor_device
 def gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, k_scale=None, v_scale=None, softmax_scale=None,
                           scale_block=64, out=None, lse=None, workspace=None):
     """Pass-Q decode over the N = shard_lens.shape[0] ranks of a context-parallel group,
@@ -501,6 +554,8 @@ def gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, k_scale=None, v_sca
     b); shard_lens int32 [N,B]; fp8 scales [N*B,Hkv,S_loc/scale_block].  Returns (out bf16
     [B,1,Hq,dv], lse fp32 [B,1,Hq])."""
     _require_cuda(q, k_shards, v_shards, shard_lens, k_scale, v_scale)
+    _same_device(q.device, k_shards=k_shards, v_shards=v_shards, shard_lens=shard_lens, k_scale=k_scale,
+                 v_scale=v_scale)
     if shard_lens.dtype != torch.int32 or not shard_lens.is_contiguous() or shard_lens.dim() != 2:
         raise ValueError("shard_lens must be contiguous int32 [n_ranks, B]")
     n_ranks, B = shard_lens.shape
@@ -510,21 +565,18 @@ def gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, k_scale=None, v_sca
         raise ValueError("q must be [B, 1, Hq, dk] with B = shard_lens.shape[1]")
     # one shard row's description: the library steps through all n_ranks * B rows
     d = make_desc(q, k_shards[:B], v_shards[:B], softmax_scale, scale_block)
-    for s_ in (k_scale, v_scale):
-        if s_ is not None and (s_.dtype != torch.float32 or not s_.is_contiguous()):
-            raise ValueError("scales must be contiguous float32 [n_ranks * B, Hkv, n_blocks]")
+    if d.kv_dtype == SKV_KV_FP8_E4M3 and scale_block > 0:
+        _check_scales((k_scale, v_scale), (n_ranks * B, d.Hkv, -(-d.S_max // scale_block)),
+                      "[n_ranks * B, Hkv, ceil(S_loc / scale_block)]")
     dev = q.device
-    if out is None:
-        out = torch.empty((d.B, d.Tq, d.Hq, d.dv), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((d.B, d.Tq, d.Hq), dtype=torch.float32, device=dev)
+    out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
     n = ctypes.c_size_t(0)
     _check(_lib.gqa_decode_attn_passq_workspace_size(ctypes.byref(d), n_ranks, ctypes.byref(n)))
-    nbytes = int(n.value)
-    ws = workspace if workspace is not None else _workspace(nbytes, dev)
+    ws, ws_bytes = _ws_arg(workspace, int(n.value), dev)
     _check(_lib.gqa_decode_attn_passq(ctypes.byref(d), n_ranks, _ptr(q), _ptr(k_shards), _ptr(v_shards),
                                       _ptr(k_scale), _ptr(v_scale), _ptr(shard_lens), _ptr(out), _ptr(lse), _ptr(ws),
-                                      nbytes if workspace is None else workspace.numel(), _stream()))
+                                      ws_bytes, _stream()))
     return out, lse
 
 

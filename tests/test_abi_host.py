@@ -213,3 +213,50 @@ def test_passq_arguments_are_checked():
     st = lib.gqa_decode_attn_passq(ctypes.byref(d), 2, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, need,
                                    None)
     assert st == skv.SKV_EINVAL  # no shard_lens
+
+
+# ---------------------------------------------------------------- binding argument checks
+
+
+def test_binding_checks_caller_buffers():
+    """Caller outputs must match exactly (shape, dtype, contiguous, device) before any
+    pointer reaches the library; a workspace tensor is sized in bytes."""
+    import torch
+
+    dev = torch.device("cpu")
+    ok = torch.empty((2, 3), dtype=torch.float32)
+    assert skv._out(ok, (2, 3), torch.float32, dev, "o") is ok
+    assert tuple(skv._out(None, (4,), torch.bfloat16, dev, "o").shape) == (4,)
+    for bad in (torch.empty((3, 2), dtype=torch.float32), torch.empty((2, 3), dtype=torch.float64),
+                torch.empty((3, 2), dtype=torch.float32).t()):
+        with pytest.raises(ValueError):
+            skv._out(bad, (2, 3), torch.float32, dev, "o")
+    ws, nbytes = skv._ws_arg(torch.empty(10, dtype=torch.float32), 999, dev)
+    assert nbytes == 40
+    with pytest.raises(ValueError):
+        skv._ws_arg(torch.empty((4, 4), dtype=torch.uint8).t(), 1, dev)
+
+
+def test_binding_checks_lengths_and_scales():
+    import torch
+
+    skv._check_lens(torch.zeros(3, dtype=torch.int32), 3, "seq_lens")
+    for bad in (torch.zeros(3, dtype=torch.int64), torch.zeros(4, dtype=torch.int32),
+                torch.zeros(6, dtype=torch.int32)[::2]):
+        with pytest.raises(ValueError):
+            skv._check_lens(bad, 3, "seq_lens")
+    skv._check_scales((torch.ones((2, 1, 5)), None), (2, 1, 5), "[B, Hkv, n]")
+    with pytest.raises(ValueError):
+        skv._check_scales((torch.ones((2, 1, 4)),), (2, 1, 5), "[B, Hkv, n]")
+
+
+def test_binding_rejects_cpu_tensors_before_the_library():
+    import torch
+
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    k = torch.zeros((1, 2, 64, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        skv.gqa_decode_attn(q, k, k, torch.zeros(1, dtype=torch.int32), [[0, 64]])
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        skv.gqa_decode_attn(q=q, k_cache=k, v_cache=k, seq_lens=torch.zeros(1, dtype=torch.int32),
+                            split_bounds=[[0, 64]])
