@@ -15,16 +15,6 @@ constexpr int kMaxBounds = 2048;
 // Tokens per KV tile of the GQA partial kernel (and the chunk granularity).
 constexpr int kTileN = 64;
 
-// Parameters of one split-KV partial-attention launch.
-//
-// Work item = (b, kv head g, split j, chunk c, row tile mt).  Split j of sequence b
-// covers tokens [bounds[b][j], bounds[b][j+1]) clipped to seq_lens[b]; chunk c of it
-// covers the tile-aligned window [a + c*chunk_tiles*kTileN, a + (c+1)*chunk_tiles*kTileN)
-// with a = floor(bounds[b][j] / kTileN) * kTileN.  Row m of kv head g's row space
-// (m < Tq*G) is query row t = m / G of query head g*G + m % G.
-//
-// The item writes its partial (normalised o, natural-log lse) to part
-// p = j * n_chunk + c of out_o [n_part][B][Tq][Hq][dv] and out_lse [n_part][B][Tq][Hq].
 // Kernel attributes set with cudaFuncSetAttribute belong to the current device's context,
 // so a launcher applies them the first time it launches on each device: `done` keeps one
 // bit per device (devices past 63 set them on every launch).
@@ -40,6 +30,16 @@ cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
   return e;
 }
 
+// Parameters of one split-KV partial-attention launch.
+//
+// Work item = (b, kv head g, split j, chunk c, row tile mt).  Split j of sequence b
+// covers tokens [bounds[b][j], bounds[b][j+1]) clipped to seq_lens[b]; chunk c of it
+// covers the tile-aligned window [a + c*chunk_tiles*kTileN, a + (c+1)*chunk_tiles*kTileN)
+// with a = floor(bounds[b][j] / kTileN) * kTileN.  Row m of kv head g's row space
+// (m < Tq*G) is query row t = m / G of query head g*G + m % G.
+//
+// The item writes its partial (normalised o, natural-log lse) to part
+// p = j * n_chunk + c of out_o [n_part][B][Tq][Hq][dv] and out_lse [n_part][B][Tq][Hq].
 struct PartialParams {
   const void* q;  // bf16 [B][Tq][Hq][dk] with strides below (elements)
   int64_t q_sb, q_st, q_sh;
