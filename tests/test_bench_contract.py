@@ -1,0 +1,94 @@
+"""bench.py's output contract, checked on the CPU.
+
+* `config` names a workload by what it is (sizes, dtype, layout, L2 policy) and carries
+  no model keys;
+* a DRAM-traffic record is reported only while the kernel sources it was measured on
+  still hash to the recorded value, and never for a workload it does not cover;
+* the reference arm (the fp64 oracle on host cores) prints one JSON line with the
+  contract's keys, its `cpu_baseline` and a host-only `e2e` (no device copies)."""
+
+import argparse
+import contextlib
+import io
+import json
+import os
+import shutil
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from mla_decode_attention_gqa_gb300 import workloads as W  # noqa: E402
+
+
+@pytest.mark.parametrize("w", W.WORKLOADS, ids=lambda w: w.name)
+def test_config_names_the_workload_only(w):
+    c = bench.config_of(w)
+    assert c["workload"] == w.name
+    for k in ("B", "Tq", "Hq", "Hkv", "dk", "dv", "S", "kv_dtype", "n_split", "l2", "parallelism"):
+        assert k in c, k
+    assert not {"model", "global_batch", "seq_len"} & set(c)
+    assert json.loads(json.dumps(c)) == c  # plain JSON
+
+
+def _records():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        return json.load(f)
+
+
+def test_traffic_records_name_existing_sources_and_a_dominant_kernel():
+    for name, rec in _records().items():
+        assert any(w.name == name for w in W.WORKLOADS), name
+        assert rec["kernel"] and rec["dram_bytes_per_launch"] > 0
+        for rel in rec["kernel_sources"]:
+            assert os.path.isfile(os.path.join(ROOT, rel)), rel
+
+
+def test_traffic_is_dropped_once_a_kernel_source_changes(tmp_path, monkeypatch):
+    recs = _records()
+    name = next(iter(recs))
+    rec = recs[name]
+    # a private copy of the record and of its sources, so that a source can be edited
+    for rel in rec["kernel_sources"]:
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copyfile(os.path.join(ROOT, rel), dst)
+    path = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(path))
+    sha = bench.kernel_source_sha(rec["kernel_sources"])
+    rec2 = dict(rec, kernel_source_sha=sha)
+    path.write_text(json.dumps({name: rec2}))
+    assert bench.ncu_traffic(name) == float(rec["dram_bytes_per_launch"])
+    assert bench.ncu_traffic("no_such_workload") is None
+    with open(tmp_path / rec["kernel_sources"][0], "a") as f:
+        f.write("\n// edited\n")
+    assert bench.ncu_traffic(name) is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.reference_arm(argparse.Namespace(steps=1, warmup=3), W.TINY_GQA, 1, 0)
+    lines = [l for l in buf.getvalue().splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["config"] == bench.config_of(W.TINY_GQA, 1)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_is_silent_off_rank_zero():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.reference_arm(argparse.Namespace(steps=1, warmup=3), W.TINY_GQA, 2, 1)
+    assert buf.getvalue() == ""
