@@ -238,24 +238,36 @@ def launches_per_step(w):
     return 1 if tensor_core else 2
 
 
+# Bounds on one oracle sample, so that a sample takes seconds rather than minutes: a decode
+# group longer than ORACLE_MAX_TOKENS tokens is cut to its first ones (time and bytes both
+# scale with the tokens), and a query chunk of more than ORACLE_MAX_ROWS rows computes every
+# (Tq / ORACLE_MAX_ROWS)-th row, its KV bytes credited in proportion to the rows computed.
+ORACLE_MAX_TOKENS = 131072
+ORACLE_MAX_ROWS = 256
+
+
 def oracle_sample(w, budget_s=12.0, max_groups=None):
-    """Time the fp64 oracle on whole (batch, KV head) groups of the workload until the
-    budget is spent; returns (KV bytes processed, seconds, groups, tokens)."""
+    """Time the fp64 oracle on bounded samples of (batch, KV head) groups of the workload
+    until the budget is spent; returns (KV bytes credited, seconds, groups, tokens per
+    group, query rows computed per group)."""
     import numpy as np
     import oracle
 
     gen = torch.Generator().manual_seed(w.seed)
     G = w.Hq // w.Hkv
-    bounds = w.split_bounds()[0]
-    pos = {}
-    if w.layout != "contiguous":  # tokens stored in a zigzag / striped layout
-        pos = {"q_positions": [W.layout_positions(w.layout, w.S, w.n_split, w.cp_rank)],
-               "k_positions": [[p for r in range(w.n_split) for p in W.layout_positions(w.layout, w.S, w.n_split, r)]]}
-    done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
     if w.passq_ranks:
         return _oracle_sample_passq(w, gen, budget_s, max_groups)
+    S = min(w.S, ORACLE_MAX_TOKENS) if w.Tq == 1 else w.S
+    bounds = [min(x, S) for x in w.split_bounds()[0]]
+    rows = np.arange(w.Tq) if w.Tq <= ORACLE_MAX_ROWS else np.arange(0, w.Tq, w.Tq // ORACLE_MAX_ROWS)
+    pos = {}
+    if w.layout != "contiguous":  # tokens stored in a zigzag / striped layout
+        pos = {"q_positions": [np.asarray(W.layout_positions(w.layout, w.S, w.n_split, w.cp_rank))[rows]],
+               "k_positions": [[p for r in range(w.n_split) for p in W.layout_positions(w.layout, w.S, w.n_split, r)]]}
+    elif len(rows) < w.Tq:  # a subset of the chunk's rows: give their positions explicitly
+        pos = {"q_positions": [w.causal_offset + rows], "k_positions": [np.arange(S)]}
+    done_bytes, elapsed, groups = 0.0, 0.0, 0
     while elapsed < budget_s and (max_groups is None or groups < max_groups):
-        S = w.S
         q = torch.randn((1, w.Tq, G, w.dk), generator=gen).to(torch.bfloat16)
         k = torch.randn((S, w.dk), generator=gen).to(torch.bfloat16)
         v = torch.randn((S, w.dv), generator=gen).to(torch.bfloat16)
@@ -263,7 +275,7 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
             kc, ks = W._quantize_e4m3_blocks(k.float(), w.scale_block)
             vc, vs = W._quantize_e4m3_blocks(v.float(), w.scale_block)
         t0 = time.perf_counter()
-        qf = oracle.bf16_bits_to_f64(q.view(torch.int16).numpy())
+        qf = oracle.bf16_bits_to_f64(q.view(torch.int16).numpy())[:, rows]
         if w.kv_dtype == "fp8_e4m3":
             kf = oracle.dequant_e4m3_blocks(kc.numpy(), ks.numpy(), w.scale_block)
             vf = oracle.dequant_e4m3_blocks(vc.numpy(), vs.numpy(), w.scale_block)
@@ -274,10 +286,18 @@ def oracle_sample(w, budget_s=12.0, max_groups=None):
                                         **pos)
         oracle.merge_lse(o, lse)
         elapsed += time.perf_counter() - t0
-        done_bytes += RL.kv_bytes(1, w.dk, w.dv, w.kv_dtype, [S], [bounds], mla=w.mla, scale_block=w.scale_block)
+        done_bytes += (RL.kv_bytes(1, w.dk, w.dv, w.kv_dtype, [S], [bounds], mla=w.mla, scale_block=w.scale_block)
+                       * len(rows) / w.Tq)
         groups += 1
-        tokens += S
-    return done_bytes, elapsed, groups, tokens
+    return done_bytes, elapsed, groups, S, len(rows)
+
+
+def oracle_sample_text(w, groups, tokens, rows):
+    """What one oracle sample covered, in words."""
+    tok = f"{tokens} tokens" + (f" (the first {tokens} of {w.S})" if tokens < w.S else "")
+    row = f"{rows} row(s)" if rows == w.Tq else f"{rows} of {w.Tq} rows (every {w.Tq // rows}th)"
+    ring = f", through the {w.passq_ranks}-rank pass-Q ring" if w.passq_ranks else ""
+    return f"{groups} (batch, KV head) group(s) of {tok} x {row} x {w.Hq // w.Hkv} heads{ring}"
 
 
 def _oracle_sample_passq(w, gen, budget_s, max_groups):
@@ -291,7 +311,7 @@ def _oracle_sample_passq(w, gen, budget_s, max_groups):
     N, G = w.passq_ranks, w.Hq // w.Hkv
     lens = W.passq_shard_lens(W.scaled(w, B=N), [w.S] + [0] * (N - 1))
     S_loc = max(lens[r][0] for r in range(N))
-    done_bytes, elapsed, groups, tokens = 0, 0.0, 0, 0
+    done_bytes, elapsed, groups = 0, 0.0, 0
     while elapsed < budget_s and (max_groups is None or groups < max_groups):
         q = torch.randn((N, 1, G, w.dk), generator=gen).to(torch.bfloat16)
         k = torch.randn((N, 1, S_loc, w.dk), generator=gen).to(torch.bfloat16)  # request 0 on each rank
@@ -306,8 +326,7 @@ def _oracle_sample_passq(w, gen, budget_s, max_groups):
         elapsed += time.perf_counter() - t0
         done_bytes += RL.kv_bytes(1, w.dk, w.dv, "bf16", [w.S], [[0, w.S]])
         groups += 1
-        tokens += w.S
-    return done_bytes, elapsed, groups, tokens
+    return done_bytes, elapsed, groups, w.S, 1
 
 
 def reference_arm(args, w, ws, rank):
@@ -317,13 +336,12 @@ def reference_arm(args, w, ws, rank):
     bytes_total, secs_total = 0, 0.0
     sample = None
     for i in range(args.warmup + args.steps):
-        b, s, g, t = oracle_sample(w, budget_s=float("inf"), max_groups=1)
+        b, s, g, t, r = oracle_sample(w, budget_s=float("inf"), max_groups=1)
         if i >= args.warmup:
             steps.append(s)
             bytes_total += b
             secs_total += s
-            sample = (f"{g} (batch, KV head) group(s) of {t // max(g, 1)} tokens x {w.Tq} rows x {w.Hq // w.Hkv} "
-                      f"heads per step" + (f", through the {w.passq_ranks}-rank pass-Q ring" if w.passq_ranks else ""))
+            sample = oracle_sample_text(w, g, t, r) + " per step"
     gbs = bytes_total / secs_total / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
@@ -553,10 +571,9 @@ def ours_arm(args, w, ws, rank, local):
                  "tflops": round(flops / step_s / 1e12, 2), "tensor_frac": round(flops / step_s / 1e12 / tc, 4)})
     cpu = None
     if not args.no_cpu_baseline and ws >= 1:
-        b, s, g, t = oracle_sample(w, budget_s=args.cpu_budget)
+        b, s, g, t, r = oracle_sample(w, budget_s=args.cpu_budget)
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle",
-               "sample": f"{g} (batch, KV head) groups x {t // max(g, 1)} tokens, {w.Tq} row(s) x {w.Hq // w.Hkv} heads each, "
-                         f"{s:.1f} s"}
+               "sample": oracle_sample_text(w, g, t, r) + f", {s:.1f} s"}
     line = {
         "metric": METRIC,
         "value": round(value_gbs, 2),
