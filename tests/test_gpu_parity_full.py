@@ -67,7 +67,10 @@ def test_ring_prefill_full_size_sampled_rows():
     inp = W.make_inputs(w, DEV)
     out, lse = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"],
                                    w.causal_offset, softmax_scale=w.scale)
+    # the eight ring steps' own partials too (2 GiB of fp32), compared split by split
+    po, pl = skv.attn_partial(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"], w.causal_offset,
+                              softmax_scale=w.scale)
     torch.cuda.synchronize()
     assert skv.device_error() == 0
     rows = [0, 1, 63, 64, 2047, 4094, 4095]
-    _check_groups(w, inp, out, lse, [(0, 0), (0, 7)], rows)
+    _check_groups(w, inp, out, lse, [(0, 0), (0, 7)], rows, parts=(po, pl))
