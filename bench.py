@@ -329,6 +329,37 @@ def _oracle_sample_passq(w, gen, budget_s, max_groups):
     return done_bytes, elapsed, groups, w.S, 1
 
 
+def oracle_parity(w, par):
+    """Max-abs error of the timed steps' output and lse for batch 0, KV head 0 against the
+    fp64 oracle on the same bytes (the cpu_baseline leg's check of the bench's own result)."""
+    if "error" in par:
+        return par
+    try:
+        import numpy as np
+        import oracle
+
+        n_tok, rows = par["n_tok"], np.asarray(par["rows"])
+        qf = oracle.bf16_bits_to_f64(par["q"].view(torch.int16).numpy())[None]  # [1, R, G, dk]
+        if par["ks"] is not None:
+            kf = oracle.dequant_e4m3_blocks(par["k"].numpy(), par["ks"].numpy(), w.scale_block)
+            vf = oracle.dequant_e4m3_blocks(par["v"].numpy(), par["vs"].numpy(), w.scale_block)
+        else:
+            kf = oracle.bf16_bits_to_f64(par["k"].view(torch.int16).numpy())
+            vf = oracle.bf16_bits_to_f64(par["v"].view(torch.int16).numpy())
+        bounds = [min(x, n_tok) for x in w.split_bounds()[0]]
+        pos = {}
+        if w.causal_offset != W.NO_CAUSAL:
+            pos = {"q_positions": [w.causal_offset + rows], "k_positions": [np.arange(n_tok)]}
+        o, lse = oracle.split_attention(qf, kf[None, None], vf[None, None], [n_tok], [bounds], w.causal_offset,
+                                        w.scale, **pos)
+        mo, ml = oracle.merge_lse(o, lse)
+        return {"sample": f"batch 0, KV head 0: {len(rows)} of {w.Tq} row(s) x {qf.shape[2]} heads, {n_tok} tokens",
+                "out_max_abs_err": float(np.max(np.abs(par["out"].numpy() - mo[0]))),
+                "lse_max_abs_err": float(np.max(np.abs(par["lse"].numpy() - ml[0])))}
+    except Exception as e:  # the parity sample must never cost the bench line
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
 def reference_arm(args, w, ws, rank):
     if rank != 0:
         return
@@ -465,6 +496,25 @@ def ours_arm(args, w, ws, rank, local):
     value_gbs = all_bytes / (max_total_ms * 1e-3) / 1e9
     ms_per_step = max_total_ms / args.steps
 
+    # one (batch, KV head) group's inputs and the timed steps' result for it, kept on the host
+    # for the cpu_baseline leg's parity sample (plain caches with at most ORACLE_MAX_TOKENS
+    # tokens in the group; a long query chunk keeps every (Tq / ORACLE_MAX_ROWS)-th row)
+    par = None
+    if not args.no_cpu_baseline and not (w.paged or w.passq_ranks or w.ring_steps or positional):
+        try:
+            G = w.Hq // w.Hkv
+            n_tok = inp["seq_lens_host"][0]
+            rows = list(range(w.Tq)) if w.Tq <= ORACLE_MAX_ROWS else list(range(0, w.Tq, w.Tq // ORACLE_MAX_ROWS))
+            if n_tok <= ORACLE_MAX_TOKENS:
+                fp8 = w.kv_dtype == "fp8_e4m3"
+                par = {"n_tok": n_tok, "rows": rows,
+                       "q": inp["q"][0, rows, :G].contiguous().cpu(),
+                       "k": inp["k"][0, 0, :n_tok].contiguous().cpu(), "v": inp["v"][0, 0, :n_tok].contiguous().cpu(),
+                       "ks": inp["k_scale"][0, 0].cpu() if fp8 else None, "vs": inp["v_scale"][0, 0].cpu() if fp8 else None,
+                       "out": out[0, rows, :G].float().cpu(), "lse": lse[0, rows, :G].cpu()}
+        except Exception as e:  # the parity sample must never cost the bench line
+            par = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     # e2e: the public call with host (pinned) inputs; copies in and the result back every step
     e2e = None
     if not args.no_e2e:
@@ -574,6 +624,8 @@ def ours_arm(args, w, ws, rank, local):
         b, s, g, t, r = oracle_sample(w, budget_s=args.cpu_budget)
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle",
                "sample": oracle_sample_text(w, g, t, r) + f", {s:.1f} s"}
+        if par is not None:
+            cpu["parity"] = oracle_parity(w, par)
     line = {
         "metric": METRIC,
         "value": round(value_gbs, 2),

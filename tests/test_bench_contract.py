@@ -5,7 +5,8 @@
 * a DRAM-traffic record is reported only while the kernel sources it was measured on
   still hash to the recorded value, and never for a workload it does not cover;
 * the reference arm (the fp64 oracle on host cores) prints one JSON line with the
-  contract's keys, its `cpu_baseline` and a host-only `e2e` (no device copies)."""
+  contract's keys, its `cpu_baseline` and a host-only `e2e` (no device copies);
+* the cpu_baseline leg's parity sample reports the error of the result it is given."""
 
 import argparse
 import contextlib
@@ -16,6 +17,7 @@ import shutil
 import sys
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -92,3 +94,32 @@ def test_reference_arm_is_silent_off_rank_zero():
     with contextlib.redirect_stdout(buf):
         bench.reference_arm(argparse.Namespace(steps=1, warmup=3), W.TINY_GQA, 2, 1)
     assert buf.getvalue() == ""
+
+
+def test_parity_sample_reports_the_error_of_the_given_result():
+    """oracle_parity compares a stored result with the oracle on the same bytes: an exact
+    result (the oracle's own, rounded to bf16) gives errors at rounding level, and a planted
+    error in one output element shows up in full."""
+    import numpy as np
+
+    import oracle
+
+    w = W.scaled(W.HELIX_DENSE_128K, B=1, Hq=16, Hkv=1, S=512)
+    inp = W.make_inputs(w)
+    G, n = w.Hq // w.Hkv, inp["seq_lens_host"][0]
+    qf = oracle.bf16_bits_to_f64(inp["q"][0:1, :, :G].contiguous().view(torch.int16).numpy())
+    kf = oracle.bf16_bits_to_f64(inp["k"][0, 0, :n].contiguous().view(torch.int16).numpy())
+    vf = oracle.bf16_bits_to_f64(inp["v"][0, 0, :n].contiguous().view(torch.int16).numpy())
+    o, l = oracle.split_attention(qf, kf[None, None], vf[None, None], [n], [w.split_bounds()[0]], w.causal_offset,
+                                  w.scale)
+    mo, ml = oracle.merge_lse(o, l)
+    par = {"n_tok": n, "rows": [0], "q": inp["q"][0, [0], :G].contiguous(), "k": inp["k"][0, 0, :n].contiguous(),
+           "v": inp["v"][0, 0, :n].contiguous(), "ks": None, "vs": None,
+           "out": torch.from_numpy(mo[0]).to(torch.bfloat16).float(), "lse": torch.from_numpy(ml[0]).float()}
+    good = bench.oracle_parity(w, par)
+    assert good["out_max_abs_err"] < 2 ** -8 * float(np.abs(mo).max()) + 1e-6 and good["lse_max_abs_err"] < 1e-6
+    par["out"] = par["out"].clone()
+    par["out"][0, 3, 5] += 0.5
+    bad = bench.oracle_parity(w, par)
+    assert bad["out_max_abs_err"] > 0.49
+    assert "error" in bench.oracle_parity(w, {"error": "x"})
