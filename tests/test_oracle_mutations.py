@@ -43,9 +43,10 @@ def _kv_head_interleaved(h, Hq, Hkv):
 
 def _merge_linear_weights(o_parts, lse_parts):
     lse_parts = np.asarray(lse_parts, dtype=np.float64)
-    w = lse_parts - lse_parts.min(axis=0) + 1.0  # weights not exponentiated
-    o = (w[..., None] * np.asarray(o_parts)).sum(0) / w.sum(0)[..., None]
-    return o, np.log(np.exp(lse_parts).sum(0))
+    with np.errstate(all="ignore"):  # empty splits (lse = -inf) make this slip produce NaN
+        w = lse_parts - lse_parts.min(axis=0) + 1.0  # weights not exponentiated
+        o = (w[..., None] * np.asarray(o_parts)).sum(0) / w.sum(0)[..., None]
+        return o, np.log(np.exp(lse_parts).sum(0))
 
 
 def _merge_lse_without_max(o_parts, lse_parts):
@@ -142,10 +143,10 @@ MUTANTS = [
      [P.test_gqa_contiguous_groups]),
     ("merge weights not exponentiated", [(A, "merge_lse", _merge_linear_weights),
                                          (oracle, "merge_lse", _merge_linear_weights)],
-     [P.test_merge_two_fragments_closed_form_and_empty_split]),
+     [P.test_merge_two_fragments_closed_form_and_empty_split, P.test_merged_fragments_merge_again]),
     ("merged lse drops the max", [(A, "merge_lse", _merge_lse_without_max),
                                   (oracle, "merge_lse", _merge_lse_without_max)],
-     [P.test_merge_two_fragments_closed_form_and_empty_split]),
+     [P.test_merge_two_fragments_closed_form_and_empty_split, P.test_merged_fragments_merge_again]),
     ("e4m3 exponent bias 8", [(oracle, "e4m3_bits_to_f64", _e4m3_bias8)],
      [P.test_e4m3_all_codes_match_torch]),
     ("split not clipped to seq_len", [(A, "_visible_range", _split_ignores_seq_len)],

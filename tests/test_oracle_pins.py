@@ -214,6 +214,29 @@ def test_any_split_merges_to_unsplit(seed):
     np.testing.assert_allclose(o_m2, o_m, atol=1e-13)
 
 
+def test_merged_fragments_merge_again():
+    """A merged (o, lse) is itself a fragment: merging groups of splits first and then the
+    groups' results (what a KVP group's All-to-All and a ring's running output do) gives
+    the flat merge and the unsplit attention; a group whose splits are all empty merges to
+    (0, -inf) and stays neutral one level up."""
+    rng = np.random.default_rng(21)
+    B, Tq, Hq, Hkv, S = 2, 2, 4, 2, 48
+    q, k, v = _qkv(rng, B, Tq, Hq, Hkv, S, 5, 3)
+    seq = [29, 48]  # batch 0: the last two splits lie past its end
+    bounds = [[0, 5, 13, 20, 29, 40, 48]] * B
+    o_p, l_p = oracle.split_attention(q, k, v, seq, bounds, 1 << 62, 0.7)
+    groups = [[0, 1, 2], [3], [4, 5]]  # batch 0's group [4, 5] is empty
+    lvl = [oracle.merge_lse(o_p[g], l_p[g]) for g in groups]
+    assert np.all(np.isneginf(lvl[2][1][0])) and np.all(lvl[2][0][0] == 0)
+    o2, l2 = oracle.merge_lse(np.stack([x[0] for x in lvl]), np.stack([x[1] for x in lvl]))
+    o1, l1 = oracle.merge_lse(o_p, l_p)
+    o_f, l_f = oracle.full_attention(q, k, v, seq, 1 << 62, 0.7)
+    np.testing.assert_allclose(o2, o1, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, atol=1e-13)
+    np.testing.assert_allclose(o2, o_f, atol=1e-12)
+    np.testing.assert_allclose(l2, l_f, atol=1e-12)
+
+
 def test_merge_two_fragments_closed_form_and_empty_split():
     rng = np.random.default_rng(8)
     o1, o2 = rng.normal(size=(3, 4)), rng.normal(size=(3, 4))
