@@ -7,6 +7,14 @@ bf16 output + fp32 LSE.  One step = one gqa_decode_attn call (split-KV partial k
 + LSE merge) over the resident KV cache.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+                  [--extras auto|none|NAME,...]
+
+On one GPU the default run then measures, each in its own timed region with its own clock
+record and oracle parity sample, the other workloads the metric is quoted on: the
+long-context KVP=8 decode at S=2^20 with fp8-e4m3 KV, the MLA absorbed decode, and the
+ring pass-KV prefill chunk as one fused call and as eight ring steps.  They are reported
+under "workloads" in the same JSON line (time per layer, the dominant kernel's time, its
+HBM and bf16-tensor fractions of the measured peaks).
 
 Multi-GPU (torchrun): every rank runs an independent replica of the workload (the
 attention of a layer shards into independent problems; no data-path collective), the
@@ -331,7 +339,10 @@ def _oracle_sample_passq(w, gen, budget_s, max_groups):
 
 def oracle_parity(w, par):
     """Max-abs error of the timed steps' output and lse for batch 0, KV head 0 against the
-    fp64 oracle on the same bytes (the cpu_baseline leg's check of the bench's own result)."""
+    fp64 oracle on the same bytes (the parity sample of the bench's own result).  The
+    oracle walks the group one split at a time (attention of the sampled rows over the
+    split's tokens, then the exact merge of the splits), so that a group of 2^20 tokens
+    needs one split's rows in float64 at a time."""
     if "error" in par:
         return par
     try:
@@ -339,23 +350,36 @@ def oracle_parity(w, par):
         import oracle
 
         n_tok, rows = par["n_tok"], np.asarray(par["rows"])
-        qf = oracle.bf16_bits_to_f64(par["q"].view(torch.int16).numpy())[None]  # [1, R, G, dk]
-        if par["ks"] is not None:
-            kf = oracle.dequant_e4m3_blocks(par["k"].numpy(), par["ks"].numpy(), w.scale_block)
-            vf = oracle.dequant_e4m3_blocks(par["v"].numpy(), par["vs"].numpy(), w.scale_block)
-        else:
-            kf = oracle.bf16_bits_to_f64(par["k"].view(torch.int16).numpy())
-            vf = oracle.bf16_bits_to_f64(par["v"].view(torch.int16).numpy())
+        qf = oracle.bf16_bits_to_f64(par["q"].view(torch.int16).numpy())  # [R, G, dk]
+        R, G, dk = qf.shape
         bounds = [min(x, n_tok) for x in w.split_bounds()[0]]
-        pos = {}
-        if w.causal_offset != W.NO_CAUSAL:
-            pos = {"q_positions": [w.causal_offset + rows], "k_positions": [np.arange(n_tok)]}
-        o, lse = oracle.split_attention(qf, kf[None, None], vf[None, None], [n_tok], [bounds], w.causal_offset,
-                                        w.scale, **pos)
-        mo, ml = oracle.merge_lse(o, lse)
-        return {"sample": f"batch 0, KV head 0: {len(rows)} of {w.Tq} row(s) x {qf.shape[2]} heads, {n_tok} tokens",
-                "out_max_abs_err": float(np.max(np.abs(par["out"].numpy() - mo[0]))),
-                "lse_max_abs_err": float(np.max(np.abs(par["lse"].numpy() - ml[0])))}
+        q_pos = np.repeat(w.causal_offset + rows.astype(np.int64), G) if w.causal_offset != W.NO_CAUSAL else None
+        o_parts, l_parts = [], []
+        for j in range(len(bounds) - 1):
+            lo, hi = max(bounds[j], 0), bounds[j + 1]
+            if hi <= lo:
+                continue
+            if par["ks"] is not None:
+                kf = oracle.dequant_e4m3_blocks(par["k"][lo:hi].numpy(), par["ks"].numpy(), w.scale_block, t0=lo)
+                vf = oracle.dequant_e4m3_blocks(par["v"][lo:hi].numpy(), par["vs"].numpy(), w.scale_block, t0=lo)
+            else:
+                kf = oracle.bf16_bits_to_f64(par["k"][lo:hi].view(torch.int16).numpy())
+                vf = oracle.bf16_bits_to_f64(par["v"][lo:hi].view(torch.int16).numpy())
+            kv_pos = np.arange(lo, hi) if q_pos is not None else None
+            o, l = oracle.attend(qf.reshape(R * G, dk), kf, vf, w.scale, q_pos, kv_pos)
+            o_parts.append(o)
+            l_parts.append(l)
+        if o_parts:
+            mo, ml = oracle.merge_lse(np.stack(o_parts), np.stack(l_parts))
+        else:
+            mo, ml = np.zeros((R * G, w.dv)), np.full(R * G, -np.inf)
+        mo, ml = mo.reshape(R, G, w.dv), ml.reshape(R, G)
+        got_l = par["lse"].numpy().astype(np.float64)
+        fin = np.isfinite(ml)
+        return {"sample": f"batch 0, KV head 0: {R} of {w.Tq} row(s) x {G} heads, {n_tok} tokens",
+                "out_max_abs_err": float(np.max(np.abs(par["out"].numpy() - mo))),
+                "lse_max_abs_err": float(np.max(np.abs(got_l[fin] - ml[fin]))) if fin.any() else 0.0,
+                "empty_rows_match": bool(np.array_equal(np.isneginf(got_l), ~fin))}
     except Exception as e:  # the parity sample must never cost the bench line
         return {"error": f"{type(e).__name__}: {e}"[:200]}
 
@@ -387,16 +411,34 @@ def reference_arm(args, w, ws, rank):
 
 # --------------------------------------------------------------------------- GPU arm
 
-def ours_arm(args, w, ws, rank, local):
+# Workloads measured after the main one in the default run (one GPU): the long-context KVP
+# decode at S = 2^20 (fp8), the MLA absorbed decode, and the ring-prefill chunk both as one
+# fused call and as eight pass-KV ring steps.  Each gets its own timed region, clock record
+# and parity sample, reported under "workloads" in the same JSON line.
+EXTRA_WORKLOADS = (W.HELIX_KVP8_FP8_1M.name, W.MLA_ABSORBED.name, W.RING_PREFILL.name, W.RING_PREFILL_STEPS.name)
+
+# The parity sample of a decode group holds its whole sequence up to this many tokens (the
+# oracle then walks it one split at a time, so host memory stays at one split's rows).
+PARITY_MAX_TOKENS = 1 << 20
+
+
+def measure(args, w, ws, rank, local, want_e2e, want_parity):
+    """One workload on this rank's GPU: warm-up, the two timed passes (pass 1 gives value
+    and ms_per_step, pass 2 the per-step spread and the library's own kernel times), the
+    clocks sampled during both, and optionally the
+    end-to-end run from pinned host buffers and one (batch, KV head) group's inputs and
+    result for the oracle parity sample.  Returns a dict; time is the max over ranks."""
     import mla_decode_attention_gqa_gb300 as skv
 
     dev = torch.device("cuda", local)
     t0 = time.time()
     inp = W.make_inputs(w, dev)
     torch.cuda.synchronize()
-    log(f"[rank {rank}] inputs ready in {time.time() - t0:.1f}s")
+    log(f"[rank {rank}] {w.name}: inputs ready in {time.time() - t0:.1f}s")
     kw = dict(k_scale=inp["k_scale"], v_scale=inp["v_scale"], softmax_scale=w.scale, scale_block=w.scale_block)
-    bounds = inp["split_bounds"]
+    bounds = inp["split_bounds"]  # host copy: the algorithmic byte and flop counts
+    # the library reads the split bounds in device memory: uploaded once, outside the timed region
+    inp["split_bounds_dev"] = bounds_dev = torch.tensor(bounds, dtype=torch.int32, device=dev)
     kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, inp["seq_lens_host"], bounds, mla=w.mla,
                            scale_block=w.scale_block)
     positional = inp["q_pos"] is not None  # zigzag / striped storage: the *_pos entry point
@@ -421,6 +463,7 @@ def ours_arm(args, w, ws, rank, local):
         kw = dict(k_scale=inp.get("k_scale_pages"), v_scale=inp.get("v_scale_pages"), softmax_scale=w.scale,
                   scale_block=w.scale_block)
 
+    o_acc = lse_acc = None
     if w.ring_steps:  # pass-KV ring: every step's KV block in its own buffer
         C = w.S // w.n_split
         ring_blocks = [(inp["k"][:, :, j * C:(j + 1) * C].contiguous(), inp["v"][:, :, j * C:(j + 1) * C].contiguous(),
@@ -442,20 +485,20 @@ def ours_arm(args, w, ws, rank, local):
         elif w.ring_steps:
             ring_run(inp["q"], ring_blocks)
         elif w.paged:
-            skv.gqa_decode_attn_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["seq_lens"], bounds,
+            skv.gqa_decode_attn_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["seq_lens"], bounds_dev,
                                       inp["block_table"], w.causal_offset, out=out, lse=lse, **kw)
         elif positional:
-            skv.gqa_decode_attn_pos(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, inp["q_pos"], inp["k_pos"],
-                                    out=out, lse=lse, **kw)
+            skv.gqa_decode_attn_pos(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds_dev, inp["q_pos"],
+                                    inp["k_pos"], out=out, lse=lse, **kw)
         else:
-            skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, out=out,
+            skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds_dev, w.causal_offset, out=out,
                                 lse=lse, **kw)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if skv.device_error() != 0:
-        raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+        raise RuntimeError(f"{w.name}: a kernel reported a timed-out wait during warm-up")
 
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -489,35 +532,37 @@ def ours_arm(args, w, ws, rank, local):
     kernel_ms, kernel_launches = skv.kernel_timing_read()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     if skv.device_error() != 0:
-        raise RuntimeError("a kernel reported a timed-out wait in the timed region")
+        raise RuntimeError(f"{w.name}: a kernel reported a timed-out wait in the timed region")
 
     max_total_ms = max_over_ranks(total_ms, ws)
     all_bytes = sum_over_ranks(float(kv_bytes) * args.steps, ws)
-    value_gbs = all_bytes / (max_total_ms * 1e-3) / 1e9
-    ms_per_step = max_total_ms / args.steps
+    res = {"kv_bytes": kv_bytes, "flops": flops, "ms_per_step": max_total_ms / args.steps,
+           "value_gbs": all_bytes / (max_total_ms * 1e-3) / 1e9, "kernel_ms": kernel_ms,
+           "kernel_launches": kernel_launches, "step_ms": step_ms, "clocks": clocks, "par": None, "e2e": None}
 
     # one (batch, KV head) group's inputs and the timed steps' result for it, kept on the host
-    # for the cpu_baseline leg's parity sample (plain caches with at most ORACLE_MAX_TOKENS
-    # tokens in the group; a long query chunk keeps every (Tq / ORACLE_MAX_ROWS)-th row)
-    par = None
-    if not args.no_cpu_baseline and not (w.paged or w.passq_ranks or w.ring_steps or positional):
+    # for the oracle parity sample (plain caches with at most PARITY_MAX_TOKENS tokens in the
+    # group; a long query chunk keeps every (Tq / ORACLE_MAX_ROWS)-th row)
+    if want_parity and not (w.paged or w.passq_ranks or positional):
         try:
             G = w.Hq // w.Hkv
             n_tok = inp["seq_lens_host"][0]
             rows = list(range(w.Tq)) if w.Tq <= ORACLE_MAX_ROWS else list(range(0, w.Tq, w.Tq // ORACLE_MAX_ROWS))
-            if n_tok <= ORACLE_MAX_TOKENS:
+            if n_tok <= PARITY_MAX_TOKENS:
                 fp8 = w.kv_dtype == "fp8_e4m3"
-                par = {"n_tok": n_tok, "rows": rows,
-                       "q": inp["q"][0, rows, :G].contiguous().cpu(),
-                       "k": inp["k"][0, 0, :n_tok].contiguous().cpu(), "v": inp["v"][0, 0, :n_tok].contiguous().cpu(),
-                       "ks": inp["k_scale"][0, 0].cpu() if fp8 else None, "vs": inp["v_scale"][0, 0].cpu() if fp8 else None,
-                       "out": out[0, rows, :G].float().cpu(), "lse": lse[0, rows, :G].cpu()}
+                res_o, res_l = (o_acc, lse_acc) if w.ring_steps else (out, lse)
+                res["par"] = {"n_tok": n_tok, "rows": rows,
+                              "q": inp["q"][0, rows, :G].contiguous().cpu(),
+                              "k": inp["k"][0, 0, :n_tok].contiguous().cpu(),
+                              "v": inp["v"][0, 0, :n_tok].contiguous().cpu(),
+                              "ks": inp["k_scale"][0, 0].cpu() if fp8 else None,
+                              "vs": inp["v_scale"][0, 0].cpu() if fp8 else None,
+                              "out": res_o[0, rows, :G].float().cpu(), "lse": res_l[0, rows, :G].cpu()}
         except Exception as e:  # the parity sample must never cost the bench line
-            par = {"error": f"{type(e).__name__}: {e}"[:200]}
+            res["par"] = {"error": f"{type(e).__name__}: {e}"[:200]}
 
     # e2e: the public call with host (pinned) inputs; copies in and the result back every step
-    e2e = None
-    if not args.no_e2e:
+    if want_e2e:
         host = {}
         # the MLA value cache is a view of the latent (k): it is copied once, as k
         if w.ring_steps:
@@ -525,12 +570,12 @@ def ours_arm(args, w, ws, rank, local):
         elif w.passq_ranks:
             keys = ("q", "k_shards", "v_shards", "k_shard_scale", "v_shard_scale", "shard_lens")
         elif w.paged:
-            keys = ("q", "k_pages", "seq_lens", "block_table") + (() if w.mla else ("v_pages",)) + (
+            keys = ("q", "k_pages", "seq_lens", "split_bounds_dev", "block_table") + (() if w.mla else ("v_pages",)) + (
                 ("k_scale_pages", "v_scale_pages") if w.kv_dtype != "bf16" else ())
         elif w.mla:
-            keys = ("q", "k", "k_scale", "v_scale", "seq_lens")
+            keys = ("q", "k", "k_scale", "v_scale", "seq_lens", "split_bounds_dev")
         else:
-            keys = ("q", "k", "v", "k_scale", "v_scale", "seq_lens", "q_pos", "k_pos")
+            keys = ("q", "k", "v", "k_scale", "v_scale", "seq_lens", "split_bounds_dev", "q_pos", "k_pos")
         for key in keys:
             t = inp.get(key)
             host[key] = None if t is None else t.cpu().pin_memory()
@@ -569,13 +614,14 @@ def ours_arm(args, w, ws, rank, local):
             elif w.paged:
                 e2e_kw.update(k_scale=dev_bufs.get("k_scale_pages"), v_scale=dev_bufs.get("v_scale_pages"))
                 skv.gqa_decode_attn_paged(dev_bufs["q"], dev_bufs["k_pages"], dev_bufs["v_pages"], dev_bufs["seq_lens"],
-                                          bounds, dev_bufs["block_table"], w.causal_offset, **e2e_kw)
+                                          dev_bufs["split_bounds_dev"], dev_bufs["block_table"], w.causal_offset,
+                                          **e2e_kw)
             elif positional:
-                skv.gqa_decode_attn_pos(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
-                                        dev_bufs["q_pos"], dev_bufs["k_pos"], **e2e_kw)
+                skv.gqa_decode_attn_pos(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"],
+                                        dev_bufs["split_bounds_dev"], dev_bufs["q_pos"], dev_bufs["k_pos"], **e2e_kw)
             else:
-                skv.gqa_decode_attn(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"], bounds,
-                                    w.causal_offset, **e2e_kw)
+                skv.gqa_decode_attn(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["seq_lens"],
+                                    dev_bufs["split_bounds_dev"], w.causal_offset, **e2e_kw)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
@@ -593,15 +639,20 @@ def ours_arm(args, w, ws, rank, local):
         barrier(ws)
         e2e_ms = max_over_ranks(a.elapsed_time(b), ws)
         e2e_bytes = sum_over_ranks(float(kv_bytes) * e2e_steps, ws)
-        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / e2e_steps, 3)}
+        res["e2e"] = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": round(e2e_ms / e2e_steps, 3)}
+    return res
 
-    if rank != 0:
-        return
-    # dominant kernel: the attention kernel (split-KV partial / tensor-core); its device time
-    # per step comes from the events the library records around it in the timed region
-    # (a step of a ring workload holds several launches, each over 1/n of the work)
-    step_s = (kernel_ms / args.steps) * 1e-3 if kernel_launches > 0 else statistics.mean(step_ms) * 1e-3
+
+def roofline_of(w, m, steps):
+    """The dominant kernel's roofline: algorithmic bytes (decode: HBM-bound) or flops (a
+    query chunk: tensor-bound) over its own device time from the library's events in pass
+    2 (a ring step workload holds several launches per step, each over 1/n of the work)."""
+    step_ms = m["step_ms"]
+    kernel_ms, kernel_launches = m["kernel_ms"], m["kernel_launches"]
+    kv_bytes, flops = m["kv_bytes"], m["flops"]
+    step_s = (kernel_ms / steps) * 1e-3 if kernel_launches > 0 else statistics.mean(step_ms) * 1e-3
     hbm, hbm_kind = hbm_peak()
     tc, tc_kind = bf16_peak()
     tensor_bound = w.Tq > 1  # the prefill chunk is a dense contraction; decode streams KV
@@ -611,30 +662,65 @@ def ours_arm(args, w, ws, rank, local):
     else:
         roof = {"bound": "hbm", "achieved": round(kv_bytes / step_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(kv_bytes / step_s / 1e9 / hbm, 4), "peak_kind": hbm_kind}
-    roof.update({"kernel_ms_per_step": round(kernel_ms / args.steps, 4), "kernel_launches": kernel_launches,
+    roof.update({"kernel_ms_per_step": round(kernel_ms / steps, 4), "kernel_launches": kernel_launches,
                  "step_frac": round((flops / (statistics.mean(step_ms) * 1e-3) / 1e12 / tc) if tensor_bound else
                                     (kv_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9 / hbm), 4),
                  "traffic": ncu_traffic(w.name),
-                 "algorithmic_bytes_per_launch": round(kv_bytes / max(1, kernel_launches // args.steps)),
-                 "flops_per_launch": round(flops / max(1, kernel_launches // args.steps)), "hbm_gbs": round(kv_bytes / step_s / 1e9, 1),
+                 "algorithmic_bytes_per_launch": round(kv_bytes / max(1, kernel_launches // steps)),
+                 "flops_per_launch": round(flops / max(1, kernel_launches // steps)),
+                 "hbm_gbs": round(kv_bytes / step_s / 1e9, 1),
                  "hbm_frac_of_nominal_8tbs": round(kv_bytes / step_s / 1e9 / 8000.0, 4),
                  "tflops": round(flops / step_s / 1e12, 2), "tensor_frac": round(flops / step_s / 1e12 / tc, 4)})
+    return roof
+
+
+def workload_summary(w, m, steps, parity):
+    """Compact record of one extra workload for the "workloads" block: time per layer, the
+    dominant kernel's time and roofline fractions (HBM and bf16 tensor, of the measured
+    peaks), the clocks sampled during its timed region and the oracle parity sample."""
+    r = roofline_of(w, m, steps)
+    c = m["clocks"]
+    return {"ms_per_step": round(m["ms_per_step"], 4), "us_per_layer": round(m["ms_per_step"] * 1e3, 2),
+            "kernel_ms_per_step": r["kernel_ms_per_step"], "bound": r["bound"], "frac": r["frac"],
+            "step_frac": r["step_frac"], "hbm_gbs": r["hbm_gbs"], "hbm_frac": round(r["hbm_gbs"] / hbm_peak()[0], 4),
+            "tflops": r["tflops"], "tensor_frac": r["tensor_frac"], "traffic": r["traffic"],
+            "gpu_launches": launches_per_step(w) * steps,
+            "clocks": {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"), "reasons": c.get("reasons")},
+            "parity": parity}
+
+
+def ours_arm(args, w, ws, rank, local):
+    want_par = not args.no_cpu_baseline
+    m = measure(args, w, ws, rank, local, want_e2e=not args.no_e2e, want_parity=want_par)
+    torch.cuda.empty_cache()
+    extras = {}
+    for name in args.extra_names:
+        we = workload_by_name(name)
+        me = measure(args, we, ws, rank, local, want_e2e=False, want_parity=want_par)
+        torch.cuda.empty_cache()
+        if rank == 0:
+            par = oracle_parity(we, me["par"]) if me["par"] is not None else None
+            extras[name] = workload_summary(we, me, args.steps, par)
+    if rank != 0:
+        return
+    roof = roofline_of(w, m, args.steps)
     cpu = None
-    if not args.no_cpu_baseline and ws >= 1:
+    if not args.no_cpu_baseline:
         b, s, g, t, r = oracle_sample(w, budget_s=args.cpu_budget)
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": _CORES, "kind": "oracle",
                "sample": oracle_sample_text(w, g, t, r) + f", {s:.1f} s"}
-        if par is not None:
-            cpu["parity"] = oracle_parity(w, par)
+        if m["par"] is not None:
+            cpu["parity"] = oracle_parity(w, m["par"])
+    step_ms = m["step_ms"]
     line = {
         "metric": METRIC,
-        "value": round(value_gbs, 2),
+        "value": round(m["value_gbs"], 2),
         "unit": "GB/s",
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4),
-        "us_per_layer": round(ms_per_step * 1e3, 2),
+        "ms_per_step": round(m["ms_per_step"], 4),
+        "us_per_layer": round(m["ms_per_step"] * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -642,13 +728,15 @@ def ours_arm(args, w, ws, rank, local):
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V)",
         "config": config_of(w, ws),
         "roofline": roof,
-        "clocks": clocks,
+        "clocks": m["clocks"],
         "gpu_launches": launches_per_step(w) * args.steps,
-        "e2e": e2e,
+        "e2e": m["e2e"],
         "cpu_baseline": cpu,
         "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),
                                    round(max(step_ms), 4)],
     }
+    if extras:
+        line["workloads"] = extras
     print(json.dumps(line), flush=True)
 
 
@@ -665,6 +753,10 @@ def main():
     ap.add_argument("--S", type=int, default=None, help="smaller KV length of the same workload (profiling)")
     ap.add_argument("--B", type=int, default=None, help="smaller batch of the same workload (profiling)")
     ap.add_argument("--Tq", type=int, default=None, help="fewer query rows of the same workload (profiling)")
+    ap.add_argument("--extras", default="auto",
+                    help="workloads measured after the main one: 'auto' (the long-context fp8 decode, the MLA "
+                         "decode and the ring-prefill chunk fused and as ring steps, when the default workload runs "
+                         "unscaled on one GPU), 'none', or a comma-separated list of workload names")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -673,6 +765,12 @@ def main():
     if over:
         w = W.scaled(w, **over)
     ws, rank, local = dist_setup()
+    if args.extras == "auto":
+        args.extra_names = list(EXTRA_WORKLOADS) if (ws == 1 and not over and w.name == W.HELIX_DENSE_128K.name) else []
+    elif args.extras == "none":
+        args.extra_names = []
+    else:
+        args.extra_names = [workload_by_name(n).name for n in args.extras.split(",") if n]
     if args.impl == "reference":
         reference_arm(args, w, ws, rank)
     else:

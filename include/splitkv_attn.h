@@ -35,6 +35,19 @@
  *       t <= causal_offset + i.
  *     Decode passes a causal_offset >= S_max (SKV_NO_CAUSAL) so nothing is masked;
  *     a prefill chunk whose first row sits at global position P passes P.
+ *   - Split bounds are a DEVICE int32 array [B][n_split + 1] (like seq_lens), read by the
+ *     kernels and never by the host, so a call needs no host-to-device copy and takes any
+ *     batch size.  Each row should be non-decreasing; the kernels clip every split to
+ *     [0, min(seq_lens[b], S_max)) and treat a split whose upper bound does not exceed its
+ *     lower one as empty, so no row of bounds can make a kernel read outside the caches
+ *     (but overlapping splits count their common tokens once per split).  The calls that
+ *     merge their splits in one kernel (see gqa_decode_attn) attend over
+ *     [bounds[b][0], bounds[b][n_split]).
+ *   - Work decomposition: long splits are cut into chunks so that one launch fills the
+ *     GPU.  The host plans for splits of about S_max / n_split tokens and every split is
+ *     cut into the same number of chunks, sized on the device from the split's own length;
+ *     splits of very unequal length therefore load the GPU unevenly (the result is the
+ *     same).
  *   - Partials: o is normalised by its own softmax denominator and lse is the
  *     natural log of that denominator over scaled scores (softmax_scale * q.k).
  *     A split with no visible token has o = 0 and lse = -inf.
@@ -126,8 +139,7 @@ skv_status splitkv_kernel_timing_read(float* total_ms, int32_t* launches);
  *   k_scale      fp8: fp32 [B][Hkv][ceil(S_max / scale_block)] contiguous; NULL for bf16
  *   v_scale      fp8: same layout; NULL for bf16
  *   seq_lens     DEVICE int32 [B]; 0 <= seq_lens[b] <= S_max
- *   split_bounds HOST int32 [B][n_split + 1], non-decreasing per row, bounds[b][0] >= 0;
- *                B * (n_split + 1) <= 2048.  Copied at the call (by value into the launch).
+ *   split_bounds DEVICE int32 [B][n_split + 1], contiguous, 4-byte aligned (see Conventions)
  *   n_split      >= 1
  *   causal_offset  see Visibility above
  *   out_partial  fp32 [n_split][B][Tq][Hq][dv] contiguous, 16-byte aligned
@@ -138,8 +150,7 @@ skv_status splitkv_kernel_timing_read(float* total_ms, int32_t* launches);
  * Alignment: q, k_cache, v_cache 16-byte aligned; q strides multiples of 8 elements; K/V
  * token/head/batch strides multiples of 16 bytes.
  */
-skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
-                                       size_t* bytes);
+skv_status attn_partial_workspace_size(const skv_desc* desc, int32_t n_split, size_t* bytes);
 skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                         const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                         const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
@@ -162,9 +173,12 @@ skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, in
  * every query row over the union of its splits, written as bf16 out [B][Tq][Hq][dv] and
  * fp32 lse [B][Tq][Hq] (contiguous).  Arguments as attn_partial; the per-split / per-chunk
  * partials live in the caller's workspace of at least gqa_decode_attn_workspace_size() bytes.
+ * Kernels by shape: bf16 KV with dk = dv = 128, Hq / Hkv dividing 128 and at least 128
+ * (query row, head) rows per KV head runs one tensor-core kernel that merges the splits
+ * on the fly (workspace size 0; out must be 16-byte aligned); every other shape runs a
+ * split-KV partial kernel into the workspace and the merge kernel.
  */
-skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
-                                          size_t* bytes);
+skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, int32_t n_split, size_t* bytes);
 skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                            const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
@@ -179,11 +193,18 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
  * latency-critical path where an allocation (which may synchronise the whole device) is not
  * acceptable, or a foreign-language caller that only has the C ABI and no device allocator.
  * This entry point takes the same arguments as gqa_decode_attn minus the workspace and
- * allocates nothing: the per-split / per-chunk partials go to a fixed scratch array of
- * 32 MiB (33554432 bytes) compiled into the library, which every GPU that loads the library
- * keeps reserved until the process exits.
- *   - A problem whose partials need more than 32 MiB (B * Tq * Hq * (dv + 1) * 4 bytes per
- *     part, rounded) is rejected with SKV_EWORKSPACE and a message giving both sizes.
+ * allocates nothing.
+ *   - The tensor-core shapes (see gqa_decode_attn) run the same fused kernel as
+ *     gqa_decode_attn, which needs no scratch at all.
+ *   - Every other shape runs the same partial and merge kernels, with the per-split /
+ *     per-chunk partials in a fixed scratch array of 32 MiB (33554432 bytes) compiled into
+ *     the library, which every GPU that loads the library keeps reserved until the process
+ *     exits.  When gqa_decode_attn's plan would need more than that, the work is planned
+ *     again with as many chunks per split as the scratch holds (same result, possibly a
+ *     less even load).  A part needs B * Tq * Hq * (dv + 1) * 4 bytes (each of its two
+ *     arrays rounded up to 256 bytes); if even n_split parts (one chunk per split) exceed
+ *     32 MiB the call returns SKV_EWORKSPACE, with both sizes in the message, before
+ *     anything is launched.
  *   - The first call on each device looks up the scratch array's device address (with that
  *     device current) and caches it; make that first call before any stream capture.
  *   - Every call on a device uses the same scratch array, so calls that may overlap on the
@@ -285,7 +306,8 @@ skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, c
  *            normalised output and natural-log LSE, updated in place; rows that have seen
  *            no token yet hold o = 0, lse = -inf
  *   workspace  DEVICE, at least attn_ring_step_workspace_size(desc) bytes, 256-aligned
- * Errors as for attn_partial; the merge is the same one attn_merge_lse applies.
+ * No bounds table: the block is one split [0, S_max).  Errors as for attn_partial; the merge
+ * is the same one attn_merge_lse applies.
  */
 skv_status attn_ring_step_workspace_size(const skv_desc* desc, size_t* bytes);
 
@@ -326,8 +348,8 @@ skv_status attn_ring_step(const skv_desc* desc, const void* q, const void* k_blo
  * on rank (k - s) mod n_ranks and writes its partial to that owner's slot from rank k.  One
  * partial launch covers every rank and step; one merge launch covers the exchange and the
  * merge.  Caller owns every buffer; the library allocates nothing.
- * Errors: as gqa_decode_attn, plus SKV_EINVAL for n_ranks < 1, B not a multiple of n_ranks or
- * n_ranks * B above 1024; SKV_EUNSUPPORTED for Tq != 1 or the MLA latent shape.
+ * Errors: as gqa_decode_attn, plus SKV_EINVAL for n_ranks < 1 or B not a multiple of n_ranks;
+ * SKV_EUNSUPPORTED for Tq != 1 or the MLA latent shape.
  */
 skv_status gqa_decode_attn_passq_workspace_size(const skv_desc* desc, int32_t n_ranks, size_t* bytes);
 

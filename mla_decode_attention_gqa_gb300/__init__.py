@@ -6,10 +6,14 @@ provides device memory (outputs, workspace) and the current CUDA stream.  There 
 no CPU fallback: the first call loads the library and raises if it is missing, and
 every call fails if its tensors are not on a CUDA device.
 
+split_bounds is an int32 tensor [B, n_split + 1] on the call's device (the C ABI reads
+it in device memory); a nested list is accepted and copied to the device at each call.
+
 Entry points (same names as the C ABI):
   attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out_partial, lse_partial)
   attn_merge_lse(out_partials, lse_partials) -> (out, lse)
   gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, ...) -> (out, lse)
+  gqa_decode_attn_noalloc(...) -> (out, lse)   (no workspace: the library's own scratch)
   gqa_decode_attn_passq(q, k_shards, v_shards, shard_lens, ...) -> (out, lse)
 plus the position-masked (_pos), paged (_paged) and pass-KV ring-step variants.
 """
@@ -104,21 +108,24 @@ def _load():
     lib.splitkv_kernel_timing_read.restype = I32
     for name in ("attn_partial_workspace_size", "gqa_decode_attn_workspace_size"):
         f = getattr(lib, name)
-        f.argtypes = [D, I32P, I32, ctypes.POINTER(SZ)]
+        f.argtypes = [D, I32, ctypes.POINTER(SZ)]
         f.restype = I32
-    common = [D, P, P, P, P, P, P, I32P, I32, I64]
+    # split_bounds is a device pointer, like seq_lens
+    common = [D, P, P, P, P, P, P, P, I32, I64]
     lib.attn_partial.argtypes = common + [P, P, P, SZ, P]
     lib.attn_partial.restype = I32
     lib.gqa_decode_attn.argtypes = common + [P, P, P, SZ, P]
     lib.gqa_decode_attn.restype = I32
+    lib.gqa_decode_attn_noalloc.argtypes = common + [P, P, P]
+    lib.gqa_decode_attn_noalloc.restype = I32
     lib.attn_merge_lse.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P]
     lib.attn_merge_lse.restype = I32
-    common_pos = [D, P, P, P, P, P, P, I32P, I32, P, P]  # q_pos, k_pos replace causal_offset
+    common_pos = [D, P, P, P, P, P, P, P, I32, P, P]  # q_pos, k_pos replace causal_offset
     lib.attn_partial_pos.argtypes = common_pos + [P, P, P, SZ, P]
     lib.attn_partial_pos.restype = I32
     lib.gqa_decode_attn_pos.argtypes = common_pos + [P, P, P, SZ, P]
     lib.gqa_decode_attn_pos.restype = I32
-    common_paged = [D, ctypes.POINTER(SkvPaged), P, P, P, P, P, P, I32P, I32, I64]
+    common_paged = [D, ctypes.POINTER(SkvPaged), P, P, P, P, P, P, P, I32, I64]
     lib.attn_partial_paged.argtypes = common_paged + [P, P, P, SZ, P]
     lib.attn_partial_paged.restype = I32
     lib.gqa_decode_attn_paged.argtypes = common_paged + [P, P, P, SZ, P]
@@ -297,15 +304,23 @@ def make_desc(q, k_cache, v_cache, softmax_scale=None, scale_block=64):
     return d
 
 
-def _bounds_array(split_bounds, B):
+def _bounds_tensor(split_bounds, B, dev):
+    """The split bounds as the device int32 tensor [B, n_split + 1] the library reads.  A
+    tensor is checked and passed as it is; a nested list ([B][n_split + 1], or one row
+    shared by every sequence) is copied to the device here, once per call (pass a device
+    tensor to keep host-to-device copies out of a hot loop)."""
+    if isinstance(split_bounds, torch.Tensor):
+        t = split_bounds
+        if t.device != dev or t.dtype != torch.int32 or t.dim() != 2 or t.shape[0] != B or t.shape[1] < 2 \
+                or not t.is_contiguous():
+            raise ValueError(f"split_bounds must be a contiguous int32 tensor [B, n_split + 1] on {dev}")
+        return t, int(t.shape[1]) - 1
     rows = [list(map(int, r)) for r in split_bounds]
     if len(rows) == 1 and B > 1:
         rows = rows * B
-    if len(rows) != B or len({len(r) for r in rows}) != 1:
+    if len(rows) != B or len({len(r) for r in rows}) != 1 or len(rows[0]) < 2:
         raise ValueError("split_bounds must be [B][n_split+1] (or one row shared by every sequence)")
-    n_split = len(rows[0]) - 1
-    flat = (ctypes.c_int32 * (B * (n_split + 1)))(*[x for r in rows for x in r])
-    return flat, n_split
+    return torch.tensor(rows, dtype=torch.int32, device=dev), len(rows[0]) - 1
 
 
 _ws_cache = {}
@@ -334,7 +349,7 @@ def _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax
     _same_device(q.device, k_cache=k_cache, v_cache=v_cache, seq_lens=seq_lens, k_scale=k_scale, v_scale=v_scale)
     d = make_desc(q, k_cache, v_cache, softmax_scale, scale_block)
     _check_lens(seq_lens, d.B, "seq_lens")
-    bounds, n_split = _bounds_array(split_bounds, d.B)
+    bounds, n_split = (None, 1) if split_bounds is None else _bounds_tensor(split_bounds, d.B, q.device)
     if d.kv_dtype == SKV_KV_FP8_E4M3 and scale_block > 0:
         _check_scales((k_scale, v_scale), (d.B, d.Hkv, -(-d.S_max // scale_block)), "[B, Hkv, ceil(S / scale_block)]")
     return d, bounds, n_split
@@ -372,21 +387,21 @@ def _prep_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table, k_scal
     pg = SkvPaged()
     pg.block_len, pg.max_blocks, pg.num_blocks = L, block_table.shape[1], nb
     pg.block_table = block_table.data_ptr()
-    bounds, n_split = _bounds_array(split_bounds, B)
+    bounds, n_split = _bounds_tensor(split_bounds, B, q.device)
     if d.kv_dtype == SKV_KV_FP8_E4M3 and scale_block > 0:
         _check_scales((k_scale, v_scale), (nb, Hkv, L // scale_block), "[num_blocks, Hkv, block_len / scale_block]")
     return d, pg, bounds, n_split
 
 
-def attn_partial_workspace_size(desc, bounds, n_split):
+def attn_partial_workspace_size(desc, n_split):
     n = ctypes.c_size_t(0)
-    _check(_lib.attn_partial_workspace_size(ctypes.byref(desc), bounds, n_split, ctypes.byref(n)))
+    _check(_lib.attn_partial_workspace_size(ctypes.byref(desc), n_split, ctypes.byref(n)))
     return int(n.value)
 
 
-def gqa_decode_attn_workspace_size(desc, bounds, n_split):
+def gqa_decode_attn_workspace_size(desc, n_split):
     n = ctypes.c_size_t(0)
-    _check(_lib.gqa_decode_attn_workspace_size(ctypes.byref(desc), bounds, n_split, ctypes.byref(n)))
+    _check(_lib.gqa_decode_attn_workspace_size(ctypes.byref(desc), n_split, ctypes.byref(n)))
     return int(n.value)
 
 
@@ -399,10 +414,10 @@ def attn_partial(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_C
     dev = q.device
     out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
     lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
-    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    nbytes = attn_partial_workspace_size(d, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                             _ptr(seq_lens), bounds, n_split, int(causal_offset), _ptr(out_partial),
+                             _ptr(seq_lens), _ptr(bounds), n_split, int(causal_offset), _ptr(out_partial),
                              _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
     return out_partial, lse_partial
 
@@ -436,10 +451,26 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=N
     dev = q.device
     out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
     lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
-    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, n_split), dev)
     _check(_lib.gqa_decode_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                _ptr(seq_lens), bounds, n_split, int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
+                                _ptr(seq_lens), _ptr(bounds), n_split, int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws),
                                 ws_bytes, _stream()))
+    return out, lse
+
+
+@_on_tensor_device
+def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, split_bounds, causal_offset=NO_CAUSAL, k_scale=None,
+                            v_scale=None, softmax_scale=None, scale_block=64, out=None, lse=None):
+    """gqa_decode_attn without a workspace: the library keeps the partials in a fixed scratch
+    array of its own (32 MiB per device; calls that overlap on the GPU race for it)."""
+    d, bounds, n_split = _prep(q, k_cache, v_cache, seq_lens, split_bounds, k_scale, v_scale, softmax_scale,
+                               scale_block)
+    dev = q.device
+    out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
+    lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
+    _check(_lib.gqa_decode_attn_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                        _ptr(v_scale), _ptr(seq_lens), _ptr(bounds), n_split, int(causal_offset),
+                                        _ptr(out), _ptr(lse), _stream()))
     return out, lse
 
 
@@ -462,10 +493,10 @@ def attn_partial_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_pos, 
     dev = q.device
     out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
     lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
-    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    nbytes = attn_partial_workspace_size(d, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                 _ptr(v_scale), _ptr(seq_lens), bounds, n_split, _ptr(q_pos), _ptr(k_pos),
+                                 _ptr(v_scale), _ptr(seq_lens), _ptr(bounds), n_split, _ptr(q_pos), _ptr(k_pos),
                                  _ptr(out_partial), _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
     return out_partial, lse_partial
 
@@ -480,9 +511,9 @@ def gqa_decode_attn_pos(q, k_cache, v_cache, seq_lens, split_bounds, q_pos, k_po
     dev = q.device
     out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
     lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
-    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, n_split), dev)
     _check(_lib.gqa_decode_attn_pos(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                    _ptr(v_scale), _ptr(seq_lens), bounds, n_split, _ptr(q_pos), _ptr(k_pos),
+                                    _ptr(v_scale), _ptr(seq_lens), _ptr(bounds), n_split, _ptr(q_pos), _ptr(k_pos),
                                     _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream()))
     return out, lse
 
@@ -498,10 +529,10 @@ def attn_partial_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_table,
     dev = q.device
     out_partial = _out(out_partial, (n_split, d.B, d.Tq, d.Hq, d.dv), torch.float32, dev, "out_partial")
     lse_partial = _out(lse_partial, (n_split, d.B, d.Tq, d.Hq), torch.float32, dev, "lse_partial")
-    nbytes = attn_partial_workspace_size(d, bounds, n_split)
+    nbytes = attn_partial_workspace_size(d, n_split)
     ws = _workspace(nbytes, dev)
     _check(_lib.attn_partial_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
-                                   _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), bounds, n_split, int(causal_offset),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), _ptr(bounds), n_split, int(causal_offset),
                                    _ptr(out_partial), _ptr(lse_partial), _ptr(ws), nbytes, _stream()))
     return out_partial, lse_partial
 
@@ -516,9 +547,9 @@ def gqa_decode_attn_paged(q, k_pages, v_pages, seq_lens, split_bounds, block_tab
     dev = q.device
     out = _out(out, (d.B, d.Tq, d.Hq, d.dv), torch.bfloat16, dev, "out")
     lse = _out(lse, (d.B, d.Tq, d.Hq), torch.float32, dev, "lse")
-    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, bounds, n_split), dev)
+    ws, ws_bytes = _ws_arg(workspace, gqa_decode_attn_workspace_size(d, n_split), dev)
     _check(_lib.gqa_decode_attn_paged(ctypes.byref(d), ctypes.byref(pg), _ptr(q), _ptr(k_pages), _ptr(v_pages),
-                                      _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), bounds, n_split,
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(seq_lens), _ptr(bounds), n_split,
                                       int(causal_offset), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream()))
     return out, lse
 
@@ -531,8 +562,7 @@ def attn_ring_step(q, k_block, v_block, seq_lens, o_acc, lse_acc, causal_offset=
     [B,Tq,Hq] in place (written, not read, when first).  Returns (o_acc, lse_acc)."""
     _require_cuda(o_acc, lse_acc)
     _same_device(q.device, o_acc=o_acc, lse_acc=lse_acc)
-    d, _, _ = _prep(q, k_block, v_block, seq_lens, [[0, k_block.shape[2]]], k_scale, v_scale, softmax_scale,
-                    scale_block)
+    d, _, _ = _prep(q, k_block, v_block, seq_lens, None, k_scale, v_scale, softmax_scale, scale_block)
     for t, shape, name in ((o_acc, (d.B, d.Tq, d.Hq, d.dv), "o_acc"), (lse_acc, (d.B, d.Tq, d.Hq), "lse_acc")):
         if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape:
             raise ValueError(f"{name} must be contiguous float32 of shape {shape}")
@@ -604,6 +634,7 @@ __all__ = [
     "attn_partial_pos",
     "attn_merge_lse",
     "gqa_decode_attn",
+    "gqa_decode_attn_noalloc",
     "gqa_decode_attn_pos",
     "make_desc",
     "device_error",

@@ -122,7 +122,6 @@ struct Plan {
   int rows_per_cta = 0;
   int m_tiles = 1;
   int n_chunk = 1;
-  int chunk_tiles = 1;
   int64_t n_items = 0;
   int n_part = 0;  // n_split * n_chunk
 };
@@ -143,7 +142,9 @@ bool is_gqa_shape(const skv_desc* d) {
   return d->dk == 128;
 }
 
-skv_status validate(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
+// Shape, dtype and stride checks of a call (the split bounds live in device memory and are
+// never read on the host).
+skv_status validate(const skv_desc* d, int32_t n_split) {
   if (!d) return fail(SKV_EINVAL, "desc is NULL");
   if (d->B <= 0 || d->Tq <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->dk <= 0 || d->dv <= 0)
     return fail(SKV_EINVAL, "B, Tq, Hq, Hkv, dk, dv must be positive");
@@ -155,15 +156,8 @@ skv_status validate(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
   if (d->kv_dtype == SKV_KV_FP8_E4M3 && (d->scale_block <= 0 || d->scale_block % kTileN))
     return fail(SKV_EINVAL, "scale_block must be a positive multiple of 64 for fp8 KV");
   if (n_split < 1) return fail(SKV_EINVAL, "n_split must be >= 1");
-  if (static_cast<int64_t>(d->B) * (n_split + 1) > kMaxBounds)
-    return fail(SKV_EINVAL, "B * (n_split + 1) must be <= 2048");
-  if (!bounds) return fail(SKV_EINVAL, "split_bounds is NULL");
-  for (int b = 0; b < d->B; ++b) {
-    const int32_t* r = bounds + static_cast<int64_t>(b) * (n_split + 1);
-    if (r[0] < 0) return fail(SKV_EINVAL, "split_bounds must be >= 0");
-    for (int j = 0; j < n_split; ++j)
-      if (r[j + 1] < r[j]) return fail(SKV_EINVAL, "split_bounds must be non-decreasing per sequence");
-  }
+  if (static_cast<int64_t>(d->B) * (n_split + 1) >= (int64_t(1) << 31))
+    return fail(SKV_EINVAL, "B * (n_split + 1) must be below 2^31");
   for (int i = 0; i < 3; ++i) {
     if (d->q_strides[i] < 0 || d->k_strides[i] < 0 || d->v_strides[i] < 0)
       return fail(SKV_EINVAL, "strides must be non-negative");
@@ -202,7 +196,18 @@ skv_status validate_ptrs(const skv_desc* d, const void* q, const void* k, const 
   return SKV_OK;
 }
 
-Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
+// The caller's split-bounds table: a device int32 array [B][n_split + 1].
+skv_status validate_bounds(const int32_t* bounds) {
+  if (!bounds) return fail(SKV_EINVAL, "split_bounds is NULL");
+  if (!aligned(bounds, 4)) return fail(SKV_EINVAL, "split_bounds must be 4-byte aligned");
+  return SKV_OK;
+}
+
+// Work decomposition of a partial launch.  Long splits are cut into chunks so that the grid
+// fills the GPU; the host does not read the split bounds, so it plans for splits of the
+// allocated S_max cut into n_split equal parts, and each item sizes its chunk from its own
+// split's length on the device.  max_chunk > 0 caps the chunks per split.
+Plan make_plan(const skv_desc* d, int32_t n_split, int max_chunk = 0) {
   Plan pl;
   const int G = d->Hq / d->Hkv;
   const bool fp8 = d->kv_dtype == SKV_KV_FP8_E4M3;
@@ -220,26 +225,19 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
   const int64_t rows = static_cast<int64_t>(d->Tq) * G;
   pl.m_tiles = static_cast<int>((rows + li.rows_per_cta - 1) / li.rows_per_cta);
 
-  // longest split, in tiles of its tile-aligned window
-  int64_t max_tiles = 0;
-  for (int b = 0; b < d->B; ++b) {
-    const int32_t* r = bounds + static_cast<int64_t>(b) * (n_split + 1);
-    for (int j = 0; j < n_split; ++j) {
-      const int64_t lo = (r[j] / kTileN) * kTileN;
-      const int64_t hi = std::min<int64_t>(r[j + 1], d->S_max);
-      if (hi > lo) max_tiles = std::max<int64_t>(max_tiles, (hi - lo + kTileN - 1) / kTileN);
-    }
-  }
+  // expected split length in tiles: S_max cut into n_split equal splits
+  const int64_t split_tok = (d->S_max + n_split - 1) / n_split;
+  const int64_t max_tiles = (split_tok + kTileN - 1) / kTileN;
   const int64_t base = static_cast<int64_t>(d->B) * d->Hkv * n_split * pl.m_tiles;
   const int64_t slots =  // work items resident at once
       std::max<int64_t>(1, static_cast<int64_t>(device_sm_count()) * li.ctas_per_sm / li.ctas_per_item);
   pl.n_chunk = 1;
-  pl.chunk_tiles = static_cast<int>(std::max<int64_t>(max_tiles, 1));
-  if (max_tiles > 1 && base < 4 * slots) {
+  if (max_tiles > 1 && base < 4 * slots && max_chunk != 1) {
     // Cut every split into n chunks so that the grid fills the GPU in whole waves;
     // cost model: waves * (tiles per chunk + per-CTA overhead of ~3 tiles).
     double best = 1e300;
-    const int64_t n_hi = std::min<int64_t>(max_tiles, 512);
+    int64_t n_hi = std::min<int64_t>(max_tiles, 512);
+    if (max_chunk > 0) n_hi = std::min<int64_t>(n_hi, max_chunk);
     for (int64_t n = 1; n <= n_hi; ++n) {
       const int64_t ct = (max_tiles + n - 1) / n;
       const int64_t nn = (max_tiles + ct - 1) / ct;
@@ -248,7 +246,6 @@ Plan make_plan(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
       if (cost < best * 0.999) {
         best = cost;
         pl.n_chunk = static_cast<int>(nn);
-        pl.chunk_tiles = static_cast<int>(ct);
       }
     }
   }
@@ -367,10 +364,9 @@ skv_status fill_params(PartialParams* p, const skv_desc* d, const Plan& pl, cons
   p->S_max = static_cast<int32_t>(d->S_max);
   p->n_split = n_split;
   p->n_chunk = pl.n_chunk;
-  p->chunk_tiles = pl.chunk_tiles;
   p->m_tiles = pl.m_tiles;
   p->zero_empty = zero_empty ? 1 : 0;
-  for (int i = 0; i < d->B * (n_split + 1); ++i) p->bounds[i] = bounds[i];
+  p->bounds = bounds;
   return SKV_OK;
 }
 
@@ -407,10 +403,9 @@ skv_status run_tc(const skv_desc* d, const void* q, const void* k, const void* v
                   const int32_t* bounds, int32_t n_split, int64_t causal_offset, const int32_t* q_pos,
                   const int32_t* k_pos, const skv_paged* pg, bool fused, float* out_o,
                   float* out_lse, void* out_bf16, float* lse_final, cudaStream_t stream, bool accumulate = false) {
-  static thread_local PartialParams p;
+  PartialParams p;
   Plan pl;
   pl.n_chunk = 1;
-  pl.chunk_tiles = 1;
   const int rows = tc_attn_rows_per_cta();
   pl.m_tiles = static_cast<int>((static_cast<int64_t>(d->Tq) * (d->Hq / d->Hkv) + rows - 1) / rows);
   skv_status st = fill_params(&p, d, pl, q, nullptr, nullptr, seq_lens, bounds, n_split, causal_offset, q_pos,
@@ -440,7 +435,7 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
                        int32_t n_split, int64_t causal_offset, const int32_t* q_pos, const int32_t* k_pos,
                        const skv_paged* pg, float* out_o, float* out_lse, bool zero_empty, cudaStream_t stream,
                        int32_t ring_n = 0) {
-  static thread_local PartialParams p;  // ~8 KB: keep it off the stack
+  PartialParams p;
   skv_status st = fill_params(&p, d, pl, q, ks, vs, seq_lens, bounds, n_split, causal_offset, q_pos, k_pos, pg,
                               out_o, out_lse, zero_empty);
   if (st != SKV_OK) return st;
@@ -558,16 +553,15 @@ skv_status splitkv_selftest_umma_gemm(const void* A, const void* B, float* C, in
   return SKV_OK;
 }
 
-skv_status attn_partial_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
-                                       size_t* bytes) {
+skv_status attn_partial_workspace_size(const skv_desc* desc, int32_t n_split, size_t* bytes) {
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate(desc, n_split);
   if (st != SKV_OK) return st;
   if (use_tc(desc)) {
     *bytes = 0;
     return SKV_OK;
   }
-  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const Plan pl = make_plan(desc, n_split);
   *bytes = pl.n_chunk > 1 ? ws_bytes_for(desc, pl.n_part) : 0;
   return SKV_OK;
 }
@@ -600,12 +594,20 @@ skv_status validate_positions(const skv_desc* d, const int32_t* q_pos, const int
   return SKV_OK;
 }
 
+// Checks shared by every public call taking a bounds table: the shape and the table pointer.
+skv_status validate_call(const skv_desc* d, const int32_t* bounds, int32_t n_split) {
+  skv_status st = validate(d, n_split);
+  if (st != SKV_OK) return st;
+  return validate_bounds(bounds);
+}
+
+// split_bounds may be NULL here (internal callers): one split [0, S_max) per sequence.
 skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                              const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                              const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
                              const int32_t* q_pos, const int32_t* k_pos, const skv_paged* pg, float* out_partial,
                              float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate(desc, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
   if (!out_partial || !lse_partial) return fail(SKV_EINVAL, "out_partial and lse_partial must be non-NULL");
@@ -615,7 +617,7 @@ skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_
     return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, pg, false,
                   out_partial, lse_partial, nullptr, nullptr, s);
   }
-  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const Plan pl = make_plan(desc, n_split);
   if (pl.n_chunk == 1) {
     return run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
                        causal_offset, q_pos, k_pos, pg, out_partial, lse_partial, true, s);
@@ -636,12 +638,30 @@ skv_status attn_partial_impl(const skv_desc* desc, const void* q, const void* k_
   return SKV_OK;
 }
 
+// The fused call's partials (and their merge) in `workspace`, planned by `pl`.
+skv_status decode_with_plan(const skv_desc* desc, const Plan& pl, const void* q, const void* k_cache,
+                            const void* v_cache, const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, const int32_t* q_pos,
+                            const int32_t* k_pos, const skv_paged* pg, void* out, float* lse, void* workspace,
+                            cudaStream_t s) {
+  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
+  skv_status st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                              causal_offset, q_pos, k_pos, pg, ws_o, ws_l, false, s);
+  if (st != SKV_OK) return st;
+  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SKV_OK;
+}
+
 skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                                 const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                                 const int32_t* split_bounds, int32_t n_split, int64_t causal_offset,
                                 const int32_t* q_pos, const int32_t* k_pos, const skv_paged* pg, void* out,
                                 float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate(desc, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
   if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
@@ -652,20 +672,12 @@ skv_status gqa_decode_attn_impl(const skv_desc* desc, const void* q, const void*
     return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, q_pos, k_pos, pg, true,
                   nullptr, nullptr, out, lse, s);
   }
-  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const Plan pl = make_plan(desc, n_split);
   const size_t need = ws_bytes_for(desc, pl.n_part);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
     return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_workspace_size()");
-  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
-  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   q_pos, k_pos, pg, ws_o, ws_l, false, s);
-  if (st != SKV_OK) return st;
-  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return SKV_OK;
+  return decode_with_plan(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                          causal_offset, q_pos, k_pos, pg, out, lse, workspace, s);
 }
 
 }  // namespace
@@ -676,6 +688,8 @@ skv_status attn_partial(const skv_desc* desc, const void* q, const void* k_cache
                         const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                         const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, float* out_partial,
                         float* lse_partial, void* workspace, size_t workspace_bytes, void* stream) {
+  skv_status st = validate_call(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
   return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
                            causal_offset, nullptr, nullptr, nullptr, out_partial, lse_partial, workspace,
                            workspace_bytes, stream);
@@ -686,7 +700,7 @@ skv_status attn_partial_pos(const skv_desc* desc, const void* q, const void* k_c
                             const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
                             const int32_t* k_pos, float* out_partial, float* lse_partial, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate_call(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
   return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
@@ -707,16 +721,15 @@ skv_status attn_merge_lse(int32_t n_split, int32_t B, int32_t Tq, int32_t Hq, in
   return SKV_OK;
 }
 
-skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, const int32_t* split_bounds, int32_t n_split,
-                                          size_t* bytes) {
+skv_status gqa_decode_attn_workspace_size(const skv_desc* desc, int32_t n_split, size_t* bytes) {
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate(desc, n_split);
   if (st != SKV_OK) return st;
   if (use_tc(desc)) {  // the tensor-core path merges the splits on the fly: no partials
     *bytes = 0;
     return SKV_OK;
   }
-  const Plan pl = make_plan(desc, split_bounds, n_split);
+  const Plan pl = make_plan(desc, n_split);
   *bytes = ws_bytes_for(desc, pl.n_part);
   return SKV_OK;
 }
@@ -725,6 +738,8 @@ skv_status gqa_decode_attn(const skv_desc* desc, const void* q, const void* k_ca
                            const float* k_scale, const float* v_scale, const int32_t* seq_lens,
                            const int32_t* split_bounds, int32_t n_split, int64_t causal_offset, void* out,
                            float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  skv_status st = validate_call(desc, split_bounds, n_split);
+  if (st != SKV_OK) return st;
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
                               causal_offset, nullptr, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream);
 }
@@ -734,7 +749,7 @@ skv_status attn_partial_paged(const skv_desc* desc, const skv_paged* paged, cons
                               const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
                               int64_t causal_offset, float* out_partial, float* lse_partial, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate_call(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_paged(desc, paged)) != SKV_OK) return st;
   return attn_partial_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
@@ -747,7 +762,7 @@ skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, c
                                  const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
                                  int64_t causal_offset, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate_call(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_paged(desc, paged)) != SKV_OK) return st;
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
@@ -756,15 +771,8 @@ skv_status gqa_decode_attn_paged(const skv_desc* desc, const skv_paged* paged, c
 
 skv_status attn_ring_step_workspace_size(const skv_desc* desc, size_t* bytes) {
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
-  if (!desc) return fail(SKV_EINVAL, "desc is NULL");
-  if (desc->B <= 0 || 2 * static_cast<int64_t>(desc->B) > kMaxBounds) return fail(SKV_EINVAL, "B must be in [1, 1024]");
-  std::vector<int32_t> bounds(2 * desc->B);
-  for (int b = 0; b < desc->B; ++b) {
-    bounds[2 * b] = 0;
-    bounds[2 * b + 1] = static_cast<int32_t>(std::min<int64_t>(desc->S_max, INT32_MAX));
-  }
   size_t part_ws = 0;
-  skv_status st = attn_partial_workspace_size(desc, bounds.data(), 1, &part_ws);
+  skv_status st = attn_partial_workspace_size(desc, 1, &part_ws);
   if (st != SKV_OK) return st;
   const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
   *bytes = align_up(part_ws, 256) + align_up(rows * desc->dv * 4, 256) + align_up(rows * 4, 256);
@@ -781,30 +789,25 @@ skv_status attn_ring_step(const skv_desc* desc, const void* q, const void* k_blo
   if (!o_acc || !lse_acc) return fail(SKV_EINVAL, "o_acc and lse_acc must be non-NULL");
   if (!aligned(o_acc, 16) || !aligned(lse_acc, 4)) return fail(SKV_EINVAL, "o_acc / lse_acc misaligned");
   if (desc->dv % 4) return fail(SKV_EINVAL, "dv must be a multiple of 4");
-  std::vector<int32_t> bounds(2 * desc->B);  // one split: the whole block
-  for (int b = 0; b < desc->B; ++b) {
-    bounds[2 * b] = 0;
-    bounds[2 * b + 1] = static_cast<int32_t>(desc->S_max);
-  }
+  // one split per sequence, the whole block: no bounds table (the kernels take [0, S_max))
   if (first) {  // the first block's partial is the running result
-    return attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, bounds.data(), 1, causal_offset,
+    return attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, nullptr, 1, causal_offset,
                              nullptr, nullptr, nullptr, o_acc, lse_acc, workspace, workspace_bytes, stream);
   }
   if (use_tc(desc)) {  // the tensor-core kernel merges into the running output in its epilogue
-    if ((st = validate(desc, bounds.data(), 1)) != SKV_OK) return st;
     if ((st = validate_ptrs(desc, q, k_block, v_block, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
-    return run_tc(desc, q, k_block, v_block, seq_lens, bounds.data(), 1, causal_offset, nullptr, nullptr, nullptr,
+    return run_tc(desc, q, k_block, v_block, seq_lens, nullptr, 1, causal_offset, nullptr, nullptr, nullptr,
                   false, o_acc, lse_acc, nullptr, nullptr, static_cast<cudaStream_t>(stream), true);
   }
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
     return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than attn_ring_step_workspace_size()");
   const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
   size_t part_ws = 0;
-  if ((st = attn_partial_workspace_size(desc, bounds.data(), 1, &part_ws)) != SKV_OK) return st;
+  if ((st = attn_partial_workspace_size(desc, 1, &part_ws)) != SKV_OK) return st;
   char* base = static_cast<char*>(workspace);
   float* step_o = reinterpret_cast<float*>(base + align_up(part_ws, 256));
   float* step_l = reinterpret_cast<float*>(base + align_up(part_ws, 256) + align_up(rows * desc->dv * 4, 256));
-  st = attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, bounds.data(), 1, causal_offset, nullptr,
+  st = attn_partial_impl(desc, q, k_block, v_block, k_scale, v_scale, seq_lens, nullptr, 1, causal_offset, nullptr,
                          nullptr, nullptr, step_o, step_l, part_ws ? workspace : nullptr, part_ws, stream);
   if (st != SKV_OK) return st;
   cudaError_t e = launch_merge_into(o_acc, lse_acc, step_o, step_l, static_cast<int64_t>(rows), desc->dv,
@@ -818,7 +821,7 @@ skv_status gqa_decode_attn_pos(const skv_desc* desc, const void* q, const void* 
                                const int32_t* split_bounds, int32_t n_split, const int32_t* q_pos,
                                const int32_t* k_pos, void* out, float* lse, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate_call(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_positions(desc, q_pos, k_pos)) != SKV_OK) return st;
   return gqa_decode_attn_impl(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, 0, q_pos,
@@ -868,37 +871,40 @@ extern "C" skv_status gqa_decode_attn_noalloc(const skv_desc* desc, const void* 
                                               const void* v_cache, const float* k_scale, const float* v_scale,
                                               const int32_t* seq_lens, const int32_t* split_bounds, int32_t n_split,
                                               int64_t causal_offset, void* out, float* lse, void* stream) {
-  skv_status st = validate(desc, split_bounds, n_split);
+  skv_status st = validate_call(desc, split_bounds, n_split);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(desc, q, k_cache, v_cache, k_scale, v_scale, seq_lens)) != SKV_OK) return st;
   if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
   if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
-  const Plan pl = make_plan(desc, split_bounds, n_split);
-  const size_t need = ws_bytes_for(desc, pl.n_part);
-  if (need > kNoAllocScratchBytes) {
-    char buf[256];
-    snprintf(buf, sizeof buf,
-             "gqa_decode_attn_noalloc: this problem needs %zu bytes of partials but the built-in scratch holds "
-             "%zu bytes; use gqa_decode_attn with a workspace",
-             need, kNoAllocScratchBytes);
-    return fail(SKV_EWORKSPACE, buf);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_tc(desc)) {
+    // the tensor-core shapes merge their splits inside the kernel: no partials, no scratch
+    if (!aligned(out, 16)) return fail(SKV_EINVAL, "out must be 16-byte aligned for this shape");
+    return run_tc(desc, q, k_cache, v_cache, seq_lens, split_bounds, n_split, causal_offset, nullptr, nullptr,
+                  nullptr, true, nullptr, nullptr, out, lse, s);
+  }
+  Plan pl = make_plan(desc, n_split);
+  if (ws_bytes_for(desc, pl.n_part) > kNoAllocScratchBytes) {
+    // plan again with as many chunks per split as the scratch holds partials for
+    int cap = pl.n_chunk - 1;
+    while (cap >= 1 && ws_bytes_for(desc, n_split * cap) > kNoAllocScratchBytes) --cap;
+    if (cap < 1) {
+      char buf[320];
+      snprintf(buf, sizeof buf,
+               "gqa_decode_attn_noalloc: the %d split partials of this problem need %zu bytes but the built-in "
+               "scratch holds %zu bytes; use gqa_decode_attn with a workspace",
+               n_split, ws_bytes_for(desc, n_split), kNoAllocScratchBytes);
+      return fail(SKV_EWORKSPACE, buf);
+    }
+    pl = make_plan(desc, n_split, cap);
   }
   void* scratch = nullptr;
   if ((st = noalloc_scratch_ptr(&scratch)) != SKV_OK) return st;
   // Nothing in the scratch has to start at zero: the partial kernel writes the lse of
   // every (part, row) slot before the merge reads it, and the merge never reads the o
   // of a slot whose lse is -inf.
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t rows = static_cast<size_t>(desc->B) * desc->Tq * desc->Hq;
-  float* ws_o = static_cast<float*>(scratch);
-  float* ws_l = reinterpret_cast<float*>(static_cast<char*>(scratch) +
-                                         align_up(static_cast<size_t>(pl.n_part) * rows * desc->dv * 4, 256));
-  st = run_partial(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split, causal_offset,
-                   nullptr, nullptr, nullptr, ws_o, ws_l, false, s);
-  if (st != SKV_OK) return st;
-  cudaError_t e = launch_merge(ws_o, ws_l, pl.n_part, 1, static_cast<int64_t>(rows), desc->dv, out, true, lse, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return SKV_OK;
+  return decode_with_plan(desc, pl, q, k_cache, v_cache, k_scale, v_scale, seq_lens, split_bounds, n_split,
+                          causal_offset, nullptr, nullptr, nullptr, out, lse, scratch, s);
 }
 
 // ------------------------------------------------------------------ pass-Q decode
@@ -907,20 +913,17 @@ namespace {
 
 // A pass-Q call as one batched partial launch: the n_ranks * B work rows (rank, ring step,
 // slot) and the n_ranks * B cache rows (rank, request) share one count, every cache row is
-// one split [0, S_max) clipped to its shard length on the device.
-skv_status passq_setup(const skv_desc* d, int32_t n_ranks, skv_desc* vd, std::vector<int32_t>* bounds) {
+// one split [0, S_max) (no bounds table) clipped to its shard length on the device.
+skv_status passq_setup(const skv_desc* d, int32_t n_ranks, skv_desc* vd) {
   if (!d) return fail(SKV_EINVAL, "desc is NULL");
   if (n_ranks < 1) return fail(SKV_EINVAL, "n_ranks must be >= 1");
   if (d->B <= 0 || d->B % n_ranks) return fail(SKV_EINVAL, "B must be a positive multiple of n_ranks");
-  if (static_cast<int64_t>(n_ranks) * d->B > kMaxBounds / 2) return fail(SKV_EINVAL, "n_ranks * B must be <= 1024");
+  if (static_cast<int64_t>(n_ranks) * d->B >= (int64_t(1) << 30)) return fail(SKV_EINVAL, "n_ranks * B must be below 2^30");
   if (is_mla_shape(d)) return fail(SKV_EUNSUPPORTED, "pass-Q decode is not supported for the MLA latent shape");
   if (d->Tq != 1) return fail(SKV_EUNSUPPORTED, "pass-Q decode takes one query token per request (Tq = 1)");
   *vd = *d;
   vd->B = n_ranks * d->B;
-  const int32_t hi = static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(d->S_max, 0), INT32_MAX));
-  bounds->assign(2 * static_cast<size_t>(vd->B), 0);
-  for (int r = 0; r < vd->B; ++r) (*bounds)[2 * r + 1] = hi;
-  return validate(vd, bounds->data(), 1);
+  return validate(vd, 1);
 }
 
 }  // namespace
@@ -930,10 +933,9 @@ extern "C" {
 skv_status gqa_decode_attn_passq_workspace_size(const skv_desc* desc, int32_t n_ranks, size_t* bytes) {
   if (!bytes) return fail(SKV_EINVAL, "bytes is NULL");
   skv_desc vd;
-  std::vector<int32_t> bounds;
-  skv_status st = passq_setup(desc, n_ranks, &vd, &bounds);
+  skv_status st = passq_setup(desc, n_ranks, &vd);
   if (st != SKV_OK) return st;
-  const Plan pl = make_plan(&vd, bounds.data(), 1);
+  const Plan pl = make_plan(&vd, 1);
   *bytes = ws_bytes_for(&vd, pl.n_part);
   return SKV_OK;
 }
@@ -943,13 +945,12 @@ skv_status gqa_decode_attn_passq(const skv_desc* desc, int32_t n_ranks, const vo
                                  const int32_t* shard_lens, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   skv_desc vd;
-  static thread_local std::vector<int32_t> bounds;
-  skv_status st = passq_setup(desc, n_ranks, &vd, &bounds);
+  skv_status st = passq_setup(desc, n_ranks, &vd);
   if (st != SKV_OK) return st;
   if ((st = validate_ptrs(&vd, q, k_shards, v_shards, k_scale, v_scale, shard_lens)) != SKV_OK) return st;
   if (!out || !lse) return fail(SKV_EINVAL, "out and lse must be non-NULL");
   if (!aligned(out, 8) || !aligned(lse, 4)) return fail(SKV_EINVAL, "outputs misaligned");
-  const Plan pl = make_plan(&vd, bounds.data(), 1);
+  const Plan pl = make_plan(&vd, 1);
   const size_t need = ws_bytes_for(&vd, pl.n_part);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
     return fail(SKV_EWORKSPACE, "workspace missing, misaligned or smaller than gqa_decode_attn_passq_workspace_size()");
@@ -959,7 +960,7 @@ skv_status gqa_decode_attn_passq(const skv_desc* desc, int32_t n_ranks, const vo
   float* ws_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(static_cast<size_t>(pl.n_part) * rows * vd.dv * 4, 256));
   // every rank, every ring step: partials land in the owners' exchange slots
-  st = run_partial(&vd, pl, q, k_shards, v_shards, k_scale, v_scale, shard_lens, bounds.data(), 1, SKV_NO_CAUSAL,
+  st = run_partial(&vd, pl, q, k_shards, v_shards, k_scale, v_scale, shard_lens, nullptr, 1, SKV_NO_CAUSAL,
                    nullptr, nullptr, nullptr, ws_o, ws_l, false, s, n_ranks);
   if (st != SKV_OK) return st;
   // the exchange delivered [owner][source rank][part] slabs: each owner merges its

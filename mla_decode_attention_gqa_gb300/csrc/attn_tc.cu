@@ -114,9 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = static_cast<int>(item / p.Hkv);
   const int G = p.G;
   const int seq_len = p.seq_lens[b];
-  const int* bnd = p.bounds + b * (p.n_split + 1);
-  const int lo = max(x.fused ? bnd[0] : bnd[j], 0);
-  int hi = min(min(x.fused ? bnd[p.n_split] : bnd[j + 1], seq_len), p.S_max);
+  int lo, hi;
+  split_range(p, b, x.fused ? 0 : j, x.fused ? p.n_split : j + 1, seq_len, &lo, &hi);
   const int rows_total = p.Tq * G;
   const int m0 = mt * 2 * kRowsTile;
   const int m_last = min(m0 + 2 * kRowsTile, rows_total) - 1;

@@ -180,11 +180,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   if constexpr (RING) ring_rows(p, b, &bq, &bkv);
 
   const int seq_len = p.seq_lens[bkv];
-  const int* bnd = p.bounds + bkv * (p.n_split + 1);
-  int lo = max(bnd[j], 0);
-  int hi = min(min(bnd[j + 1], seq_len), p.S_max);
-  const int win_lo = (lo / TN) * TN + c * p.chunk_tiles * TN;
-  const int win_hi = win_lo + p.chunk_tiles * TN;
+  int lo, hi, win_lo, win_hi;
+  split_range(p, bkv, j, j + 1, seq_len, &lo, &hi);
+  chunk_window(p, lo, hi, c, &win_lo, &win_hi);
+  static_assert(TN == kTileN, "chunks are cut in whole tiles");
   int r_lo = max(lo, win_lo);
   int r_hi = min(hi, win_hi);
   const int rows_total = p.Tq * p.G;

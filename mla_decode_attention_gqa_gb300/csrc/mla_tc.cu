@@ -205,11 +205,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const int b = static_cast<int>(item);
   const int seq_len = p.seq_lens[b];
-  const int* bnd = p.bounds + b * (p.n_split + 1);
-  const int lo = max(x.fused ? bnd[0] : bnd[j], 0);
-  const int hi = min(min(x.fused ? bnd[p.n_split] : bnd[j + 1], seq_len), p.S_max);
-  const int win_lo = (lo / kTileN) * kTileN + c * p.chunk_tiles * kTileN;
-  const int win_hi = win_lo + p.chunk_tiles * kTileN;
+  int lo, hi, win_lo, win_hi;
+  split_range(p, b, x.fused ? 0 : j, x.fused ? p.n_split : j + 1, seq_len, &lo, &hi);
+  chunk_window(p, lo, hi, c, &win_lo, &win_hi);
   const int r_lo = max(lo, win_lo);
   int r_hi = min(hi, win_hi);
   const int rows_total = p.Tq * p.G;

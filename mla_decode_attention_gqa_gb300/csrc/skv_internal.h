@@ -9,9 +9,6 @@
 
 namespace skv {
 
-// Largest B * (n_split + 1) whose split bounds travel inside the kernel parameters.
-constexpr int kMaxBounds = 2048;
-
 // Tokens per KV tile of the GQA partial kernel (and the chunk granularity).
 constexpr int kTileN = 64;
 
@@ -33,10 +30,13 @@ cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
 // Parameters of one split-KV partial-attention launch.
 //
 // Work item = (b, kv head g, split j, chunk c, row tile mt).  Split j of sequence b
-// covers tokens [bounds[b][j], bounds[b][j+1]) clipped to seq_lens[b]; chunk c of it
-// covers the tile-aligned window [a + c*chunk_tiles*kTileN, a + (c+1)*chunk_tiles*kTileN)
-// with a = floor(bounds[b][j] / kTileN) * kTileN.  Row m of kv head g's row space
-// (m < Tq*G) is query row t = m / G of query head g*G + m % G.
+// covers tokens [bounds[b][j], bounds[b][j+1]) clipped to [0, min(seq_lens[b], S_max))
+// (no bounds table: the one split [0, S_max)); the table lives in device memory and is
+// read by the kernels, never by the host.  From its first whole kTileN-token tile the
+// split is cut into n_chunk chunks of equal tile counts, sized on the device from the
+// split's own length, so every split is spread over the same number of work items
+// whatever its length.  Row m of kv head g's row space (m < Tq*G) is query row
+// t = m / G of query head g*G + m % G.
 //
 // The item writes its partial (normalised o, natural-log lse) to part
 // p = j * n_chunk + c of out_o [n_part][B][Tq][Hq][dv] and out_lse [n_part][B][Tq][Hq].
@@ -61,14 +61,39 @@ struct PartialParams {
   float scale_log2;  // softmax_scale * log2(e)
   int32_t B, Tq, Hq, Hkv, G;
   int32_t S_max;  // tokens at or past S_max do not exist
-  int32_t n_split, n_chunk, chunk_tiles, m_tiles;
+  int32_t n_split, n_chunk, m_tiles;
   int32_t zero_empty;  // write o = 0 for items with no visible token
   int32_t ring_n;      // pass-Q ring: ranks (0: off) and query rows each rank owns; B then
   int32_t ring_bq;     //   counts ring_n * ring_n * ring_bq work rows (rank, step, slot)
-  int32_t bounds[kMaxBounds];  // [B][n_split + 1]
+  const int32_t* bounds;  // device [B][n_split + 1], or NULL: one split [0, S_max) per row
 };
 
 #ifdef __CUDACC__
+// Token range [*lo, *hi) from bound ja to bound jb of KV row b (a split: jb = ja + 1; the
+// union of all splits: 0 and n_split), clipped to the row's length and to S_max.
+__device__ __forceinline__ void split_range(const PartialParams& p, int b, int ja, int jb, int seq_len, int* lo,
+                                            int* hi) {
+  int a = 0, e = p.S_max;
+  if (p.bounds) {
+    const int32_t* bnd = p.bounds + static_cast<int64_t>(b) * (p.n_split + 1);
+    a = __ldg(bnd + ja);
+    e = __ldg(bnd + jb);
+  }
+  *lo = max(a, 0);
+  *hi = min(min(e, seq_len), p.S_max);
+}
+
+// Tile-aligned window [*win_lo, *win_hi) of chunk c of the token range [lo, hi): from the
+// tile holding lo, the range's tiles are dealt out in n_chunk runs of equal length (the
+// last ones shorter or empty).  An empty range gives an empty window.
+__device__ __forceinline__ void chunk_window(const PartialParams& p, int lo, int hi, int c, int* win_lo, int* win_hi) {
+  const int a = (lo / kTileN) * kTileN;
+  const int tiles = hi > a ? (hi - a + kTileN - 1) / kTileN : 0;
+  const int ct = (tiles + p.n_chunk - 1) / p.n_chunk;
+  *win_lo = a + c * ct * kTileN;
+  *win_hi = *win_lo + ct * kTileN;
+}
+
 // Page holding logical token `tok` of sequence b in a paged cache (the tensor maps then
 // take (tok % block_len, page) where a contiguous cache takes (tok, b)).
 __device__ __forceinline__ int kv_page_of(const PartialParams& p, int b, int tok) {

@@ -56,18 +56,12 @@ def _desc(**kw):
     return d
 
 
-def _bounds(rows):
-    flat = [x for r in rows for x in r]
-    return (ctypes.c_int32 * len(flat))(*flat), len(rows[0]) - 1
-
-
 FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
 
 
-def _call_partial(d, rows=((0, 1024), (0, 1024)), q=FAKE, k=FAKE, v=FAKE, seq=FAKE, ks=None, vs=None):
+def _call_partial(d, bounds=FAKE, n_split=1, q=FAKE, k=FAKE, v=FAKE, seq=FAKE, ks=None, vs=None):
     lib = skv.load_library()
-    b, n = _bounds(rows)
-    return lib.attn_partial(ctypes.byref(d), q, k, v, ks, vs, seq, b, n, 0, FAKE, FAKE, None, 0, None)
+    return lib.attn_partial(ctypes.byref(d), q, k, v, ks, vs, seq, bounds, n_split, 0, FAKE, FAKE, None, 0, None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -92,17 +86,28 @@ def test_bad_pointers_and_bounds_are_rejected():
     assert _call_partial(d, q=None) == skv.SKV_EINVAL
     assert _call_partial(d, seq=None) == skv.SKV_EINVAL
     assert _call_partial(d, k=ctypes.c_void_p(0x10008)) == skv.SKV_EINVAL  # not 16-byte aligned
-    assert _call_partial(d, rows=((0, 10), (5, 4))) == skv.SKV_EINVAL  # decreasing
-    assert _call_partial(d, rows=((-1, 10), (0, 4))) == skv.SKV_EINVAL  # negative
+    assert _call_partial(d, bounds=None) == skv.SKV_EINVAL  # no bounds table
+    assert "split_bounds" in skv.last_error()
+    assert _call_partial(d, bounds=ctypes.c_void_p(0x10002)) == skv.SKV_EINVAL  # bounds not 4-byte aligned
+    assert _call_partial(d, n_split=0) == skv.SKV_EINVAL
     d8 = _desc(kv_dtype=1)
     assert _call_partial(d8) == skv.SKV_EINVAL  # fp8 without scales
     assert "scale" in skv.last_error()
 
 
-def test_too_many_bounds_rejected():
-    d = _desc(B=300)
-    rows = [tuple(range(0, 1024, 128)) + (1024,)] * 300
-    assert _call_partial(d, rows=rows) == skv.SKV_EINVAL
+def test_serving_batches_pass_host_validation():
+    """The bounds table is device memory the host never reads, so the batch size is not
+    capped by it: B = 4096 sequences over 8 splits (36,864 bounds) passes every host check
+    and reaches the workspace check; pass-Q and ring steps take large batches too."""
+    lib = skv.load_library()
+    d = _desc(B=4096)
+    assert skv.gqa_decode_attn_workspace_size(d, 8) > 0
+    st = lib.gqa_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 8, 0, FAKE, FAKE, None, 0,
+                             None)
+    assert st == skv.SKV_EWORKSPACE, skv.last_error()
+    n = ctypes.c_size_t(0)
+    assert lib.attn_ring_step_workspace_size(ctypes.byref(_desc(B=2048)), ctypes.byref(n)) == skv.SKV_OK
+    assert lib.gqa_decode_attn_passq_workspace_size(ctypes.byref(_desc(B=1024)), 4, ctypes.byref(n)) == skv.SKV_OK
 
 
 def test_merge_argument_checks():
@@ -114,16 +119,17 @@ def test_merge_argument_checks():
 
 def test_workspace_sizes_are_host_queries():
     d = _desc()
-    b, n = _bounds(((0, 1024), (0, 1024)))
-    assert skv.gqa_decode_attn_workspace_size(d, b, n) > 0
-    assert skv.attn_partial_workspace_size(d, b, n) >= 0
+    assert skv.gqa_decode_attn_workspace_size(d, 1) > 0
+    assert skv.attn_partial_workspace_size(d, 1) >= 0
+    # the tensor-core shapes (bf16 d = 128, >= 128 rows per KV head) merge in the kernel
+    assert skv.gqa_decode_attn_workspace_size(_desc(Tq=32, q_strides=(32 * 16 * 128, 16 * 128, 128)), 4) == 0
 
 
 def test_missing_workspace_is_reported():
     lib = skv.load_library()
     d = _desc()
-    b, n = _bounds(((0, 1024), (0, 1024)))
-    st = lib.gqa_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, b, n, 0, FAKE, FAKE, None, 0, None)
+    st = lib.gqa_decode_attn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 1, 0, FAKE, FAKE, None, 0,
+                             None)
     assert st == skv.SKV_EWORKSPACE
 
 
@@ -134,11 +140,10 @@ def _paged(block_len=64, max_blocks=16, num_blocks=40, table=FAKE):
     return pg
 
 
-def _call_paged(d, pg, rows=((0, 1024), (0, 1024))):
+def _call_paged(d, pg):
     lib = skv.load_library()
-    b, n = _bounds(rows)
     return lib.attn_partial_paged(ctypes.byref(d), ctypes.byref(pg) if pg is not None else None, FAKE, FAKE, FAKE,
-                                  None, None, FAKE, b, n, 0, FAKE, FAKE, None, 0, None)
+                                  None, None, FAKE, FAKE, 1, 0, FAKE, FAKE, None, 0, None)
 
 
 def test_paged_arguments_are_checked_before_any_device_access():
@@ -158,10 +163,9 @@ def test_paged_arguments_are_checked_before_any_device_access():
 
 def test_position_arguments_are_checked_before_any_device_access():
     lib = skv.load_library()
-    b, n = _bounds(((0, 1024), (0, 1024)))
 
     def call(d, qp, kp):
-        return lib.attn_partial_pos(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, b, n, qp, kp, FAKE, FAKE,
+        return lib.attn_partial_pos(ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 1, qp, kp, FAKE, FAKE,
                                     None, 0, None)
 
     d = _desc()
@@ -196,7 +200,6 @@ def test_passq_arguments_are_checked():
     assert ws(_desc(B=4), 2) == skv.SKV_OK and n.value > 0
     assert ws(_desc(B=3), 2) == skv.SKV_EINVAL  # B not a multiple of the group
     assert ws(_desc(B=4), 0) == skv.SKV_EINVAL
-    assert ws(_desc(B=512), 4) == skv.SKV_EINVAL  # n_ranks * B above 1024
     assert ws(_desc(B=4, Tq=2), 2) == skv.SKV_EUNSUPPORTED  # decode only
     mla = _desc(B=4, Hq=128, Hkv=1, dk=576, dv=512, q_strides=(128 * 576, 128 * 576, 576),
                 k_strides=(1024 * 576, 1024 * 576, 576), v_strides=(1024 * 576, 1024 * 576, 576))

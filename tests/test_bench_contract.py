@@ -123,3 +123,44 @@ def test_parity_sample_reports_the_error_of_the_given_result():
     bad = bench.oracle_parity(w, par)
     assert bad["out_max_abs_err"] > 0.49
     assert "error" in bench.oracle_parity(w, {"error": "x"})
+
+
+@pytest.mark.parametrize("kind", ["fp8_ragged", "causal_rows"])
+def test_parity_sample_walks_splits_like_the_whole_group(kind):
+    """oracle_parity takes the group one split at a time (dequantising each split's rows by
+    absolute position, masking rows by their chunk position); fed the whole-group oracle
+    result it reports rounding-level errors, for fp8 block-scaled KV with ragged splits and
+    for a causal query chunk sampled every few rows."""
+    import numpy as np
+
+    import oracle
+
+    if kind == "fp8_ragged":
+        w = W.scaled(W.HELIX_KVP8_FP8_1M, B=1, Hq=16, Hkv=1, S=1024, seed=77)
+        rows = [0]
+    else:
+        w = W.scaled(W.RING_PREFILL, B=1, Hq=16, Hkv=1, Tq=64, S=512, seed=78)
+        rows = list(range(0, 64, 4))
+    inp = W.make_inputs(w)
+    G, n = w.Hq // w.Hkv, inp["seq_lens_host"][0]
+    qf = oracle.bf16_bits_to_f64(inp["q"][0:1, rows, :G].contiguous().view(torch.int16).numpy())
+    if w.kv_dtype == "fp8_e4m3":
+        kf = oracle.dequant_e4m3_blocks(inp["k"][0, 0, :n].numpy(), inp["k_scale"][0, 0].numpy(), w.scale_block)
+        vf = oracle.dequant_e4m3_blocks(inp["v"][0, 0, :n].numpy(), inp["v_scale"][0, 0].numpy(), w.scale_block)
+    else:
+        kf = oracle.bf16_bits_to_f64(inp["k"][0, 0, :n].contiguous().view(torch.int16).numpy())
+        vf = oracle.bf16_bits_to_f64(inp["v"][0, 0, :n].contiguous().view(torch.int16).numpy())
+    pos = {}
+    if w.causal_offset != W.NO_CAUSAL:
+        pos = {"q_positions": [w.causal_offset + np.asarray(rows)], "k_positions": [np.arange(n)]}
+    o, l = oracle.split_attention(qf, kf[None, None], vf[None, None], [n], [w.split_bounds()[0]], w.causal_offset,
+                                  w.scale, **pos)
+    mo, ml = oracle.merge_lse(o, l)
+    fp8 = w.kv_dtype == "fp8_e4m3"
+    par = {"n_tok": n, "rows": rows, "q": inp["q"][0, rows, :G].contiguous(), "k": inp["k"][0, 0, :n].contiguous(),
+           "v": inp["v"][0, 0, :n].contiguous(), "ks": inp["k_scale"][0, 0] if fp8 else None,
+           "vs": inp["v_scale"][0, 0] if fp8 else None,
+           "out": torch.from_numpy(mo[0]).float(), "lse": torch.from_numpy(ml[0]).float()}
+    res = bench.oracle_parity(w, par)
+    assert "error" not in res, res
+    assert res["out_max_abs_err"] < 1e-6 and res["lse_max_abs_err"] < 1e-5 and res["empty_rows_match"], res

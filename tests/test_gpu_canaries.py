@@ -84,7 +84,7 @@ def _decode_family(w):
     om.check("merged out")
     lm.check("merged lse")
     d = skv.make_desc(inp["q"], inp["k"], inp["v"], w.scale, w.scale_block)
-    nbytes = skv.gqa_decode_attn_workspace_size(d, *skv._bounds_array(bounds, w.B))
+    nbytes = skv.gqa_decode_attn_workspace_size(d, len(bounds[0]) - 1)
     ws = Guarded((max(nbytes, 1),), torch.uint8)
     of, lf = _outs(w)
     skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], bounds, w.causal_offset, out=of.t, lse=lf.t,
