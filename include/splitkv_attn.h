@@ -51,7 +51,13 @@
  *   - Partials: o is normalised by its own softmax denominator and lse is the
  *     natural log of that denominator over scaled scores (softmax_scale * q.k).
  *     A split with no visible token has o = 0 and lse = -inf.
- *   - fp8-e4m3 KV: value = e4m3(code) * scale[b][kv_head][t / scale_block].
+ *   - fp8-e4m3 KV: value = e4m3(code) * scale[b][kv_head][t / scale_block].  The products
+ *     run on f16 tensor cores: the codes widen to fp16 exactly; the bf16 query rows of
+ *     each 16-row group are multiplied by the power of two that puts their largest
+ *     magnitude in [2^14, 2^15) and rounded to fp16 (exact for every element within 2^-29
+ *     of that largest; the power of two is divided out of the scores), so any finite bf16
+ *     query is accepted; p times the V block scale is rounded to fp16 for the PV product
+ *     (finite while the V block scale stays below 65504, i.e. |V| below 2.9e7).
  *   - MLA (latent KV): Hkv = 1, dk = 576 (512 latent + 64 rope), dv = 512 and
  *     v_cache = k_cache with the same strides (V is the first 512 latent columns).
  */

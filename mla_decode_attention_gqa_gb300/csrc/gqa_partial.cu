@@ -73,7 +73,9 @@ struct GqaCfg {
   static constexpr int ML_BYTES = WN * ROWS * 2 * 4;
   // fp8 variants keep their fp16 q fragments in shared memory ([WM][D/16][32 lanes] x 16 B)
   static constexpr int QF_BYTES = FP8 ? WM * (D / 16) * 32 * 16 : 0;
-  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + ML_BYTES + QF_BYTES;
+  // ... and the score scale of each warp row (the softmax scale times their q scaling)
+  static constexpr int QS_BYTES = FP8 ? 16 : 0;
+  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + ML_BYTES + QF_BYTES + QS_BYTES;
   static_assert(ROW_BYTES % 128 == 0, "token rows must be whole 128-byte boxes");
   static_assert(WN == 1 || WN * ROWS * D * 4 <= RING_BYTES, "combine buffer must fit in the ring");
   static_assert(D % 16 == 0, "head dim must be a multiple of 16");
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
   uint64_t* empty = full + C::NFULL;                                     // [NSTAGE]
   float* ml = reinterpret_cast<float*>(smem + C::RING_BYTES + C::BAR_BYTES);  // [WN][ROWS][2]
   uint4* qfrag = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ml) + C::ML_BYTES);  // fp8 only
+  float* qscale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(qfrag) + C::QF_BYTES);  // fp8: [WM]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -260,10 +263,40 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 
   // ---- Q fragments (A operand, 16 rows x D): registers for bf16, shared memory for fp8
   uint32_t qa[C::FP8 ? 1 : D / 16][4];
+  // fp8 KV: the warp's 16 q rows are multiplied by 2^-qe (their largest magnitude then
+  // lies in [2^14, 2^15)) before the fp16 conversion the f16 MMA needs, and 2^qe goes back
+  // into the score scale: the conversion cannot overflow, and every element within 2^-29
+  // of the rows' largest converts exactly.  The scale waits in shared memory (the kernel
+  // has no register to spare for it).
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* q0 = q + bq * p.q_sb + tq0 * p.q_st + h0 * p.q_sh;
     const __nv_bfloat16* q1 = q + bq * p.q_sb + tq1 * p.q_st + h1 * p.q_sh;
+    float qsc = 1.f;  // 2^-qe
+    if constexpr (C::FP8) {
+      float amax = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int d0 = 16 * ks + 4 * tq;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (r == 0 ? v0 : v1) {
+            const uint2 u = *reinterpret_cast<const uint2*>((r == 0 ? q0 : q1) + d0);
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+            const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+            amax = fmaxf(fmaxf(amax, fmaxf(fabsf(__low2float(a)), fabsf(__high2float(a)))),
+                         fmaxf(fabsf(__low2float(bb)), fabsf(__high2float(bb))));
+          }
+        }
+      }
+      // non-negative floats order as their bit patterns (a NaN above every number)
+      amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+      int qe = 0;  // all-zero or non-finite rows keep their values
+      if (amax > 0.f && amax <= 3.4e38f)
+        qe = min(max(static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100), 100);
+      qsc = __uint_as_float(static_cast<uint32_t>(127 - qe) << 23);
+      if (wn == 0 && lane == 0) qscale[wm] = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + qe) << 23);
+    }
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       if constexpr (!C::FP8) {
@@ -281,13 +314,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
           const uint2 u = *reinterpret_cast<const uint2*>(q0 + d0);
           const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
           const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-          f0[0] = __low2float(a); f0[1] = __high2float(a); f0[2] = __low2float(bb); f0[3] = __high2float(bb);
+          f0[0] = __low2float(a) * qsc; f0[1] = __high2float(a) * qsc;
+          f0[2] = __low2float(bb) * qsc; f0[3] = __high2float(bb) * qsc;
         }
         if (v1) {
           const uint2 u = *reinterpret_cast<const uint2*>(q1 + d0);
           const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
           const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-          f1[0] = __low2float(a); f1[1] = __high2float(a); f1[2] = __low2float(bb); f1[3] = __high2float(bb);
+          f1[0] = __low2float(a) * qsc; f1[1] = __high2float(a) * qsc;
+          f1[2] = __low2float(bb) * qsc; f1[3] = __high2float(bb) * qsc;
         }
         if (wn == 0) {
           qfrag[(wm * (D / 16) + ks) * 32 + lane] =
@@ -297,7 +332,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       }
     }
   }
-  if constexpr (C::FP8) named_bar_sync(1, C::NCW * 32);  // q fragments visible to every consumer
+  if constexpr (C::FP8) named_bar_sync(1, C::NCW * 32);  // q fragments and scales visible to every consumer
 
   float o[D / 8][4];
 #pragma unroll
@@ -386,8 +421,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       }
     }
 
-    // ---- scale, mask, online softmax
-    const float sl = p.scale_log2 * ksc;
+    // ---- scale, mask, online softmax (fp8: the q scaling undone here)
+    float sl = p.scale_log2;
+    if constexpr (C::FP8) sl = *reinterpret_cast<volatile const float*>(qscale + wm) * ksc;
     const bool in_range = (t0s >= r_lo) && (t0s + NS <= r_hi);
     const bool need_mask = POS || !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
     float tmax[2] = {-INFINITY, -INFINITY};

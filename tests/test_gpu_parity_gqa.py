@@ -146,3 +146,19 @@ def test_repeat_calls_are_deterministic():
     b = skv.gqa_decode_attn(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["split_bounds"])
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("q_exp", [17, -20], ids=["q_above_fp16_max", "q_below_fp16_normal"])
+@pytest.mark.parametrize("Tq", [1, 4], ids=["decode", "prefill_rows"])
+def test_fp8_query_outside_the_fp16_range(q_exp, Tq):
+    """fp8 KV runs its products in f16, so the bf16 query is converted to fp16.  The kernels
+    scale each warp's query rows by a power of two first and fold it back into the score
+    scale, so a query far above fp16's largest finite value (2^17 > 65504) or below its
+    smallest normal (2^-20 < 2^-14) gives the same result as the oracle's exact product.
+    The softmax scale compensates, so the scores stay those of N(0,1) data."""
+    w = W.scaled(W.HELIX_KVP8_FP8_1M, B=2, Tq=Tq, S=2048, n_split=2, seed=1700 + q_exp + Tq,
+                 softmax_scale=2.0 ** -q_exp / np.sqrt(128.0))
+    inp = W.make_inputs(w, DEV)
+    inp["q"] = (inp["q"].float() * 2.0 ** q_exp).to(torch.bfloat16)  # a power of two: exact in bf16
+    assert inp["q"].float().abs().max().item() > (65504.0 if q_exp > 0 else 0.0)
+    _run_all_paths(w, inp)
