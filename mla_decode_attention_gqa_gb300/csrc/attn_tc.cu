@@ -270,14 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_used > 0) {
+    // The whole warp runs the loop and waits; one elected lane issues the MMAs and commits
+    // (a lone lane-0 loop pays about twice as much per wait and more per MMA).
+    if (n_used > 0) {
       const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
       const uint32_t idesc_pv = tc::idesc_f16(128, kD, true, false, true);
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
-      bool ok = mbar_wait(&bars->q_full, 0, p.err, kDevErrFullWait);
-      // Descriptors are built once per call and the k-steps add compile-time offsets: a
-      // single issuing thread that recomputes them per step cannot keep the tensor pipe fed.
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err, kDevErrFullWait));
+      };
+      bool ok = wait_all(&bars->q_full, 0);
+      // Descriptors are built once per call and the k-steps add compile-time offsets.
       auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 128 tokens, K 128)
         const uint64_t ad0 = tc::smem_desc_sw128(q_base + k * kQTileBytes, 16, 1024);
         const uint64_t bd0 = tc::smem_desc_sw128(ring + (i % kNStage) * kStageBytes, 16, 1024);
@@ -301,36 +305,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                          ks > 0 ? 1u : acc0);
         }
       };
-      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, p.err, kDevErrFullWait);
+      if (ok) ok = wait_all(&bars->kv_full[0], 0);
       if (ok) {
         tc::fence_after_sync();
-        issue_s(0, 0);
-        tc::mma_commit(smem_u32(&bars->s_full[0]));
-        issue_s(1, 0);
-        tc::mma_commit(smem_u32(&bars->s_full[1]));
+        if (tc::elect_one()) {
+          issue_s(0, 0);
+          tc::mma_commit(smem_u32(&bars->s_full[0]));
+          issue_s(1, 0);
+          tc::mma_commit(smem_u32(&bars->s_full[1]));
+        }
+        __syncwarp();
         for (int i = 0; i < n_used && ok; ++i) {
-          ok = mbar_wait(&bars->p_full[0], i & 1, p.err, kDevErrFullWait);
+          ok = wait_all(&bars->p_full[0], i & 1);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_pv(0, i);
-          tc::mma_commit(smem_u32(&bars->pv_done[0]));
+          if (tc::elect_one()) {
+            issue_pv(0, i);
+            tc::mma_commit(smem_u32(&bars->pv_done[0]));
+          }
+          __syncwarp();
           if (i + 1 < n_used) {
-            ok = mbar_wait(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1, p.err, kDevErrFullWait);
+            ok = wait_all(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1);
             if (!ok) break;
             tc::fence_after_sync();
-            issue_s(0, i + 1);
-            tc::mma_commit(smem_u32(&bars->s_full[0]));
+            if (tc::elect_one()) {
+              issue_s(0, i + 1);
+              tc::mma_commit(smem_u32(&bars->s_full[0]));
+            }
+            __syncwarp();
           }
-          ok = mbar_wait(&bars->p_full[1], i & 1, p.err, kDevErrFullWait);
+          ok = wait_all(&bars->p_full[1], i & 1);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_pv(1, i);
-          tc::mma_commit(smem_u32(&bars->pv_done[1]));
-          tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
-          if (i + 1 < n_used) {
-            issue_s(1, i + 1);
-            tc::mma_commit(smem_u32(&bars->s_full[1]));
+          if (tc::elect_one()) {
+            issue_pv(1, i);
+            tc::mma_commit(smem_u32(&bars->pv_done[1]));
+            tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
+            if (i + 1 < n_used) {
+              issue_s(1, i + 1);
+              tc::mma_commit(smem_u32(&bars->s_full[1]));
+            }
           }
+          __syncwarp();
         }
       }
     }

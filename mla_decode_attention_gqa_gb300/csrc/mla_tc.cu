@@ -305,43 +305,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp == 6) {
       // ---------------------------------------------------------- MMA issuers: S = Q K^T
       // warp 1: k-steps 0..17 into S buffer + 0; warp 6: k-steps 18..35 into S buffer + 64
-      // (its last four, the rope dims, take A = Q from shared memory)
-      if (lane == 0 && n_tiles > 0) {
+      // (its last four, the rope dims, take A = Q from shared memory).  Each warp runs the
+      // loop and its waits together; one elected lane issues the MMAs and commits.
+      if (n_tiles > 0) {
         const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
         const uint32_t ring = smem_u32(smem);
         const uint64_t qrope_d0 = tc::smem_desc_sw128(smem_u32(smem + kOffQRope), 16, 1024);
-        bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrFullWait);
+        bool ok = warp_wait(&bars->q_moved, 0, p.err);
         for (int i = 0; i < n_tiles && ok; ++i) {
           const int s = i % kNStage0;
-          ok = mbar_wait(&bars->kv_full0[s], (i / kNStage0) & 1, p.err, kDevErrFullWait);
-          if (ok && i >= 2) ok = mbar_wait(&bars->s_free[i & 1], ((i >> 1) - 1) & 1, p.err, kDevErrFullWait);
+          ok = warp_wait(&bars->kv_full0[s], (i / kNStage0) & 1, p.err);
+          if (ok && i >= 2) ok = warp_wait(&bars->s_free[i & 1], ((i >> 1) - 1) & 1, p.err);
           if (!ok) break;
           tc::fence_after_sync();
           // descriptors built once per tile; the k-steps add compile-time offsets
           const uint64_t bd0 = tc::smem_desc_sw128(ring + s * kStage0Bytes, 16, 1024);
-          if (warp == 1) {
-            const uint32_t d = tmem + kColS + 128 * (i & 1);
+          if (tc::elect_one()) {
+            if (warp == 1) {
+              const uint32_t d = tmem + kColS + 128 * (i & 1);
 #pragma unroll
-            for (int ks = 0; ks < kKStepsA; ++ks) {
-              const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
-              tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
-            }
-          } else {
-            const uint32_t d = tmem + kColS + 128 * (i & 1) + 64;
+              for (int ks = 0; ks < kKStepsA; ++ks) {
+                const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+                tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
+              }
+            } else {
+              const uint32_t d = tmem + kColS + 128 * (i & 1) + 64;
 #pragma unroll
-            for (int ks = kKStepsA; ks < kKSteps; ++ks) {
-              const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
-              const uint32_t acc = ks > kKStepsA ? 1u : 0u;
-              if (ks < kQTmemBoxes * 4) {
-                tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, acc);
-              } else {
-                const uint64_t ad = qrope_d0 + static_cast<uint64_t>(((ks & 3) * 32) >> 4);
-                tc::mma_f16_ss(d, ad, bd, idesc_s, acc);
+              for (int ks = kKStepsA; ks < kKSteps; ++ks) {
+                const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+                const uint32_t acc = ks > kKStepsA ? 1u : 0u;
+                if (ks < kQTmemBoxes * 4) {
+                  tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, acc);
+                } else {
+                  const uint64_t ad = qrope_d0 + static_cast<uint64_t>(((ks & 3) * 32) >> 4);
+                  tc::mma_f16_ss(d, ad, bd, idesc_s, acc);
+                }
               }
             }
+            tc::mma_commit(smem_u32(&bars->s_full[i & 1]));
+            tc::mma_commit(smem_u32(&bars->kv_empty0[s]));
           }
-          tc::mma_commit(smem_u32(&bars->s_full[i & 1]));
-          tc::mma_commit(smem_u32(&bars->kv_empty0[s]));
+          __syncwarp();
         }
       }
     } else {
@@ -549,8 +553,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer: O += P V
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->l_full, kRows * 4);
+      // (the whole warp runs the loop and waits; one elected lane arrives, issues, commits)
+      {
+        if (tc::elect_one()) mbar_arrive_expect_tx(&bars->l_full, kRows * 4);
+        __syncwarp();
         const uint32_t idesc_pv = tc::idesc_f16(128, 256, true, false, true);
         const uint32_t ring = smem_u32(smem);
         const uint32_t precv = smem_u32(smem + kOffPRecv);
@@ -558,27 +564,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < n_tiles && ok; ++i) {
           const int s = i % kNStage1;
-          mbar_arrive_expect_tx(&bars->p_full[i & 1], kPMsgBytes);
-          ok = mbar_wait(&bars->kv_full1[s], (i / kNStage1) & 1, p.err, kDevErrFullWait);
-          if (ok) ok = mbar_wait(&bars->p_full[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
-          if (ok) ok = mbar_wait(&bars->o_ready[i & 1], (i >> 1) & 1, p.err, kDevErrFullWait);
+          if (tc::elect_one()) mbar_arrive_expect_tx(&bars->p_full[i & 1], kPMsgBytes);
+          __syncwarp();
+          ok = warp_wait(&bars->kv_full1[s], (i / kNStage1) & 1, p.err);
+          if (ok) ok = warp_wait(&bars->p_full[i & 1], (i >> 1) & 1, p.err);
+          if (ok) ok = warp_wait(&bars->o_ready[i & 1], (i >> 1) & 1, p.err);
           if (!ok) break;
           tc::fence_after_sync();
           const uint64_t vd0 = tc::smem_desc_sw128(ring + s * kStage1Bytes, kBoxBytes, 1024);
           const uint64_t ad0 = tc::smem_desc_sw128(precv + (i & 1) * kPBytes, 16, 1024);
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < kTN / 16; ++ks) {
-            const uint64_t ad = ad0 + static_cast<uint64_t>((ks * 32) >> 4);
-            const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-            tc::mma_f16_ss(tmem + kColO, ad, vd0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv, acc);
-            tc::mma_f16_ss(tmem + kColO + 256, ad, vd0 + static_cast<uint64_t>((4 * kBoxBytes + ks * 2048) >> 4),
-                           idesc_pv, acc);
+            for (int ks = 0; ks < kTN / 16; ++ks) {
+              const uint64_t ad = ad0 + static_cast<uint64_t>((ks * 32) >> 4);
+              const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+              tc::mma_f16_ss(tmem + kColO, ad, vd0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv, acc);
+              tc::mma_f16_ss(tmem + kColO + 256, ad, vd0 + static_cast<uint64_t>((4 * kBoxBytes + ks * 2048) >> 4),
+                             idesc_pv, acc);
+            }
+            tc::mma_commit(smem_u32(&bars->pv_done));
+            tc::mma_commit(smem_u32(&bars->kv_empty1[s]));
+            // CTA 0 may refill P slot i & 1 (it waits for this only when a tile i + 2 exists)
+            if (i + 2 < n_tiles) mma_commit_multicast(smem_u32(&bars->p_empty[i & 1]), 0x1);
+            if (i == n_tiles - 1) tc::mma_commit(smem_u32(&bars->o_final));
           }
-          tc::mma_commit(smem_u32(&bars->pv_done));
-          tc::mma_commit(smem_u32(&bars->kv_empty1[s]));
-          // CTA 0 may refill P slot i & 1 (it waits for this only when a tile i + 2 exists)
-          if (i + 2 < n_tiles) mma_commit_multicast(smem_u32(&bars->p_empty[i & 1]), 0x1);
-          if (i == n_tiles - 1) tc::mma_commit(smem_u32(&bars->o_final));
+          __syncwarp();
         }
       }
     } else if (warp <= 5) {

@@ -56,6 +56,20 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// One lane of the (converged) warp, the same one on every call: the MMA-issuing roles run
+// their loops with the whole warp (waits, loop control and descriptors stay warp-uniform)
+// and let this lane issue.  Issued that way an MMA costs its issuer ~48 cycles; from a
+// lone lane-0 thread in a divergent branch, ~54-86, and a barrier wait there ~2x more.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
