@@ -12,19 +12,24 @@
 // item.  The output O = P V of 128 heads x 512 dims in fp32 fills all 512 TMEM columns
 // of one SM, and the scores need the whole 576-dim contraction, so the pair splits the
 // two products instead of the dims:
-//   CTA 0 (scores) keeps Q (128 x 576) in tensor memory, streams the 576-dim latent
-//          tiles, computes S = Q K^T (M 128, N 64 tokens, A from TMEM), runs the online
-//          softmax (one thread per head = TMEM lane) and pushes P (bf16, already the
-//          MMA operand) plus one rescale factor per head into CTA 1's shared memory
-//          with bulk DSMEM copies;
-//   CTA 1 (values) streams the same tiles' first 512 dims (the second read of each
-//          tile hits L2), applies the rescale factors to O in tensor memory when a
-//          row maximum moved, and accumulates O += P V (A = P from shared memory,
+//   CTA 0 (scores) keeps Q (128 x 576) -- dims 0..511 in tensor memory, the 64 rope dims
+//          in shared memory -- streams the latent in tiles of 128 tokens, computes
+//          S = Q K^T (M 128 heads, N 128 tokens, A from TMEM), runs the online softmax
+//          (one thread per head = TMEM lane) and pushes P (bf16, already the MMA
+//          operand) in two 64-token halves, with one rescale factor per head, into CTA 1's
+//          shared memory with bulk DSMEM copies;
+//   CTA 1 (values) streams the same tokens' first 512 dims in 64-token tiles (the second
+//          read of each tile hits L2), applies the rescale factors to O in tensor memory
+//          when a row maximum moved, and accumulates O += P V (A = P from shared memory,
 //          B = the MN-major V tile, two N = 256 halves).
-// Tensor work per 64-token tile: 36 k-steps of N = 64 on CTA 0 (split over two issuing
-// warps: one thread cannot issue N = 64 MMAs fast enough to keep the pipe busy), 8 of
-// N = 256 on CTA 1.  Only bf16 P (16 KB per tile) crosses between the SMs, one way.
-// Warp roles per CTA: TMA producer, MMA issuer(s), four row warps (softmax on CTA 0;
+// Tensor work per 128 tokens: 36 MMAs of N = 128 on CTA 0 and 16 of N = 256 on CTA 1.
+// An MMA-issuing warp runs its loop converged and lets one elected lane issue: an MMA then
+// costs its issuer ~48 cycles, so N = 128 (64 cycles of tensor work) keeps the pipe busy
+// from one warp, where N = 64 tiles (32 cycles) left it idle a third of the time.  CTA 0's
+// latent tiles stream through a ring of 64-dim x 128-token boxes, waited for and released
+// in three groups of three boxes per tile (one wait, fence and commit per twelve MMAs).
+// Only bf16 P (32 KB per 128 tokens) crosses between the SMs, one way.
+// Warp roles per CTA: TMA producer, MMA issuer, four row warps (softmax on CTA 0;
 // rescale, boundary-row zeroing and the epilogue on CTA 1).  Every wait is bounded.
 #include <cuda_runtime.h>
 
@@ -36,21 +41,26 @@ namespace skv {
 
 namespace {
 
-constexpr int kTN = 64;          // tokens per latent tile
+constexpr int kTN = 64;          // tokens per value tile (CTA 1) and per P half
+constexpr int kTS = 128;         // tokens per score tile (CTA 0): two value tiles
 constexpr int kRows = 128;       // heads per item (MMA M)
-constexpr int kThreads = 7 * 32;  // warp 6: second score-MMA issuer on CTA 0
+constexpr int kThreads = 6 * 32;
 constexpr int kKBoxes = 9;       // 64-dim boxes of the 576-dim key
 constexpr int kVBoxes = 8;       // 64-dim boxes of the 512-dim value
-constexpr int kBoxBytes = kTN * 128;     // 64 tokens x 64 dims
+constexpr int kBoxBytes = kTN * 128;     // 64 tokens x 64 dims (one TMA box)
+constexpr int kSBoxBytes = kTS * 128;    // 128 tokens x 64 dims (a CTA 0 ring slot, two TMA boxes)
 constexpr int kQBoxBytes = kRows * 128;  // 128 heads x 64 dims
-// CTA 0 (scores): Q staging, then a 2-stage ring of whole 576-dim tiles in the same bytes
-constexpr int kNStage0 = 2;
-constexpr int kStage0Bytes = kKBoxes * kBoxBytes;  // 72 KB
-constexpr int kOffPStage = kNStage0 * kStage0Bytes;  // 144 KB: P staging, 2 slots x 16 KB
+// CTA 0 (scores): Q staging, then a ring of kNBox0 box slots in the same bytes, filled and
+// released in groups of kGrp consecutive boxes of the stream (one wait and one release per
+// group: per box, the issuing warp's wait, fence and commit cost as much as its four MMAs)
+constexpr int kNBox0 = 10;
+constexpr int kGrp = 3;                // three groups per score tile, one ring slot each
+constexpr int kNGrp0 = kKBoxes / kGrp;  // group slots (the tenth box slot stays unused)
+constexpr int kOffPStage = kNBox0 * kSBoxBytes;      // 160 KB: P staging, 2 halves x 16 KB
 constexpr int kPBytes = kRows * 128;                 // 128 heads x 64 tokens bf16
 constexpr int kOffAStage = kOffPStage + 2 * kPBytes;  // rescale factors, 2 slots x 512 B
 constexpr int kOffLStage = kOffAStage + 2 * kRows * 4;  // final row sums, 512 B
-constexpr int kOffQRope = 182272;  // Q dims 512..575 (the rope part), 16 KB, kept in shared memory
+constexpr int kOffQRope = 198656;  // Q dims 512..575 (the rope part), 16 KB, kept in shared memory
 constexpr int kQTmemBoxes = 8;     // Q dims 0..511 live in TMEM
 // CTA 1 (values): a 3-stage ring of 512-dim tiles, P / factor / row-sum receive buffers
 constexpr int kNStage1 = 3;
@@ -59,32 +69,22 @@ constexpr int kOffPRecv = kNStage1 * kStage1Bytes;  // 192 KB
 constexpr int kOffARecv = kOffPRecv + 2 * kPBytes;
 constexpr int kOffLRecv = kOffARecv + 2 * kRows * 4;
 constexpr int kOffBar = kOffLRecv + kRows * 4;
-constexpr int kSmem = 1024 + kOffBar + 256;
-static_assert(kQTmemBoxes * kQBoxBytes <= kNStage0 * kStage0Bytes, "Q staging reuses the ring bytes");
+constexpr int kSmem = 1024 + kOffBar + 512;
+static_assert(kQTmemBoxes * kQBoxBytes <= kNBox0 * kSBoxBytes, "Q staging reuses the ring bytes");
 static_assert(kOffQRope % 1024 == 0 && kOffQRope >= kOffLStage + kRows * 4 && kOffQRope + kQBoxBytes <= kOffBar,
               "CTA 0's rope Q sits between its staging buffers and the barriers");
 static_assert(kOffLStage + kRows * 4 <= kOffBar, "CTA 0 layout fits below the barriers");
 static_assert(kOffPStage % 1024 == 0 && kOffPRecv % 1024 == 0, "P tiles need 1024-byte swizzle atoms");
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
+static_assert(kNBox0 > kKBoxes, "the ring holds a whole score tile and the start of the next");
+static_assert(kKBoxes % kGrp == 0 && kNGrp0 * kGrp <= kNBox0, "whole groups of a tile's boxes per ring slot");
 constexpr uint32_t kTmemCols = 512;
-// CTA 0: S buffer b at kColS + 128 b holds two partial sums, columns +0 (k-steps 0..17,
-// issued by warp 1) and +64 (k-steps 18..35, issued by warp 6): a single issuing thread
-// cannot keep the tensor pipe busy with N = 64 MMAs, two can.
+// CTA 0: S buffer b (128 x 128 fp32) at columns 128 b; Q dims 0..511 at 256.. (two bf16 per column)
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColQ = 256;  // CTA 0: Q dims 0..511, 256 columns (two bf16 per column)
-constexpr int kKSteps = kKBoxes * 4;     // 36 k-steps of 16 dims
-constexpr int kKStepsA = kKSteps / 2;    // warp 1: k-steps 0..17; warp 6: 18..35
+constexpr uint32_t kColQ = 256;
 constexpr uint32_t kColO = 0;    // CTA 1: O, 512 columns
-constexpr uint32_t kPMsgBytes = 4 * (32 * 128 + 32 * 4);  // P rows + factors, four warps
+constexpr uint32_t kPMsgBytes = 4 * (32 * 128 + 32 * 4);  // P rows + factors of one half, four warps
 constexpr float kRescaleThreshold = 8.0f;
-// CTA 0's two 72 KB stages keep too few bytes in flight to cover the HBM latency (a tile
-// took ~2.1k cycles from issue to arrival, so the ring ran at (latency + MMA) / 2 per
-// tile); its producer also prefetches the tile this far ahead into L2, so that the ring's
-// own loads (and CTA 1's reads) hit L2.  Measured: 3, 4 and 5 ahead all take the step from
-// 0.181 to ~0.165 ms; 6 and 8 gain less.  Over a paged cache the same prefetch (its page
-// looked up one tile ahead) cost 4 % (0.191 -> 0.199 ms, same box), so the paged
-// instantiation does not prefetch.
-constexpr int kL2Ahead = 4;
 
 // One barrier block at the same offset in both CTAs (remote arrivals address a peer's
 // barrier by this CTA's own offset).
@@ -92,9 +92,9 @@ struct MlaBars {
   // CTA 0
   uint64_t q_full;        // Q staged in shared memory
   uint64_t q_moved;       // Q copied into TMEM by the four row warps; staging bytes free
-  uint64_t kv_full0[kNStage0];
-  uint64_t kv_empty0[kNStage0];
-  uint64_t s_full[2];     // S(i) in TMEM buffer i & 1 (one commit from each issuing warp)
+  uint64_t grp_full[kNGrp0];   // the boxes of a group landed
+  uint64_t grp_empty[kNGrp0];  // the MMAs that read a group completed
+  uint64_t s_full[2];     // S of score tile T in TMEM buffer T & 1
   uint64_t s_free[2];     // the row warps have read S buffer b
   uint64_t p_empty[2];    // CTA 1 finished PV with P slot b (arrived by CTA 1's MMA commit)
   // CTA 1
@@ -107,7 +107,7 @@ struct MlaBars {
   uint64_t l_full;        // the final row sums landed
   uint32_t tmem_base;
 };
-static_assert(sizeof(MlaBars) <= 256, "barrier block");
+static_assert(sizeof(MlaBars) <= 512, "barrier block");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -155,14 +155,6 @@ __device__ __forceinline__ void tma_load_4d_plain(void* dst, const CUtensorMap* 
       : "memory");
 }
 
-// Prefetch one tensor-map box into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-
 // Bulk copy of `bytes` contiguous shared-memory bytes to global memory (this thread's bulk
 // group), and the waits for this thread's groups: sources read / copies complete.
 __device__ __forceinline__ void bulk_store_global(void* dst, uint32_t src_smem, uint32_t bytes) {
@@ -178,6 +170,22 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
   const bool ok = mbar_wait(bar, parity, err, kDevErrFullWait);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Page (paged cache) or sequence (contiguous) and row coordinate of the 64-token tile that
+// starts at token `tok`.  A tile at or past S_max holds only masked tokens; over a paged
+// cache it reads the page of the last tile inside S_max instead of a block-table entry past
+// the sequence's row.
+template <bool PAGED>
+__device__ __forceinline__ void tile_coords(const PartialParams& p, int b, int tok, int* outer, int* row) {
+  if constexpr (PAGED) {
+    const int t = tok < p.S_max ? tok : ((p.S_max - 1) / kTN) * kTN;
+    *outer = kv_page_of(p, b, t);
+    *row = t % p.block_len;
+  } else {
+    *outer = b;
+    *row = tok;
+  }
 }
 
 // PAGED: the latent lives in pages with a block table (kept out of the contiguous
@@ -217,22 +225,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t horizon = p.causal_offset + m_last / p.G;
     if (horizon < static_cast<int64_t>(r_hi) - 1) r_hi = static_cast<int>(max(horizon + 1, (int64_t)r_lo));
   }
+  // value tiles (64 tokens) from tile_begin; score tiles pair them, so the value CTA runs
+  // an even count (a last value tile past r_hi holds only masked tokens)
   const int tile_begin = r_lo / kTN;
-  const int n_tiles = (r_hi > r_lo) ? ((r_hi + kTN - 1) / kTN - tile_begin) : 0;
+  const int n64 = (r_hi > r_lo) ? ((r_hi + kTN - 1) / kTN - tile_begin) : 0;
+  const int n_score = (n64 + 1) / 2;
+  const int n_tiles = 2 * n_score;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_moved, 4);
-    for (int s = 0; s < kNStage0; ++s) {
-      mbar_init(&bars->kv_full0[s], 1);
-      mbar_init(&bars->kv_empty0[s], 2);  // both score-MMA warps release the stage
+    for (int s = 0; s < kNGrp0; ++s) {
+      mbar_init(&bars->grp_full[s], 1);
+      mbar_init(&bars->grp_empty[s], 1);
     }
     for (int s = 0; s < kNStage1; ++s) {
       mbar_init(&bars->kv_full1[s], 1);
       mbar_init(&bars->kv_empty1[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars->s_full[k], 2);
+      mbar_init(&bars->s_full[k], 1);
       mbar_init(&bars->s_free[k], 4);
       mbar_init(&bars->p_empty[k], 1);
       mbar_init(&bars->p_full[k], 1);
@@ -260,7 +272,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ================================================================ CTA 0: scores
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
-      if (lane == 0 && n_tiles > 0) {
+      // box bx (dims 64 bx ..) of every score tile sits in ring box slot bx; group g = boxes 3g .. 3g + 2
+      if (lane == 0 && n_score > 0) {
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tml);
         mbar_arrive_expect_tx(&bars->q_full, kKBoxes * kQBoxBytes);
@@ -268,84 +281,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int bx = 0; bx < kKBoxes; ++bx)
           tma_load_4d_plain(smem + (bx < kQTmemBoxes ? bx * kQBoxBytes : kOffQRope), &tmq, &bars->q_full, bx * 64, 0,
                             t_start, b);
-        // L2 prefetch of tile i (contiguous cache only)
-        auto prefetch = [&](int i) {
-          for (int bx = 0; bx < kKBoxes; ++bx) tma_prefetch_l2_4d(&tml, bx * 64, (tile_begin + i) * kTN, 0, b);
-        };
-        if constexpr (!PAGED)
-          for (int i = kNStage0; i < min(kL2Ahead, n_tiles); ++i) prefetch(i);
         bool ok = mbar_wait(&bars->q_moved, 0, p.err, kDevErrEmptyWait);  // the ring bytes are free
-        int page_next = b;  // paged: the next tile's page, read one tile ahead
-        if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * kTN);
-        int issued = 0;
-        for (int i = 0; i < n_tiles && ok; ++i) {
-          const int s = i % kNStage0;
-          if (i >= kNStage0 && !mbar_wait(&bars->kv_empty0[s], ((i / kNStage0) - 1) & 1, p.err, kDevErrEmptyWait))
-            break;
-          mbar_arrive_expect_tx(&bars->kv_full0[s], kStage0Bytes);
-          uint8_t* st = smem + s * kStage0Bytes;
-          const int tok = (tile_begin + i) * kTN;
-          const int outer = page_next;
-          int row = tok;
-          if constexpr (PAGED) {
-            row = tok % p.block_len;
-            if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
+        int outer0 = b, row0 = 0, outer1 = b, row1 = 0;
+        int issued = 0;  // groups issued
+        for (int T = 0; T < n_score && ok; ++T) {
+          const int tok = (tile_begin + 2 * T) * kTN;
+          tile_coords<PAGED>(p, b, tok, &outer0, &row0);
+          tile_coords<PAGED>(p, b, tok + kTN, &outer1, &row1);
+          for (int g = 0; g < kNGrp0; ++g) {  // group g of tile T goes to slot g
+            if (T >= 1 && !mbar_wait(&bars->grp_empty[g], (T - 1) & 1, p.err, kDevErrEmptyWait)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->grp_full[g], kGrp * kSBoxBytes);
+            for (int e = 0; e < kGrp; ++e) {
+              const int bx = g * kGrp + e;
+              uint8_t* st = smem + bx * kSBoxBytes;
+              tma_load_4d_plain(st, &tml, &bars->grp_full[g], bx * 64, row0, 0, outer0);
+              tma_load_4d_plain(st + kBoxBytes, &tml, &bars->grp_full[g], bx * 64, row1, 0, outer1);
+            }
+            ++issued;
           }
-          for (int bx = 0; bx < kKBoxes; ++bx)
-            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full0[s], bx * 64, row, 0, outer);
-          if constexpr (!PAGED)
-            if (i + kL2Ahead < n_tiles) prefetch(i + kL2Ahead);
-          issued = i + 1;
         }
-        for (int i = max(0, issued - kNStage0); i < issued; ++i) {
-          if (!mbar_wait(&bars->kv_full0[i % kNStage0], (i / kNStage0) & 1, p.err, kDevErrDrainWait)) break;
+        for (int gi = max(0, issued - kNGrp0); gi < issued; ++gi) {
+          if (!mbar_wait(&bars->grp_full[gi % kNGrp0], (gi / kNGrp0) & 1, p.err, kDevErrDrainWait)) break;
         }
         if (!ok) mbar_wait(&bars->q_full, 0, p.err, kDevErrDrainWait);  // Q copy still in flight
       }
-    } else if (warp == 1 || warp == 6) {
-      // ---------------------------------------------------------- MMA issuers: S = Q K^T
-      // warp 1: k-steps 0..17 into S buffer + 0; warp 6: k-steps 18..35 into S buffer + 64
-      // (its last four, the rope dims, take A = Q from shared memory).  Each warp runs the
-      // loop and its waits together; one elected lane issues the MMAs and commits.
-      if (n_tiles > 0) {
-        const uint32_t idesc_s = tc::idesc_f16(128, kTN, true, false, false);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer: S = Q K^T
+      // Per score tile: for each 64-dim box, four k-steps (M 128, N 128 tokens, K 16; A = Q
+      // from TMEM, the rope box's from shared memory), then the box is released.  The warp
+      // runs the loop and its waits together; one elected lane issues and commits.
+      if (n_score > 0) {
+        const uint32_t idesc_s = tc::idesc_f16(128, kTS, true, false, false);
         const uint32_t ring = smem_u32(smem);
         const uint64_t qrope_d0 = tc::smem_desc_sw128(smem_u32(smem + kOffQRope), 16, 1024);
         bool ok = warp_wait(&bars->q_moved, 0, p.err);
-        for (int i = 0; i < n_tiles && ok; ++i) {
-          const int s = i % kNStage0;
-          ok = warp_wait(&bars->kv_full0[s], (i / kNStage0) & 1, p.err);
-          if (ok && i >= 2) ok = warp_wait(&bars->s_free[i & 1], ((i >> 1) - 1) & 1, p.err);
-          if (!ok) break;
-          tc::fence_after_sync();
-          // descriptors built once per tile; the k-steps add compile-time offsets
-          const uint64_t bd0 = tc::smem_desc_sw128(ring + s * kStage0Bytes, 16, 1024);
-          if (tc::elect_one()) {
-            if (warp == 1) {
-              const uint32_t d = tmem + kColS + 128 * (i & 1);
+        // Every MMA operand is a compile-time offset from per-CTA bases (box bx of a tile
+        // always sits in ring box slot bx): the unrolled tile body issues at the tensor
+        // pipe's pace.  Only the S buffer alternates between tiles.
+        const uint64_t bd_ring = tc::smem_desc_sw128(ring, 16, 1024);
+        for (int T = 0; T < n_score && ok; ++T) {
+          if (T >= 2) {  // S buffer T & 1 was read by the softmax of tile T - 2
+            ok = warp_wait(&bars->s_free[T & 1], ((T >> 1) - 1) & 1, p.err);
+            if (!ok) break;
+          }
+          const uint32_t d = tmem + kColS + 128 * (T & 1);
 #pragma unroll
-              for (int ks = 0; ks < kKStepsA; ++ks) {
-                const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
-                tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, ks > 0 ? 1u : 0u);
-              }
-            } else {
-              const uint32_t d = tmem + kColS + 128 * (i & 1) + 64;
+          for (int g = 0; g < kNGrp0; ++g) {
+            ok = warp_wait(&bars->grp_full[g], T & 1, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+            if (tc::elect_one()) {
 #pragma unroll
-              for (int ks = kKStepsA; ks < kKSteps; ++ks) {
-                const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
-                const uint32_t acc = ks > kKStepsA ? 1u : 0u;
-                if (ks < kQTmemBoxes * 4) {
-                  tc::mma_f16_ts(d, tmem + kColQ + ks * 8, bd, idesc_s, acc);
-                } else {
-                  const uint64_t ad = qrope_d0 + static_cast<uint64_t>(((ks & 3) * 32) >> 4);
-                  tc::mma_f16_ss(d, ad, bd, idesc_s, acc);
+              for (int e = 0; e < kGrp; ++e) {
+                const int bx = g * kGrp + e;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd = bd_ring + static_cast<uint64_t>((bx * kSBoxBytes + k * 32) >> 4);
+                  if (bx < kQTmemBoxes)
+                    tc::mma_f16_ts(d, tmem + kColQ + 32 * bx + 8 * k, bd, idesc_s, (bx | k) ? 1u : 0u);
+                  else
+                    tc::mma_f16_ss(d, qrope_d0 + static_cast<uint64_t>((k * 32) >> 4), bd, idesc_s, 1u);
                 }
               }
+              tc::mma_commit(smem_u32(&bars->grp_empty[g]));
+              if (g == kNGrp0 - 1) tc::mma_commit(smem_u32(&bars->s_full[T & 1]));
             }
-            tc::mma_commit(smem_u32(&bars->s_full[i & 1]));
-            tc::mma_commit(smem_u32(&bars->kv_empty0[s]));
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
     } else {
@@ -366,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l_sum = 0.f, l_pv = 0.f;
       bool ok = true;
 
-      if (n_tiles > 0) {
+      if (n_score > 0) {
         // Q row, dims 0..511 -> TMEM columns kColQ + 32 bx + (0..31): the A operand of the
         // TMEM-fed S MMAs
         ok = warp_wait(&bars->q_full, 0, p.err);
@@ -396,109 +401,105 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->q_moved);
       }
 
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int t0 = (tile_begin + i) * kTN;
-        ok = warp_wait(&bars->s_full[i & 1], (i >> 1) & 1, p.err);
+      const float sl = p.scale_log2;
+      for (int T = 0; T < n_score && ok; ++T) {
+        const int t0 = (tile_begin + 2 * T) * kTN;
+        ok = warp_wait(&bars->s_full[T & 1], (T >> 1) & 1, p.err);
         if (!ok) break;
         tc::fence_after_sync();
-        float sv[kTN];
+        float sv[kTS];
         {
-          uint32_t r[4][16];
-          const uint32_t sc = t_lane + kColS + 128 * (i & 1);
+          uint32_t r[8][16];
+          const uint32_t sc = t_lane + kColS + 128 * (T & 1);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(sc + 16 * cc, r[cc]);
+          for (int cc = 0; cc < 8; ++cc) tc::tmem_ld16(sc + 16 * cc, r[cc]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
             for (int e = 0; e < 16; ++e) sv[16 * cc + e] = __uint_as_float(r[cc][e]);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld16(sc + 64 + 16 * cc, r[cc]);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sv[16 * cc + e] += __uint_as_float(r[cc][e]);
         }
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[i & 1]);
+        if (lane == 0) mbar_arrive(&bars->s_free[T & 1]);
 
         // ---- mask, running maximum (moved only when it rises by more than 2^8)
-        const bool in_range = (t0 >= r_lo) && (t0 + kTN <= r_hi);
-        const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTN - 1 > hz_min);
+        const bool in_range = (t0 >= r_lo) && (t0 + kTS <= r_hi);
+        const bool need_mask = !in_range || (static_cast<int64_t>(t0) + kTS - 1 > hz_min);
         if (need_mask) {
-          const int c_lo = min(max(r_lo - t0, 0), kTN);
+          const int c_lo = min(max(r_lo - t0, 0), kTS);
           const int c_hi = static_cast<int>(
-              min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTN));
+              min(max(min(static_cast<int64_t>(r_hi), hz + 1) - t0, (int64_t)0), (int64_t)kTS));
           const unsigned span = static_cast<unsigned>(max(c_hi - c_lo, 0));
 #pragma unroll
-          for (int cc = 0; cc < kTN; ++cc) sv[cc] = (static_cast<unsigned>(cc - c_lo) < span) ? sv[cc] : -INFINITY;
+          for (int cc = 0; cc < kTS; ++cc) sv[cc] = (static_cast<unsigned>(cc - c_lo) < span) ? sv[cc] : -INFINITY;
         }
-        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+        float mx[4] = {fmaxf(sv[0], sv[4]), fmaxf(sv[1], sv[5]), fmaxf(sv[2], sv[6]), fmaxf(sv[3], sv[7])};
 #pragma unroll
-        for (int cc = 4; cc < kTN; cc += 4) {
-          mx[0] = fmaxf(mx[0], sv[cc]);
-          mx[1] = fmaxf(mx[1], sv[cc + 1]);
-          mx[2] = fmaxf(mx[2], sv[cc + 2]);
-          mx[3] = fmaxf(mx[3], sv[cc + 3]);
+        for (int cc = 8; cc < kTS; cc += 8) {  // columns cc .. cc + 7
+          mx[0] = fmax3(mx[0], sv[cc], sv[cc + 4]);
+          mx[1] = fmax3(mx[1], sv[cc + 1], sv[cc + 5]);
+          mx[2] = fmax3(mx[2], sv[cc + 2], sv[cc + 6]);
+          mx[3] = fmax3(mx[3], sv[cc + 3], sv[cc + 7]);
         }
-        const float sl = p.scale_log2;
         const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
-        float alpha = 1.f;  // factor CTA 1 applies to O before adding P(i) V(i)
+        float alpha = 1.f;  // factor CTA 1 applies to O before adding the first half's P V
         if ((tmax != -INFINITY) && (m_used == -INFINITY || tmax > m_used + kRescaleThreshold)) {
           const float m_new = fmaxf(m_used, tmax);
-          alpha = (i > 0) ? fast_exp2(m_used - m_new) : 1.f;
+          alpha = (T > 0) ? fast_exp2(m_used - m_new) : 1.f;
           l_sum *= alpha;
           l_pv *= alpha;
           m_used = m_new;
         }
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
 
-        // ---- P(i) into staging slot i & 1 (SW128 K-major rows); the slot's previous
-        // copy has landed once CTA 1 finished PV(i - 2) with it
-        if (i >= 2) {
-          ok = warp_wait(&bars->p_empty[i & 1], ((i >> 1) - 1) & 1, p.err);
-          if (!ok) break;
-        }
-        uint8_t* pst = smem + kOffPStage + (i & 1) * kPBytes;
-        uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
+        // ---- P of the two 64-token halves into staging slots 0 and 1 (SW128 K-major rows);
+        // a slot's previous copy has landed once CTA 1 finished PV with it (half 2T - 2 + hf)
 #pragma unroll
-        for (int ch = 0; ch < kTN / 8; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(fmaf(sv[8 * ch + 2 * e], sl, -base));
-            const float p1 = fast_exp2(fmaf(sv[8 * ch + 2 * e + 1], sl, -base));
-            ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
-            w[e] = pack_bf16(p0, p1);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (T >= 1) {
+            ok = warp_wait(&bars->p_empty[hf], (T - 1) & 1, p.err);
+            if (!ok) break;
           }
-          *reinterpret_cast<uint4*>(pst + swz128(row, ch * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l_sum += sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
-        float* ast = reinterpret_cast<float*>(smem + kOffAStage + (i & 1) * kRows * 4);
-        ast[row] = alpha;
-        fence_proxy_async_smem();  // generic writes before the bulk copy reads them
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t bar = (i & 1) ? peer_p_full1 : peer_p_full0;
-          const uint32_t off = static_cast<uint32_t>((i & 1) * kPBytes + lgrp * 32 * 128);
-          bulk_copy_to_peer(peer_precv + off, smem_u32(smem + kOffPStage + off), 32 * 128, bar);
-          const uint32_t aoff = static_cast<uint32_t>((i & 1) * kRows * 4 + lgrp * 32 * 4);
-          bulk_copy_to_peer(peer_arecv + aoff, smem_u32(smem + kOffAStage + aoff), 32 * 4, bar);
-        }
-        // the sum of the rounded weights, off the path to the copy: re-read the staged row
-        // (the copy only reads it too; the slot is rewritten only after PV(i) is done)
-        uint64_t lr[2] = {0ull, 0ull};
+          uint8_t* pst = smem + kOffPStage + hf * kPBytes;
+          uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
 #pragma unroll
-        for (int ch = 0; ch < kTN / 8; ++ch) {
-          const uint4 q = *reinterpret_cast<const uint4*>(pst + swz128(row, ch * 16));
-          lr[0] = add_f32x2(lr[0], bf16_lo(q.x), bf16_hi(q.x));
-          lr[1] = add_f32x2(lr[1], bf16_lo(q.y), bf16_hi(q.y));
-          lr[0] = add_f32x2(lr[0], bf16_lo(q.z), bf16_hi(q.z));
-          lr[1] = add_f32x2(lr[1], bf16_lo(q.w), bf16_hi(q.w));
+          for (int ch = 0; ch < kTN / 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = fast_exp2(fmaf(sv[hf * kTN + 8 * ch + 2 * e], sl, -base));
+              const float p1 = fast_exp2(fmaf(sv[hf * kTN + 8 * ch + 2 * e + 1], sl, -base));
+              ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
+              w[e] = pack_bf16(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(pst + swz128(row, ch * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          l_sum += sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
+          float* ast = reinterpret_cast<float*>(smem + kOffAStage + hf * kRows * 4);
+          ast[row] = hf == 0 ? alpha : 1.f;
+          fence_proxy_async_smem();  // generic writes before the bulk copy reads them
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t bar = hf ? peer_p_full1 : peer_p_full0;
+            const uint32_t off = static_cast<uint32_t>(hf * kPBytes + lgrp * 32 * 128);
+            bulk_copy_to_peer(peer_precv + off, smem_u32(smem + kOffPStage + off), 32 * 128, bar);
+            const uint32_t aoff = static_cast<uint32_t>(hf * kRows * 4 + lgrp * 32 * 4);
+            bulk_copy_to_peer(peer_arecv + aoff, smem_u32(smem + kOffAStage + aoff), 32 * 4, bar);
+          }
+          // the sum of the rounded weights, off the path to the copy: re-read the staged row
+          // (the copy only reads it too; the slot is rewritten only after this PV is done)
+          uint64_t lr[2] = {0ull, 0ull};
+#pragma unroll
+          for (int ch = 0; ch < kTN / 8; ++ch) {
+            const uint4 q = *reinterpret_cast<const uint4*>(pst + swz128(row, ch * 16));
+            lr[0] = add_f32x2(lr[0], bf16_lo(q.x), bf16_hi(q.x));
+            lr[1] = add_f32x2(lr[1], bf16_lo(q.y), bf16_hi(q.y));
+            lr[0] = add_f32x2(lr[0], bf16_lo(q.z), bf16_hi(q.z));
+            lr[1] = add_f32x2(lr[1], bf16_lo(q.w), bf16_hi(q.w));
+          }
+          l_pv += sum_f32x2(lr[0]) + sum_f32x2(lr[1]);
         }
-        l_pv += sum_f32x2(lr[0]) + sum_f32x2(lr[1]);
       }
 
       // ---- final row sums to CTA 1 (it normalises O); lse from here
@@ -527,24 +528,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       if (lane == 0 && n_tiles > 0) {
         tma_prefetch_desc(&tml);
-        int page_next = b;  // paged: the next tile's page, read one tile ahead
-        if constexpr (PAGED) page_next = kv_page_of(p, b, tile_begin * kTN);
+        int outer = b, row_c = 0;
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
           const int s = i % kNStage1;
           if (i >= kNStage1 && !mbar_wait(&bars->kv_empty1[s], ((i / kNStage1) - 1) & 1, p.err, kDevErrEmptyWait))
             break;
+          tile_coords<PAGED>(p, b, (tile_begin + i) * kTN, &outer, &row_c);
           mbar_arrive_expect_tx(&bars->kv_full1[s], kStage1Bytes);
           uint8_t* st = smem + s * kStage1Bytes;
-          const int tok = (tile_begin + i) * kTN;
-          const int outer = page_next;
-          int row = tok;
-          if constexpr (PAGED) {
-            row = tok % p.block_len;
-            if (i + 1 < n_tiles) page_next = kv_page_of(p, b, tok + kTN);
-          }
           for (int bx = 0; bx < kVBoxes; ++bx)
-            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row, 0, outer);
+            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row_c, 0, outer);
           issued = i + 1;
         }
         for (int i = max(0, issued - kNStage1); i < issued; ++i) {
@@ -591,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
-    } else if (warp <= 5) {
+    } else {
       // ---------------------------------------------------------- row warps
       const int m = m0 + row;
       const bool valid = m < rows_total;
