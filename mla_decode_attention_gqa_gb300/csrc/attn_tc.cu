@@ -31,6 +31,8 @@
 #include <climits>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "skv_common.cuh"
 #include "skv_internal.h"
 #include "tc_common.cuh"
@@ -281,30 +283,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err, kDevErrFullWait));
       };
       bool ok = wait_all(&bars->q_full, 0);
-      // Descriptors are built once per call and the k-steps add compile-time offsets.
-      auto issue_s = [&](int k, int i) {  // S_k = Q_k K_i^T  (M 128, N 128 tokens, K 128)
-        const uint64_t ad0 = tc::smem_desc_sw128(q_base + k * kQTileBytes, 16, 1024);
-        const uint64_t bd0 = tc::smem_desc_sw128(ring + (i % kNStage) * kStageBytes, 16, 1024);
+      // Every MMA operand is a compile-time offset from per-CTA descriptor bases: the loop
+      // over K/V tiles is unrolled by the ring depth, so a tile's stage is a constant too
+      // (a stage index computed at run time raised each MMA's issue cost by a half).
+      const uint64_t qd_base = tc::smem_desc_sw128(q_base, 16, 1024);
+      const uint64_t kd_base = tc::smem_desc_sw128(ring, 16, 1024);
+      const uint64_t vd_base = tc::smem_desc_sw128(ring + kKTileBytes, kKVBoxBytes, 1024);
+      auto issue_s = [&](int k, int stage) {  // S_k = Q_k K^T  (M 128, N 128 tokens, K 128)
         const uint32_t d = tmem + kColS + 128 * k;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint64_t ad = ad0 + static_cast<uint64_t>(((ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32) >> 4);
-          const uint64_t bd = bd0 + static_cast<uint64_t>(((ks >> 2) * kKVBoxBytes + (ks & 3) * 32) >> 4);
+          const uint64_t ad =
+              qd_base + static_cast<uint64_t>((k * kQTileBytes + (ks >> 2) * (kQTileBytes / 2) + (ks & 3) * 32) >> 4);
+          const uint64_t bd =
+              kd_base + static_cast<uint64_t>((stage * kStageBytes + (ks >> 2) * kKVBoxBytes + (ks & 3) * 32) >> 4);
           tc::mma_f16_ss(d, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int k, int i) {  // O_k += P_k V_i  (M 128, N 128, K 128; P_k from TMEM)
-        const uint64_t bd0 =
-            tc::smem_desc_sw128(ring + (i % kNStage) * kStageBytes + kKTileBytes, kKVBoxBytes, 1024);
+      auto issue_pv = [&](int k, int stage, uint32_t acc0) {  // O_k += P_k V  (M 128, N 128, K 128; P_k from TMEM)
         const uint32_t d = tmem + kColO + 128 * k;
         const uint32_t a = tmem + kColS + 128 * k;
-        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < kTN / 16; ++ks) {
-          tc::mma_f16_ts(d, a + ks * 8, bd0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv,
-                         ks > 0 ? 1u : acc0);
+          tc::mma_f16_ts(d, a + ks * 8, vd_base + static_cast<uint64_t>((stage * kStageBytes + ks * 2048) >> 4),
+                         idesc_pv, ks > 0 ? 1u : acc0);
         }
       };
+      // one K/V tile i in stage ST (= i % kNStage): PV0(i), S0(i+1), PV1(i), S1(i+1)
+      auto tile = [&](auto stage_c, int i) {
+        constexpr int ST = decltype(stage_c)::value;
+        constexpr int NX = (ST + 1) % kNStage;
+        ok = wait_all(&bars->p_full[0], i & 1);
+        if (!ok) return;
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          issue_pv(0, ST, i > 0 ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bars->pv_done[0]));
+        }
+        __syncwarp();
+        if (i + 1 < n_used) {
+          ok = wait_all(&bars->kv_full[NX], ((i + 1) / kNStage) & 1);
+          if (!ok) return;
+          tc::fence_after_sync();
+          if (tc::elect_one()) {
+            issue_s(0, NX);
+            tc::mma_commit(smem_u32(&bars->s_full[0]));
+          }
+          __syncwarp();
+        }
+        ok = wait_all(&bars->p_full[1], i & 1);
+        if (!ok) return;
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          issue_pv(1, ST, i > 0 ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bars->pv_done[1]));
+          tc::mma_commit(smem_u32(&bars->kv_empty[ST]));
+          if (i + 1 < n_used) {
+            issue_s(1, NX);
+            tc::mma_commit(smem_u32(&bars->s_full[1]));
+          }
+        }
+        __syncwarp();
+      };
+      static_assert(kNStage == 2, "the tile loop is unrolled by the ring depth");
       if (ok) ok = wait_all(&bars->kv_full[0], 0);
       if (ok) {
         tc::fence_after_sync();
@@ -315,38 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_commit(smem_u32(&bars->s_full[1]));
         }
         __syncwarp();
-        for (int i = 0; i < n_used && ok; ++i) {
-          ok = wait_all(&bars->p_full[0], i & 1);
-          if (!ok) break;
-          tc::fence_after_sync();
-          if (tc::elect_one()) {
-            issue_pv(0, i);
-            tc::mma_commit(smem_u32(&bars->pv_done[0]));
-          }
-          __syncwarp();
-          if (i + 1 < n_used) {
-            ok = wait_all(&bars->kv_full[(i + 1) % kNStage], ((i + 1) / kNStage) & 1);
-            if (!ok) break;
-            tc::fence_after_sync();
-            if (tc::elect_one()) {
-              issue_s(0, i + 1);
-              tc::mma_commit(smem_u32(&bars->s_full[0]));
-            }
-            __syncwarp();
-          }
-          ok = wait_all(&bars->p_full[1], i & 1);
-          if (!ok) break;
-          tc::fence_after_sync();
-          if (tc::elect_one()) {
-            issue_pv(1, i);
-            tc::mma_commit(smem_u32(&bars->pv_done[1]));
-            tc::mma_commit(smem_u32(&bars->kv_empty[i % kNStage]));
-            if (i + 1 < n_used) {
-              issue_s(1, i + 1);
-              tc::mma_commit(smem_u32(&bars->s_full[1]));
-            }
-          }
-          __syncwarp();
+        for (int i = 0; i < n_used && ok; i += 2) {
+          tile(std::integral_constant<int, 0>{}, i);
+          if (ok && i + 1 < n_used) tile(std::integral_constant<int, 1>{}, i + 1);
         }
       }
     }
