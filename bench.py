@@ -689,6 +689,65 @@ def workload_summary(w, m, steps, parity):
             "parity": parity}
 
 
+def kvp_arm(args, w, ws, rank, local):
+    """KVP decode across ranks (--mode kvp): rank r holds shard r (tokens [r S/N, (r+1) S/N))
+    of every sequence of the workload, runs its partials into the All-to-All send buffer,
+    exchanges them over the query-head axis (NCCL all_to_all_single; identity on one rank)
+    and merges the received partials of its own Hq/N heads: the step of
+    mla_decode_attention_gqa_gb300.kvp.kvp_decode_step.  value = the KV bytes of all shards
+    over the slowest rank's step time ("scaling": "strong": the problem is fixed)."""
+    import mla_decode_attention_gqa_gb300 as skv  # noqa: F401 - loads the library
+    from mla_decode_attention_gqa_gb300 import kvp
+
+    dev = torch.device("cuda", local)
+    S_loc = w.S // ws
+    gen = torch.Generator().manual_seed(w.seed)
+    seq = (torch.randint(w.S // 2, w.S + 1, (w.B,), generator=gen) if w.ragged else torch.full((w.B,), w.S)).tolist()
+    lens = [min(max(n - rank * S_loc, 0), S_loc) for n in seq]
+    shard = W.scaled(w, S=S_loc, ragged=False, n_split=1, seed=w.seed + 1 + rank)
+    inp = W.make_inputs(shard, dev, poison=False)
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
+    scales = (kvp.slab_scales(inp["k_scale"], inp["v_scale"], w.Hq, w.Hkv, ws) if w.kv_dtype == "fp8_e4m3" else None)
+    all_lens = [min(max(n - r * S_loc, 0), S_loc) for r in range(ws) for n in seq]
+    kv_bytes = RL.kv_bytes(w.Hkv, w.dk, w.dv, w.kv_dtype, all_lens, [[0, S_loc]] * len(all_lens),
+                           scale_block=w.scale_block)
+    bufs = None
+
+    def step():
+        nonlocal bufs
+        _, _, bufs = kvp.kvp_decode_step(inp["q"], inp["k"], inp["v"], seq_lens, softmax_scale=w.scale,
+                                         scale_block=w.scale_block, scales=scales, buffers=bufs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    ms = max_over_ranks(a.elapsed_time(b), ws) / args.steps
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(kv_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "us_per_layer": round(ms * 1e3, 2),
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3 KV, bf16 q", "data": "synthetic (seeded N(0,1))",
+            "config": dict(config_of(w, ws), parallelism=f"kvp{ws}", kvp_shard_tokens=S_loc),
+            "mode": "kvp", "clocks": clocks,
+            "gpu_launches": (ws + 1) * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def ours_arm(args, w, ws, rank, local):
     want_par = not args.no_cpu_baseline
     m = measure(args, w, ws, rank, local, want_e2e=not args.no_e2e, want_parity=want_par)
@@ -753,6 +812,9 @@ def main():
     ap.add_argument("--S", type=int, default=None, help="smaller KV length of the same workload (profiling)")
     ap.add_argument("--B", type=int, default=None, help="smaller batch of the same workload (profiling)")
     ap.add_argument("--Tq", type=int, default=None, help="fewer query rows of the same workload (profiling)")
+    ap.add_argument("--mode", choices=["replicas", "kvp"], default="replicas",
+                    help="replicas: every rank runs the whole workload (default); kvp: the workload's sequence is "
+                         "sharded over the ranks and one All-to-All over the query heads exchanges the partials")
     ap.add_argument("--extras", default="auto",
                     help="workloads measured after the main one: 'auto' (the long-context fp8 decode, the MLA "
                          "decode and the ring-prefill chunk fused and as ring steps, when the default workload runs "
@@ -765,6 +827,8 @@ def main():
     if over:
         w = W.scaled(w, **over)
     ws, rank, local = dist_setup()
+    if args.mode == "kvp" and args.config == W.HELIX_DENSE_128K.name:
+        w = W.HELIX_KVP8_FP8_1M  # the KVP mode's workload: the long-context fp8 decode
     if args.extras == "auto":
         args.extra_names = list(EXTRA_WORKLOADS) if (ws == 1 and not over and w.name == W.HELIX_DENSE_128K.name) else []
     elif args.extras == "none":
@@ -773,6 +837,8 @@ def main():
         args.extra_names = [workload_by_name(n).name for n in args.extras.split(",") if n]
     if args.impl == "reference":
         reference_arm(args, w, ws, rank)
+    elif args.mode == "kvp":
+        kvp_arm(args, w, ws, rank, local)
     else:
         ours_arm(args, w, ws, rank, local)
     if ws > 1:

@@ -60,6 +60,13 @@
  *     (finite while the V block scale stays below 65504, i.e. |V| below 2.9e7).
  *   - MLA (latent KV): Hkv = 1, dk = 576 (512 latent + 64 rope), dv = 512 and
  *     v_cache = k_cache with the same strides (V is the first 512 latent columns).
+ *   - Supported shapes (anything else returns SKV_EUNSUPPORTED before launch): bf16 KV
+ *     with dk = dv = 64 or 128; fp8-e4m3 KV with dk = dv = 128; the bf16 MLA latent above.
+ *     Any Hq multiple of Hkv, any Tq and B; bf16 dk = dv = 128 with Hq / Hkv dividing 128
+ *     and at least 128 (query row, head) rows per KV head runs on the tensor-core kernel,
+ *     the MLA latent with Hq dividing 128 on the tensor-core cluster kernel.  Strides are
+ *     free within the alignment rules of each call (16-byte aligned rows, 16-byte
+ *     multiples for K/V strides, 8-element multiples for q strides).
  */
 #ifndef SPLITKV_ATTN_H
 #define SPLITKV_ATTN_H

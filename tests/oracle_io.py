@@ -10,10 +10,19 @@ import oracle
 TOL_BF16 = {"out": 1e-2, "lse": 1e-3}
 TOL_FP8 = {"out": 4e-2, "lse": 4e-2}
 # The bars apply to the computed output.  An output stored in bf16 is further rounded to
-# nearest: at most half an ulp, 2^-8 * |o| (0.0156 at |o| = 4, where a row that sees one
-# token returns a raw V row), so bf16 outputs get that term on top of the bar; fp32
-# outputs (the partials) are held to the bare bar.
-BF16_STORE_REL = 2.0 ** -8
+# nearest, by up to half an ulp (0.0156 for |o| in [4, 8): a weighted mean of a few V rows
+# can land there), so a bf16 output element may also differ from the reference by the
+# reference's own bf16 rounding |bf16(o_ref) - o_ref|.  Where the GPU's value rounds to the
+# other neighbour the two sit on either side of a rounding midpoint within the computation
+# error e of each other, so the excess over that allowance is at most 2e: the bar still
+# bounds the computation.  fp32 outputs (the partials) are held to the bare bar.
+
+
+def bf16_round(x):
+    """Nearest bfloat16 value of float64 x (ties to even), as float64: 8 significant bits."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)  # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)  # np.rint rounds halves to even
 
 
 def tol_for(w):
@@ -24,13 +33,35 @@ def q_f64(q):
     return oracle.bf16_bits_to_f64(q.contiguous().view(torch.int16).cpu().numpy())
 
 
-def kv_f64(inp, w, which, b, g):
-    """Dequantised K or V rows [S, d] of (batch b, KV head g) as float64."""
+_E4M3_TABLE = None
+
+
+def e4m3_table():
+    """The oracle's value of every e4m3 code (its bit-layout decoder applied to all 256)."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        _E4M3_TABLE = oracle.e4m3_bits_to_f64(np.arange(256, dtype=np.uint8))
+    return _E4M3_TABLE
+
+
+def dequant_fp8_rows(codes, scales, block):
+    """oracle.dequant_e4m3_blocks for rows 0.. of a (batch, KV head), through the oracle's
+    code table (one gather instead of the bit decoding of every element: the full-size
+    caches hold 2^27 codes per group)."""
+    codes = np.asarray(codes)
+    s = np.asarray(scales, dtype=np.float64)[np.arange(codes.shape[0]) // block]
+    return e4m3_table()[codes] * s[:, None]
+
+
+def kv_f64(inp, w, which, b, g, n_tok=None):
+    """Dequantised K or V rows [n_tok, d] (default: all S) of (batch b, KV head g) as float64."""
     t = inp[which][b, g]
+    if n_tok is not None:
+        t = t[:n_tok]
     if w.kv_dtype == "bf16":
         return oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).cpu().numpy())
     scales = inp["k_scale" if which == "k" else "v_scale"][b, g].cpu().numpy()
-    return oracle.dequant_e4m3_blocks(t.contiguous().cpu().numpy(), scales, w.scale_block)
+    return dequant_fp8_rows(t.contiguous().cpu().numpy(), scales, w.scale_block)
 
 
 def oracle_group(inp, w, b, g, bounds=None, causal_offset=None):
@@ -80,8 +111,9 @@ def assert_close(got_o, got_lse, ref_o, ref_lse, tol, what=""):
     err_o = float(np.max(np.abs(go - ref_o))) if go.size else 0.0
     err_l = float(np.max(np.abs(gl[full] - ref_lse[full]))) if full.any() else 0.0
     if stored_bf16:
-        # element-wise: |o - o_ref| <= bar + 2^-8 |o_ref|; report the excess over the bar
-        excess = float(np.max(np.abs(go - ref_o) - BF16_STORE_REL * np.abs(ref_o))) if go.size else 0.0
+        # element-wise: |o - o_ref| <= bar + |bf16(o_ref) - o_ref|; report the excess over the bar
+        allow = np.abs(bf16_round(ref_o) - ref_o)
+        excess = float(np.max(np.abs(go - ref_o) - allow)) if go.size else 0.0
         assert excess <= tol["out"], (f"{what}: out err beyond bf16 storage rounding {excess:.3e} > {tol['out']} "
                                       f"(max-abs {err_o:.3e})")
     else:
@@ -118,8 +150,9 @@ def oracle_rows(inp, w, b, g, t_rows, bounds=None, causal_offset=None):
     seq = inp["seq_lens_host"][b]
     t_rows = list(t_rows)
     qb = q_f64(inp["q"][b, t_rows, g * G : (g + 1) * G])  # [R, G, dk]
-    kf = kv_f64(inp, w, "k", b, g)
-    vf = kv_f64(inp, w, "v", b, g)
+    n_tok = min(seq, w.S)  # tokens at or past seq_len are never visible
+    kf = kv_f64(inp, w, "k", b, g, n_tok)
+    vf = kv_f64(inp, w, "v", b, g, n_tok)
     R = len(t_rows)
     o = np.zeros((n_split, R, G, w.dv))
     lse = np.full((n_split, R, G), -np.inf)

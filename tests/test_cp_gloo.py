@@ -6,8 +6,10 @@ KVP decode ("Helix Parallelism: Why Tensor Parallelism Hits a Wall at Million-To
 Context", section "Sharding the sequence instead"): every rank holds one contiguous shard
 of every sequence's KV, computes the partial of all query heads over it, and one
 All-to-All over the query-head axis gives each rank every shard's partial for its own
-slab of heads, which it merges exactly by the lse.  The test also checks that
-a rank's send buffer is its split's slab of the single-GPU partial layout
+slab of heads, which it merges exactly by the lse.  The ranks run the package's exchange
+step (mla_decode_attention_gqa_gb300.kvp.kvp_decode_step, the function bench.py's KVP mode
+runs over NCCL) with the oracle as the attention and the merge.  The test also checks that
+a rank's send buffer, slabs side by side, is its split of the single-GPU partial layout
 [split][B][Tq][Hq][dv], the layout attn_partial writes.
 
 Pass-KV prefill ("Context Parallelism for Scalable Million-Token Inference", section
@@ -67,6 +69,7 @@ def _kvp_worker(rank, port, out_q):
     import torch.distributed as dist
 
     import oracle
+    from mla_decode_attention_gqa_gb300 import kvp
 
     dist.init_process_group("gloo", rank=rank, world_size=N_RANKS)
     q, k, v, lens = _kvp_problem()
@@ -75,19 +78,28 @@ def _kvp_worker(rank, port, out_q):
     # this rank's shard: tokens [lo, lo + m) of every sequence, and how many of them exist
     k_loc, v_loc = k[:, :, lo:lo + m], v[:, :, lo:lo + m]
     lens_loc = [min(max(n - lo, 0), m) for n in lens]
-    o, lse = oracle.split_attention(q, k_loc, v_loc, lens_loc, [[0, m]] * B, NO_CAUSAL, SCALE)
-    o, lse = o[0], lse[0]  # [B, 1, Hq, D], [B, 1, Hq]
-    # All-to-All over the head axis: slab j of the heads goes to rank j
-    hs = HQ // N_RANKS
-    send_o = torch.from_numpy(np.ascontiguousarray(o.reshape(B, 1, N_RANKS, hs, D).transpose(2, 0, 1, 3, 4)))
-    send_l = torch.from_numpy(np.ascontiguousarray(lse.reshape(B, 1, N_RANKS, hs).transpose(2, 0, 1, 3)))
-    recv_o, recv_l = torch.empty_like(send_o), torch.empty_like(send_l)
-    dist.all_to_all_single(recv_o, send_o)
-    dist.all_to_all_single(recv_l, send_l)
-    mo, ml = oracle.merge_lse(recv_o.numpy(), recv_l.numpy())  # [B, 1, hs, D]: this rank's heads
+
+    def partial(qs, ks, vs, sl, k_scale, v_scale, scale, scale_block, out_o, out_l):  # the oracle as the attention
+        o, lse = oracle.split_attention(qs.numpy(), ks.numpy(), vs.numpy(), sl.tolist(), [[0, m]] * B, NO_CAUSAL,
+                                        scale)
+        out_o.copy_(torch.from_numpy(o))
+        out_l.copy_(torch.from_numpy(lse))
+
+    def merge(o, lse):
+        mo, ml = oracle.merge_lse(o.numpy(), lse.numpy())
+        return torch.from_numpy(mo), torch.from_numpy(ml)
+
+    # the package's exchange step: partials straight into the All-to-All send buffer, one
+    # slab per destination rank, then the exchange and the merge of this rank's heads
+    mo, ml, (send_o, send_l, _, _) = kvp.kvp_decode_step(
+        torch.from_numpy(q), torch.from_numpy(np.ascontiguousarray(k_loc)), torch.from_numpy(np.ascontiguousarray(v_loc)),
+        torch.tensor(lens_loc, dtype=torch.int32), softmax_scale=SCALE, partial=partial, merge=merge)
+    # the send buffer's slabs side by side over the head axis: this rank's partial of every head
+    o = np.concatenate([send_o[s].numpy() for s in range(N_RANKS)], axis=2)
+    lse = np.concatenate([send_l[s].numpy() for s in range(N_RANKS)], axis=2)
     dist.barrier()
     dist.destroy_process_group()
-    out_q.put((rank, o, lse, mo, ml))
+    out_q.put((rank, o, lse, mo.numpy(), ml.numpy()))
 
 
 def _passkv_worker(rank, port, layout, out_q):
@@ -183,3 +195,17 @@ def test_two_rank_passkv_ring_prefill(layout):
         assert sources == [(rank - s) % N_RANKS for s in range(N_RANKS)]
         assert np.allclose(o, ro[:, my_pos], atol=1e-12, rtol=0)
         assert np.allclose(lse, rl[:, my_pos], atol=1e-12, rtol=0)
+
+
+def test_head_slabs_cover_whole_groups_or_lie_inside_one():
+    sys.path.insert(0, ROOT)
+    from mla_decode_attention_gqa_gb300 import kvp
+
+    # Helix dense decode on 8 ranks: one KV head (16 query heads) per rank
+    assert kvp.head_slabs(128, 8, 8) == [((16 * s, 16 * s + 16), (s, s + 1)) for s in range(8)]
+    # 2 ranks: four KV heads per slab
+    assert kvp.head_slabs(128, 8, 2) == [((0, 64), (0, 4)), ((64, 128), (4, 8))]
+    # the MLA latent (one KV head) on 8 ranks: every slab inside the one group
+    assert kvp.head_slabs(128, 1, 8)[3] == ((48, 64), (0, 1))
+    with pytest.raises(ValueError):
+        kvp.head_slabs(24, 8, 12)  # groups of 3 heads, slabs of 2: a slab would straddle two groups

@@ -63,13 +63,15 @@ def test_mla_absorbed_full_size_sampled():
                                    softmax_scale=w.scale)
     torch.cuda.synchronize()
     assert skv.device_error() == 0
-    for b in (0, 15):
+    worst = 0.0
+    for b in range(w.B):  # every sequence (the chunk planner spreads them over waves)
         ro_p, rl_p = io.oracle_rows(inp, w, b, 0, [0])
         ro, rl = oracle.merge_lse(ro_p, rl_p)
         io.assert_close(out[b, [0]], lse[b, [0]], ro, rl, io.TOL_BF16, f"b={b}")
         rel = io.rel_rms_err(out[b, [0]], ro)
-        print(f"{w.name} b={b}: max-abs err / RMS(out) = {rel:.3e}")
+        worst = max(worst, rel)
         assert rel <= io.REL_RMS_BAR, f"b={b}: err / RMS {rel:.3e} > {io.REL_RMS_BAR}"
+    print(f"{w.name}: {w.B} sequences checked, largest err / RMS(out) {worst:.3e}")
 
 
 def test_mla_64_heads_half_row_tile():

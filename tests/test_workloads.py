@@ -80,3 +80,20 @@ def test_kvp_shards_cut_the_allocated_length_into_equal_parts():
     assert len(bounds) == w.B and all(row == bounds[0] for row in bounds)
     assert bounds[0] == [j * w.S // w.n_split for j in range(w.n_split + 1)]
     assert w.n_split == 8 and w.S == 1 << 20
+
+
+def test_table_dequantiser_of_the_parity_helpers_equals_the_oracle():
+    """tests/oracle_io.dequant_fp8_rows (the oracle's 256 code values, gathered) gives the
+    same float64 values as oracle.dequant_e4m3_blocks, NaN codes included."""
+    import numpy as np
+
+    import oracle
+    from tests import oracle_io as io
+
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 256, size=(1000, 64), dtype=np.uint8)
+    scales = rng.random(1000 // 64 + 1) * 3
+    a = io.dequant_fp8_rows(codes, scales, 64)
+    b = oracle.dequant_e4m3_blocks(codes, scales, 64)
+    assert np.array_equal(np.isnan(a), np.isnan(b))
+    assert np.array_equal(a[~np.isnan(a)], b[~np.isnan(b)])
