@@ -303,6 +303,35 @@ skv_status encode_kv_map(CUtensorMap* map, const void* base, const skv_desc* d, 
   return SKV_OK;
 }
 
+// The MLA latent [B][S_max][dk] viewed as (64 dims, token row, 64-dim slice, sequence): a
+// box of (64, rows, slices, 1) lands in shared memory as `slices` consecutive 128-byte-
+// swizzled [rows][64 dims] tiles, one copy for what would take rows/64 x slices boxes of the
+// plain view.  (The slice stride, 128 bytes, is below the token stride; the map only adds the
+// strides up per element.)
+skv_status encode_latent_slices_map(CUtensorMap* map, const void* base, const skv_desc* d, int box_rows,
+                                    int box_slices) {
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (!encode) return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
+  const int64_t row_b = d->k_strides[2] * 2;
+  int64_t seq_b = d->k_strides[0] * 2;
+  if (d->B == 1 || seq_b == 0) seq_b = std::max<int64_t>(seq_b, row_b * d->S_max);
+  cuuint64_t gdim[4] = {64, static_cast<cuuint64_t>(d->S_max), static_cast<cuuint64_t>(d->dk / 64),
+                        static_cast<cuuint64_t>(d->B)};
+  cuuint64_t gstride[3] = {static_cast<cuuint64_t>(row_b), 128, static_cast<cuuint64_t>(seq_b)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_slices), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim, gstride, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (latent slices) failed (CUresult %d)", static_cast<int>(r));
+    return fail(SKV_ECUDA, buf);
+  }
+  return SKV_OK;
+}
+
 // 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per row,
 // `outer` rows `row_bytes` apart, box of box_inner x box_outer.
 skv_status encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
@@ -450,15 +479,23 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
     if (use_mla_tc(d)) {
       // one latent map (64-dim x 64-token boxes) serves K and V; each CTA of the pair
       // loads its own slice of dims
-      CUtensorMap tmq;
+      CUtensorMap tmq, tmg, tmv2;
       if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
       if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, mla_tc_kv_tile(), pg)) != SKV_OK) return st;
+      if (pg) {  // paged: the per-slice map serves every load
+        tmg = tmk;
+        tmv2 = tmk;
+      } else {
+        if ((st = encode_latent_slices_map(&tmg, k, d, mla_tc_score_tile(), mla_tc_group_slices())) != SKV_OK)
+          return st;
+        if ((st = encode_latent_slices_map(&tmv2, k, d, mla_tc_kv_tile(), 8)) != SKV_OK) return st;
+      }
       TcAttnExtra x;
       x.fused = 0;
       x.out_bf16 = nullptr;
       x.out_lse = nullptr;
       e = timing_mark(false, stream);
-      if (e == cudaSuccess) e = launch_mla_tc(p, x, tmq, tmk, pl.n_items, stream);
+      if (e == cudaSuccess) e = launch_mla_tc(p, x, tmq, tmk, tmg, tmv2, pl.n_items, stream);
       if (e == cudaSuccess) e = timing_mark(true, stream);
       if (e != cudaSuccess) return cuda_fail(e, "MLA tensor-core attention launch");
       return SKV_OK;

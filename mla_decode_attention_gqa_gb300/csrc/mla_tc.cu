@@ -193,7 +193,8 @@ __device__ __forceinline__ void tile_coords(const PartialParams& p, int b, int t
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ TcAttnExtra x,
-                  const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tml) {
+                  const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tml,
+                  const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + kOffBar);
@@ -275,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // box bx (dims 64 bx ..) of every score tile sits in ring box slot bx; group g = boxes 3g .. 3g + 2
       if (lane == 0 && n_score > 0) {
         tma_prefetch_desc(&tmq);
-        tma_prefetch_desc(&tml);
+        tma_prefetch_desc(PAGED ? &tml : &tmg);
         mbar_arrive_expect_tx(&bars->q_full, kKBoxes * kQBoxBytes);
         const int t_start = m0 / p.G;
         for (int bx = 0; bx < kKBoxes; ++bx)
@@ -294,11 +295,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&bars->grp_full[g], kGrp * kSBoxBytes);
-            for (int e = 0; e < kGrp; ++e) {
-              const int bx = g * kGrp + e;
-              uint8_t* st = smem + bx * kSBoxBytes;
-              tma_load_4d_plain(st, &tml, &bars->grp_full[g], bx * 64, row0, 0, outer0);
-              tma_load_4d_plain(st + kBoxBytes, &tml, &bars->grp_full[g], bx * 64, row1, 0, outer1);
+            if constexpr (!PAGED) {
+              // the group's three 64-dim slices of the tile's 128 tokens in one copy: the
+              // chunked view's box lands as [slice][token][128 B], the ring's own layout
+              tma_load_4d_plain(smem + g * kGrp * kSBoxBytes, &tmg, &bars->grp_full[g], 0, row0, g * kGrp, outer0);
+            } else {
+              for (int e = 0; e < kGrp; ++e) {
+                const int bx = g * kGrp + e;
+                uint8_t* st = smem + bx * kSBoxBytes;
+                tma_load_4d_plain(st, &tml, &bars->grp_full[g], bx * 64, row0, 0, outer0);
+                tma_load_4d_plain(st + kBoxBytes, &tml, &bars->grp_full[g], bx * 64, row1, 0, outer1);
+              }
             }
             ++issued;
           }
@@ -527,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0 && n_tiles > 0) {
-        tma_prefetch_desc(&tml);
+        tma_prefetch_desc(PAGED ? &tml : &tmv);
         int outer = b, row_c = 0;
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
@@ -537,8 +544,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tile_coords<PAGED>(p, b, (tile_begin + i) * kTN, &outer, &row_c);
           mbar_arrive_expect_tx(&bars->kv_full1[s], kStage1Bytes);
           uint8_t* st = smem + s * kStage1Bytes;
-          for (int bx = 0; bx < kVBoxes; ++bx)
-            tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row_c, 0, outer);
+          if constexpr (!PAGED) {  // the tile's eight 64-dim slices in one copy
+            tma_load_4d_plain(st, &tmv, &bars->kv_full1[s], 0, row_c, 0, outer);
+          } else {
+            for (int bx = 0; bx < kVBoxes; ++bx)
+              tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row_c, 0, outer);
+          }
           issued = i + 1;
         }
         for (int i = max(0, issued - kNStage1); i < issued; ++i) {
@@ -737,9 +748,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 int mla_tc_rows_per_item() { return kRows; }
 int mla_tc_kv_tile() { return kTN; }
+int mla_tc_score_tile() { return kTS; }
+int mla_tc_group_slices() { return kGrp; }
 
 cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
-                          const CUtensorMap& tml, int64_t n_items, cudaStream_t stream) {
+                          const CUtensorMap& tml, const CUtensorMap& tmg, const CUtensorMap& tmv, int64_t n_items,
+                          cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e0 = once_per_device(attr_done, [] {
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -750,9 +764,9 @@ cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CU
   if (e0 != cudaSuccess) return e0;
   if (n_items <= 0) return cudaSuccess;
   if (p.block_table)
-    mla_tc_kernel<true><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);
+    mla_tc_kernel<true><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml, tmg, tmv);
   else
-    mla_tc_kernel<false><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml);
+    mla_tc_kernel<false><<<static_cast<unsigned int>(2 * n_items), kThreads, kSmem, stream>>>(p, x, tmq, tml, tmg, tmv);
   return cudaGetLastError();
 }
 

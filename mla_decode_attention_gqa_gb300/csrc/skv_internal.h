@@ -149,10 +149,16 @@ cudaError_t launch_tc_attn(const PartialParams& p, const TcAttnExtra& x, const C
 
 // Tensor-core MLA latent attention (see mla_tc.cu): a cluster pair per work item of the
 // partial decomposition (b, split j, chunk c, 128-row tile), writing fp32 partials.
+// tml: the latent as (dim, token row, head, sequence | page) with 64 x kv_tile boxes;
+// tmg / tmv (contiguous caches): the latent's chunked view (64 dims, token row, 64-dim
+// slice, sequence) with boxes of (64, score tile, group slices) and (64, kv tile, 8).
 int mla_tc_rows_per_item();
 int mla_tc_kv_tile();
+int mla_tc_score_tile();
+int mla_tc_group_slices();
 cudaError_t launch_mla_tc(const PartialParams& p, const TcAttnExtra& x, const CUtensorMap& tmq,
-                          const CUtensorMap& tml, int64_t n_items, cudaStream_t stream);
+                          const CUtensorMap& tml, const CUtensorMap& tmg, const CUtensorMap& tmv, int64_t n_items,
+                          cudaStream_t stream);
 
 // tcgen05 self-test GEMM (see umma_selftest.cu).
 cudaError_t launch_umma_selftest(const CUtensorMap& ta, const CUtensorMap& tb, float* C, int N, bool b_mn_major,
