@@ -494,6 +494,11 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
       x.fused = 0;
       x.out_bf16 = nullptr;
       x.out_lse = nullptr;
+      if (!pg) {
+        x.kv = static_cast<const uint8_t*>(k);
+        x.kv_seq_bytes = d->k_strides[0] * 2;
+        x.kv_tok_bytes = d->k_strides[2] * 2;
+      }
       e = timing_mark(false, stream);
       if (e == cudaSuccess) e = launch_mla_tc(p, x, tmq, tmk, tmg, tmv2, pl.n_items, stream);
       if (e == cudaSuccess) e = timing_mark(true, stream);

@@ -64,6 +64,7 @@ constexpr int kOffQRope = 198656;  // Q dims 512..575 (the rope part), 16 KB, ke
 constexpr int kQTmemBoxes = 8;     // Q dims 0..511 live in TMEM
 // CTA 1 (values): a 3-stage ring of 512-dim tiles, P / factor / row-sum receive buffers
 constexpr int kNStage1 = 3;
+constexpr int kPfAhead = 6;  // value tiles (64 tokens) between CTA 1's load and its L2 prefetch
 constexpr int kStage1Bytes = kVBoxes * kBoxBytes;  // 64 KB
 constexpr int kOffPRecv = kNStage1 * kStage1Bytes;  // 192 KB
 constexpr int kOffARecv = kOffPRecv + 2 * kPBytes;
@@ -546,6 +547,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * kStage1Bytes;
           if constexpr (!PAGED) {  // the tile's eight 64-dim slices in one copy
             tma_load_4d_plain(st, &tmv, &bars->kv_full1[s], 0, row_c, 0, outer);
+            // this CTA's copy engine warms L2 with a coming score tile of CTA 0 (whose own
+            // engine is the busier one): the item's own tokens only
+            const int pf_tok = (tile_begin + i + kPfAhead) * kTN;
+            if ((i & 1) == 0 && x.kv != nullptr && pf_tok < r_hi) {
+              const int n = min(kTS, r_hi - pf_tok);
+              const uint8_t* src = x.kv + b * x.kv_seq_bytes + static_cast<int64_t>(pf_tok) * x.kv_tok_bytes;
+              const uint32_t bytes = static_cast<uint32_t>((n - 1) * x.kv_tok_bytes + kKBoxes * 128);
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                           "r"(bytes)
+                           : "memory");
+            }
           } else {
             for (int bx = 0; bx < kVBoxes; ++bx)
               tma_load_4d_plain(st + bx * kBoxBytes, &tml, &bars->kv_full1[s], bx * 64, row_c, 0, outer);

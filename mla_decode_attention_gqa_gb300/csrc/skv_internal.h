@@ -141,6 +141,10 @@ struct TcAttnExtra {
   // partial mode with one split: merge the result into the running (out_o, out_lse) held
   // there already instead of overwriting it (a pass-KV ring step)
   int32_t accumulate = 0;
+  // MLA over a contiguous latent: its base and byte strides (sequence, token), for the value
+  // CTA's L2 prefetches of the score CTA's coming tiles (NULL: none)
+  const uint8_t* kv = nullptr;
+  int64_t kv_seq_bytes = 0, kv_tok_bytes = 0;
 };
 int tc_attn_rows_per_cta();
 int tc_attn_kv_tile();  // tokens per K/V tile = rows of the K/V tensor-map box
