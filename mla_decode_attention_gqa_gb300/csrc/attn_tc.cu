@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = fast_exp2(a1);
           ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
           pk[16 * cc + e] = pack_bf16(p0, p1);
-          lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(pk[16 * cc + e]), bf16_hi(pk[16 * cc + e]));
+          lr[e & 1] = add_bf16x2_f32x2(lr[e & 1], pk[16 * cc + e]);
         }
       }
       // Redo when this is the row's first visible tile, or when its p grew past the limit
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = fast_exp2(fmaf(v1, sl, -base));
             ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
             w[e] = pack_bf16(p0, p1);
-            lr[e & 1] = add_f32x2(lr[e & 1], bf16_lo(w[e]), bf16_hi(w[e]));
+            lr[e & 1] = add_bf16x2_f32x2(lr[e & 1], w[e]);
           }
           tc::tmem_st16(s_col + 16 * cc, w);  // S columns 32cc.. were read before P 16cc.. is written
         }

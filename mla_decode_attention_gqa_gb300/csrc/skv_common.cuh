@@ -213,6 +213,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// The same sums of a packed pair's two rounded values without unpacking it: the
+// mixed-precision adds (fp32 accumulator + bf16 operand, widened exactly, one IEEE round-
+// to-nearest add each) take the pair's halves directly, so the result equals
+// add_f32x2(acc, bf16_lo(w), bf16_hi(w)) bit for bit, with no integer shift / mask on the
+// ALU pipe that the softmax loops saturate.
+__device__ __forceinline__ uint64_t add_bf16x2_f32x2(uint64_t acc, uint32_t w) {
+  uint64_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 x, y;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\tmov.b64 {x, y}, %1;\n\t"
+      "add.rn.f32.bf16 x, lo, x;\n\tadd.rn.f32.bf16 y, hi, y;\n\t"
+      "mov.b64 %0, {x, y};\n\t}"
+      : "=l"(r)
+      : "l"(acc), "r"(w));
+  return r;
+}
+
 // Two running fp32 sums in one 64-bit register, advanced by one packed add (two IEEE
 // round-to-nearest adds in one instruction): the softmax row sums take one instruction per
 // pair of columns.
