@@ -477,8 +477,9 @@ skv_status run_partial(const skv_desc* d, const Plan& pl, const void* q, const v
   if (pl.mla) {
     if (q_pos) return fail(SKV_EUNSUPPORTED, "position-masked attention is not supported for the MLA latent shape");
     if (use_mla_tc(d)) {
-      // one latent map (64-dim x 64-token boxes) serves K and V; each CTA of the pair
-      // loads its own slice of dims
+      // the latent is both K (all 576 dims) and V (its first 512): a per-slice map with
+      // 64-dim x 64-token boxes, and over a contiguous cache the chunked view that lets one
+      // copy land a whole score group (CTA 0) or value tile (CTA 1)
       CUtensorMap tmq, tmg, tmv2;
       if ((st = encode_q_map(&tmq, q, d)) != SKV_OK) return st;
       if ((st = encode_kv_map(&tmk, k, d, d->k_strides, d->dk, mla_tc_kv_tile(), pg)) != SKV_OK) return st;
