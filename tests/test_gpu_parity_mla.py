@@ -55,6 +55,20 @@ def test_mla_ragged_lengths_with_nan_past_the_end():
     _all_paths(w, inp)
 
 
+def test_mla_strided_latent_view():
+    """The latent as a view into a NaN-filled buffer with padded token rows (640 elements)
+    and 64 spare rows per sequence: the tensor maps (the chunked view that lands a whole score
+    group or value tile in one copy included) and the L2 prefetch address rows by the cache's
+    own strides, so a read outside the view would put NaN into the output."""
+    w = W.scaled(W.MLA_ABSORBED, B=2, S=1024, n_split=2)
+    inp = W.make_inputs(w, DEV)
+    big = torch.full((w.B, 1, w.S + 64, 640), float("nan"), dtype=torch.bfloat16, device=DEV)
+    big[:, :, :w.S, :576] = inp["k"]
+    view = big[:, :, :w.S, :576]
+    assert not view.is_contiguous()
+    _all_paths(w, dict(inp, k=view, v=view[..., :512]))
+
+
 @pytest.mark.slow
 def test_mla_absorbed_full_size_sampled():
     w = W.MLA_ABSORBED  # B=16, Hq=128, latent 576 (V 512), S=32768, 4 splits
