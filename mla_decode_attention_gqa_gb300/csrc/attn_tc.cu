@@ -41,6 +41,14 @@ namespace skv {
 
 namespace {
 
+// The softmax pass's mask mode: a run-time flag, or a compile-time one (std::true_type /
+// std::false_type) that removes the test from the unrolled column loop.
+__device__ __forceinline__ bool mask_on(bool m) { return m; }
+template <bool B>
+__device__ __forceinline__ constexpr bool mask_on(std::integral_constant<bool, B>) {
+  return B;
+}
+
 constexpr int kD = 128;         // dk = dv
 constexpr int kTN = 128;        // tokens per K/V tile
 constexpr int kNStage = 2;      // K/V ring depth
@@ -446,31 +454,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
       uint64_t lr[2] = {0ull, 0ull};  // the same of the bf16-rounded p
       const float base0 = (m_used == -INFINITY) ? 0.f : m_used;
+      // masked: a bool, or (contiguous mode) a compile-time constant, one instantiation per
+      // mask mode (need_mask is warp-uniform), so that the tiles away from the diagonal and
+      // the split ends -- nearly all of them -- carry no per-column visibility test.  (Position
+      // mode keeps the run-time test: two copies of its pass spilled registers.)
+      auto pass = [&](auto masked) {
 #pragma unroll
-      for (int cc = 0; cc < kTN / 32; ++cc) {
-        uint32_t r[2][16];
-        tc::tmem_ld16(s_col + 32 * cc, r[0]);
-        tc::tmem_ld16(s_col + 32 * cc + 16, r[1]);
-        tc::tmem_wait_ld();
+        for (int cc = 0; cc < kTN / 32; ++cc) {
+          uint32_t r[2][16];
+          tc::tmem_ld16(s_col + 32 * cc, r[0]);
+          tc::tmem_ld16(s_col + 32 * cc + 16, r[1]);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = 32 * cc + 2 * e;
-          float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
-          float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
-          if (need_mask) {
-            v0 = visible(col) ? v0 : -INFINITY;
-            v1 = visible(col + 1) ? v1 : -INFINITY;
+          for (int e = 0; e < 16; ++e) {
+            const int col = 32 * cc + 2 * e;
+            float v0 = __uint_as_float(r[e >> 3][(2 * e) & 15]);
+            float v1 = __uint_as_float(r[e >> 3][(2 * e + 1) & 15]);
+            if (mask_on(masked)) {
+              v0 = visible(col) ? v0 : -INFINITY;
+              v1 = visible(col + 1) ? v1 : -INFINITY;
+            }
+            // pairwise: one packed FMA and packed adds per column pair
+            float a0, a1;
+            fma_pair(v0, v1, sl, -base0, a0, a1);
+            const float p0 = fast_exp2(a0);
+            const float p1 = fast_exp2(a1);
+            ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
+            pk[16 * cc + e] = pack_bf16(p0, p1);
+            lr[e & 1] = add_bf16x2_f32x2(lr[e & 1], pk[16 * cc + e]);
           }
-          // pairwise: one packed FMA and packed adds per column pair
-          float a0, a1;
-          fma_pair(v0, v1, sl, -base0, a0, a1);
-          const float p0 = fast_exp2(a0);
-          const float p1 = fast_exp2(a1);
-          ls[e & 1] = add_f32x2(ls[e & 1], p0, p1);
-          pk[16 * cc + e] = pack_bf16(p0, p1);
-          lr[e & 1] = add_bf16x2_f32x2(lr[e & 1], pk[16 * cc + e]);
         }
-      }
+      };
+      if constexpr (POS)
+        pass(need_mask);
+      else if (need_mask)
+        pass(std::true_type{});
+      else
+        pass(std::false_type{});
       // Redo when this is the row's first visible tile, or when its p grew past the limit
       // (then some score rose far above m_used; every p <= the tile sum <= 2^16 otherwise).
       const float tile_sum = sum_f32x2(ls[0]) + sum_f32x2(ls[1]);
