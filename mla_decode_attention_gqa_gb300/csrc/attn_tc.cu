@@ -41,9 +41,8 @@ namespace skv {
 
 namespace {
 
-// The softmax pass's mask mode: a run-time flag, or a compile-time one (std::true_type /
-// std::false_type) that removes the test from the unrolled column loop.
-__device__ __forceinline__ bool mask_on(bool m) { return m; }
+// The softmax pass's mask mode, a compile-time flag (std::true_type / std::false_type): the
+// unmasked instantiation has no test in its unrolled column loop.
 template <bool B>
 __device__ __forceinline__ constexpr bool mask_on(std::integral_constant<bool, B>) {
   return B;
@@ -454,10 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t ls[2] = {0ull, 0ull};  // fp32 pair sums of p (0 bits = +0.0f)
       uint64_t lr[2] = {0ull, 0ull};  // the same of the bf16-rounded p
       const float base0 = (m_used == -INFINITY) ? 0.f : m_used;
-      // masked: a bool, or (contiguous mode) a compile-time constant, one instantiation per
-      // mask mode (need_mask is warp-uniform), so that the tiles away from the diagonal and
-      // the split ends -- nearly all of them -- carry no per-column visibility test.  (Position
-      // mode keeps the run-time test: two copies of its pass spilled registers.)
+      // masked: a compile-time constant, one instantiation per mask mode (need_mask is warp-
+      // uniform), so that the tiles away from the diagonal and the split ends -- nearly all of
+      // them -- carry no per-column visibility test (in position mode the two copies spill a
+      // few registers and are still faster)
       auto pass = [&](auto masked) {
 #pragma unroll
         for (int cc = 0; cc < kTN / 32; ++cc) {
@@ -485,9 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if constexpr (POS)
-        pass(need_mask);
-      else if (need_mask)
+      if (need_mask)
         pass(std::true_type{});
       else
         pass(std::false_type{});
