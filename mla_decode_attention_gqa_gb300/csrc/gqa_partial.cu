@@ -38,6 +38,8 @@
 //     the K block scale multiplies the score and the V block scale multiplies p.
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "skv_common.cuh"
 #include "skv_internal.h"
 
@@ -427,22 +429,32 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const bool in_range = (t0s >= r_lo) && (t0s + NS <= r_hi);
     const bool need_mask = POS || !in_range || (static_cast<int64_t>(t0s) + NS - 1 > hz_min);
     float tmax[2] = {-INFINITY, -INFINITY};
+    // fp8: one instantiation per mask mode (need_mask is warp-uniform; written as one loop
+    // with the test inside, the compiler evaluated it on every tile, and the fp8 decode does
+    // twice the arithmetic per byte of the bf16 one).  bf16 keeps the single masked loop: its
+    // kernel time moved by under 1 % either way.
+    auto scale_mask = [&](auto masked) {
 #pragma unroll
-    for (int nt = 0; nt < NS / 8; ++nt) {
+      for (int nt = 0; nt < NS / 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = sc[nt][e] * sl;
-        if (need_mask) {
-          const int tok = t0s + 8 * nt + 2 * tq + (e & 1);
-          const int64_t hz = (e < 2) ? hz0 : hz1;
-          bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
-          if constexpr (POS) ok = ok && __ldg(kpos_b + tok) <= ((e < 2) ? qp0 : qp1);
-          x = ok ? x : -INFINITY;
+        for (int e = 0; e < 4; ++e) {
+          float x = sc[nt][e] * sl;
+          if constexpr (decltype(masked)::value) {
+            const int tok = t0s + 8 * nt + 2 * tq + (e & 1);
+            const int64_t hz = (e < 2) ? hz0 : hz1;
+            bool ok = tok >= r_lo && tok < r_hi && static_cast<int64_t>(tok) <= hz;
+            if constexpr (POS) ok = ok && __ldg(kpos_b + tok) <= ((e < 2) ? qp0 : qp1);
+            x = ok ? x : -INFINITY;
+          }
+          sc[nt][e] = x;
+          tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
         }
-        sc[nt][e] = x;
-        tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
       }
-    }
+    };
+    if (!C::FP8 || need_mask)
+      scale_mask(std::true_type{});
+    else
+      scale_mask(std::false_type{});
     float base[2], alpha[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -499,13 +511,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
       }
     }
 
-    // ---- O += P V
+    // ---- O += P V (the masks of V rows outside [r_lo, r_hi): as for the scores, fp8 keeps
+    // them out of the instantiation for tiles that need none)
     const bool vmask = !in_range;
+    auto pv = [&](auto vmasked) {
 #pragma unroll
     for (int kk = 0; kk < NS / 16; ++kk) {
       if constexpr (!C::FP8) {
         uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-        if (vmask) {
+        if constexpr (decltype(vmasked)::value) {
           const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
           mlo = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
           mhi = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
@@ -516,8 +530,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
           const uint32_t byte = (2 * dp + (mi >> 1)) * 16;
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
-          mma_bf16(o[2 * dp], pa[kk], r0 & mlo, r1 & mhi);
-          mma_bf16(o[2 * dp + 1], pa[kk], r2 & mlo, r3 & mhi);
+          if constexpr (decltype(vmasked)::value) {
+            r0 &= mlo, r1 &= mhi, r2 &= mlo, r3 &= mhi;
+          }
+          mma_bf16(o[2 * dp], pa[kk], r0, r1);
+          mma_bf16(o[2 * dp + 1], pa[kk], r2, r3);
         }
       } else {
         // O^T[dv x rows] += V^T[dv x tok] P^T[tok x rows]: ldmatrix.trans of the e4m3 tile
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         // 16-dv chunk c are dv 16c+2gq / 16c+2gq+1, and P's fragments are already the B
         // operand (columns = the 16 rows).
         uint32_t m0 = 0xFFFFFFFFu, m1 = 0xFFFFFFFFu;
-        if (vmask) {
+        if constexpr (decltype(vmasked)::value) {
           const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
           m0 = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
           m1 = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
@@ -538,13 +555,21 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
           uint32_t r0, r1;
           ldsm_x2_t(vbase + tile_off<C>(tok, cc * 16), r0, r1);
           uint32_t a[4];
-          e4m3x4_to_f16x2x2(prmt(r0 & m0, 0u, 0x3120u), a[0], a[1]);
-          e4m3x4_to_f16x2x2(prmt(r1 & m1, 0u, 0x3120u), a[2], a[3]);
+          if constexpr (decltype(vmasked)::value) {
+            r0 &= m0, r1 &= m1;
+          }
+          e4m3x4_to_f16x2x2(prmt(r0, 0u, 0x3120u), a[0], a[1]);
+          e4m3x4_to_f16x2x2(prmt(r1, 0u, 0x3120u), a[2], a[3]);
           mma_f16(o[2 * cc], a, b00, b01);
           mma_f16(o[2 * cc + 1], a, b10, b11);
         }
       }
     }
+    };
+    if (!C::FP8 || vmask)
+      pv(std::true_type{});
+    else
+      pv(std::false_type{});
     }  // sub-steps
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
