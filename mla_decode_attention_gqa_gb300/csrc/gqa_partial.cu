@@ -516,55 +516,55 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const bool vmask = !in_range;
     auto pv = [&](auto vmasked) {
 #pragma unroll
-      for (int kk = 0; kk < NS / 16; ++kk) {
-        if constexpr (!C::FP8) {
-          uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-          if constexpr (decltype(vmasked)::value) {
-            const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
-            mlo = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
-            mhi = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
-          }
+    for (int kk = 0; kk < NS / 16; ++kk) {
+      if constexpr (!C::FP8) {
+        uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+        if constexpr (decltype(vmasked)::value) {
+          const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
+          mlo = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
+          mhi = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
+        }
 #pragma unroll
-          for (int dp = 0; dp < D / 16; ++dp) {
-            const uint32_t tok = tb + 16 * kk + (mi & 1) * 8 + (lane & 7);
-            const uint32_t byte = (2 * dp + (mi >> 1)) * 16;
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4_t(vbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
-            if constexpr (decltype(vmasked)::value) {
-              r0 &= mlo, r1 &= mhi, r2 &= mlo, r3 &= mhi;
-            }
-            mma_bf16(o[2 * dp], pa[kk], r0, r1);
-            mma_bf16(o[2 * dp + 1], pa[kk], r2, r3);
-          }
-        } else {
-          // O^T[dv x rows] += V^T[dv x tok] P^T[tok x rows]: ldmatrix.trans of the e4m3 tile
-          // (16-bit view) gives each lane bytes V[2tq][2gq], V[2tq][2gq+1], V[2tq+1][2gq],
-          // V[2tq+1][2gq+1]; one byte permute pairs them by dv, so the A rows gq / gq+8 of a
-          // 16-dv chunk c are dv 16c+2gq / 16c+2gq+1, and P's fragments are already the B
-          // operand (columns = the 16 rows).
-          uint32_t m0 = 0xFFFFFFFFu, m1 = 0xFFFFFFFFu;
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const uint32_t tok = tb + 16 * kk + (mi & 1) * 8 + (lane & 7);
+          const uint32_t byte = (2 * dp + (mi >> 1)) * 16;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vbase + tile_off<C>(tok, byte), r0, r1, r2, r3);
           if constexpr (decltype(vmasked)::value) {
-            const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
-            m0 = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
-            m1 = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
+            r0 &= mlo, r1 &= mhi, r2 &= mlo, r3 &= mhi;
           }
-          const uint32_t b00 = pa[kk][0], b01 = pa[kk][2], b10 = pa[kk][1], b11 = pa[kk][3];
+          mma_bf16(o[2 * dp], pa[kk], r0, r1);
+          mma_bf16(o[2 * dp + 1], pa[kk], r2, r3);
+        }
+      } else {
+        // O^T[dv x rows] += V^T[dv x tok] P^T[tok x rows]: ldmatrix.trans of the e4m3 tile
+        // (16-bit view) gives each lane bytes V[2tq][2gq], V[2tq][2gq+1], V[2tq+1][2gq],
+        // V[2tq+1][2gq+1]; one byte permute pairs them by dv, so the A rows gq / gq+8 of a
+        // 16-dv chunk c are dv 16c+2gq / 16c+2gq+1, and P's fragments are already the B
+        // operand (columns = the 16 rows).
+        uint32_t m0 = 0xFFFFFFFFu, m1 = 0xFFFFFFFFu;
+        if constexpr (decltype(vmasked)::value) {
+          const int ta = t0s + 16 * kk + 2 * tq, tb2 = ta + 8;
+          m0 = half_mask(ta >= r_lo && ta < r_hi, ta + 1 >= r_lo && ta + 1 < r_hi);
+          m1 = half_mask(tb2 >= r_lo && tb2 < r_hi, tb2 + 1 >= r_lo && tb2 + 1 < r_hi);
+        }
+        const uint32_t b00 = pa[kk][0], b01 = pa[kk][2], b10 = pa[kk][1], b11 = pa[kk][3];
 #pragma unroll
-          for (int cc = 0; cc < D / 16; ++cc) {
-            const uint32_t tok = tb + 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
-            uint32_t r0, r1;
-            ldsm_x2_t(vbase + tile_off<C>(tok, cc * 16), r0, r1);
-            uint32_t a[4];
-            if constexpr (decltype(vmasked)::value) {
-              r0 &= m0, r1 &= m1;
-            }
-            e4m3x4_to_f16x2x2(prmt(r0, 0u, 0x3120u), a[0], a[1]);
-            e4m3x4_to_f16x2x2(prmt(r1, 0u, 0x3120u), a[2], a[3]);
-            mma_f16(o[2 * cc], a, b00, b01);
-            mma_f16(o[2 * cc + 1], a, b10, b11);
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const uint32_t tok = tb + 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
+          uint32_t r0, r1;
+          ldsm_x2_t(vbase + tile_off<C>(tok, cc * 16), r0, r1);
+          uint32_t a[4];
+          if constexpr (decltype(vmasked)::value) {
+            r0 &= m0, r1 &= m1;
           }
+          e4m3x4_to_f16x2x2(prmt(r0, 0u, 0x3120u), a[0], a[1]);
+          e4m3x4_to_f16x2x2(prmt(r1, 0u, 0x3120u), a[2], a[3]);
+          mma_f16(o[2 * cc], a, b00, b01);
+          mma_f16(o[2 * cc + 1], a, b10, b11);
         }
       }
+    }
     };
     if (!C::FP8 || vmask)
       pv(std::true_type{});
